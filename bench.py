@@ -1,0 +1,368 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged latent-cache attention path on GB300.
+
+One step is one pass of the whole path over one batch of synthetic input that
+is already resident in HBM: per cache, append each stream's current rows
+(tf_paged_append) and attend over its pages (tf_paged_mla_attend); for the
+full-model workload, then copy a kept state's first `at` rows
+(tf_state_copy_rows).  The default workload is the decode batch (8 streams,
+64 heads, lengths U[4,096, 65,536], streams 0-3 sharing 16 pages).
+
+Prints ONE JSON line (rank 0).  With --gpus N > 1 (torchrun), every rank runs an
+independent replica of the workload on its own GPU ("replicas only": the path
+has no exchange step), value = the units of all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = ["decode_batch", "tiny_decode", "long_window", "prefill_100k", "prefill_208k", "full_model"]
+METRIC = "paged MLA decode KV GB/s + tokens/s vs HBM roofline; prefill TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=WORKLOADS, default="decode_batch")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def make_workload(name):
+    from paged_mla_kv_gb300 import synth as Y
+    return Y.WORKLOADS[name]()
+
+
+def step_units(w):
+    """Algorithmic work of one step: bytes, flops, tokens."""
+    from paged_mla_kv_gb300 import synth as Y
+    S, R, H, C = w.S, w.R, w.H, w.num_caches
+    kv = int(np.sum(w.lens)) * Y.ROW_BYTES
+    q = S * R * H * Y.DK * 2
+    out = S * R * H * (512 * 2 + 4)
+    app = 2 * S * R * Y.ROW_BYTES
+    attend_bytes = kv + q + out
+    at = int(w.extra.get("at", 0))
+    copy = 2 * at * Y.ROW_BYTES * C
+    pairs = 0
+    for s in range(S):
+        L = int(w.lens[s])
+        pairs += sum(L - R + r + 1 for r in range(R)) if R <= 4096 else 0
+    flops = 2 * (Y.DK + 512) * H * pairs * C
+    return dict(bytes=C * (attend_bytes + app) + copy, attend_bytes=attend_bytes, flops=flops,
+                attend_flops=flops // C, tokens=S * R if R <= 2 else S * R, kv=kv)
+
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index, self.rows, self.proc, self.th = index, [], None, None
+
+    def start(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+
+        def rd():
+            for line in self.proc.stdout:
+                self.rows.append([x.strip() for x in line.split(",")])
+        self.th = threading.Thread(target=rd, daemon=True)
+        self.th.start()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=2)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                pass
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_rate(w, seconds: float):
+    """Time the oracle, as it stands, on a bounded sample of the workload.
+
+    The sample is the first k heads of every stream (all query rows), k chosen so
+    the run takes about `seconds`; the rate is reported as KV bytes a second
+    (a stream's rows count once for all its heads, scaled by k / H)."""
+    from oracle import attend as OA
+    threads = os.cpu_count() or 1
+    qall = w.q(0)
+    rows = [w.stream_rows(0, s) for s in range(w.S)]
+
+    def run(k):
+        t0 = time.perf_counter()
+        nbytes = 0.0
+        for s in range(w.S):
+            items = np.array([r * w.H + h for r in range(w.R) for h in range(k)], np.int32)
+            OA.attend_stream(qall[s], rows[s][0], rows[s][1], w.scale, items, threads)
+            nbytes += int(w.lens[s]) * 1152 * k / w.H
+        return time.perf_counter() - t0, nbytes
+
+    t1, _ = run(1)
+    k = int(max(1, min(w.H, seconds / max(t1, 1e-3))))
+    t, nbytes = run(k)
+    return dict(value=nbytes / t / 1e9, unit="GB/s", cores=threads, kind="oracle",
+                sample=f"first {k} of {w.H} heads of all {w.S} streams, all {w.R} rows, cache 0 ({t:.1f} s)")
+
+
+def cpu_oracle_prefill_rate(w, seconds: float):
+    from oracle import attend as OA
+    threads = os.cpu_count() or 1
+    qall = w.q(0)
+    lat, rope = w.stream_rows(0, 0)
+    g = np.random.default_rng(0)
+    flops_per = lambda r: 2 * 1088 * (int(w.lens[0]) - w.R + r + 1)
+
+    def run(n):
+        rows = np.sort(g.choice(w.R, size=n, replace=False))
+        items = np.array([r * w.H + h for r in rows for h in range(w.H)], np.int32)
+        t0 = time.perf_counter()
+        OA.attend_stream(qall[0], lat, rope, w.scale, items, threads)
+        return time.perf_counter() - t0, sum(flops_per(r) for r in rows) * w.H, n
+
+    t1, _, _ = run(1)
+    n = int(max(1, min(w.R, seconds / max(t1, 1e-3))))
+    t, fl, n = run(n)
+    return dict(value=fl / t / 1e12, unit="TFLOP/s", cores=threads, kind="oracle",
+                sample=f"{n} of {w.R} query rows (all {w.H} heads), spread over the chunk ({t:.1f} s)")
+
+
+def reference_arm(args, rank, world):
+    """The oracle timed as the reference arm (host cores, bounded sample each step)."""
+    if rank != 0:
+        return
+    w = make_workload(args.workload)
+    prefill = w.R > 2
+    per_step = max(2.0, 120.0 / max(1, args.steps + args.warmup))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_oracle_prefill_rate(w, per_step) if prefill else cpu_oracle_rate(w, per_step)
+        if i >= args.warmup:
+            vals.append(r)
+    v = statistics.median(x["value"] for x in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": vals[0]["unit"], "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "S": w.S, "R": w.R, "H": w.H, "caches": w.num_caches},
+            "cpu_baseline": {"kind": "oracle", "cores": vals[0]["cores"], "sample": vals[0]["sample"], "value": v},
+            "e2e": {"value": v, "unit": vals[0]["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+    import torch
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    from paged_mla_kv_gb300 import binding as B
+    from paged_mla_kv_gb300 import build as BUILD
+    from paged_mla_kv_gb300.harness import Resident
+    BUILD.build()
+    peaks, peak_src = load_peaks()
+    w = make_workload(args.workload)
+    prefill = w.R > 2
+    units = step_units(w)
+    res = Resident(w, poison=True)
+    qs = [res.q(c) for c in range(w.num_caches)]
+    cur = [res.current_rows(c) for c in range(w.num_caches)]
+    out = torch.empty((w.S, w.R, w.H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.S, w.R, w.H), dtype=torch.float32, device="cuda")
+    ws = res.workspace()
+    at = int(w.extra.get("at", 0))
+    if at:
+        pages = -(-at // 512)
+        dst = torch.from_numpy(res.pool.take(pages)).cuda()
+        src = torch.from_numpy(res.pt_host[0, :pages].copy()).cuda()
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") \
+        if units["kv"] < 2 * L2_BYTES else None
+
+    def step(q_list=qs, rows=cur):
+        for c in range(w.num_caches):
+            res.append_current(c, rows[c][0], rows[c][1])
+            B.tf_paged_mla_attend(res.pool, c, res.pt, res.max_pages, res.lens, q_list[c], w.scale, out, lse, ws)
+        if at:
+            B.tf_state_copy_rows(res.pool, -1, src, dst, at)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if pg is not None:
+            pg.barrier()
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    res.pool.profile(True)
+    res.pool.profile_read(B.PROF_ATTEND)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    n0 = B.tf_launch_count()
+    barrier()
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        ev[i][0].record()
+        step()
+        ev[i][1].record()
+    barrier()
+    launches = B.tf_launch_count() - n0
+    total_ms = sum(a.elapsed_time(b) for a, b in ev)
+    att_ms, att_n = res.pool.profile_read(B.PROF_ATTEND)
+    res.pool.profile(False)
+    clocks = sampler.stop() if sampler else None
+    rc, detail = res.pool.last_error()
+    if rc != 0:
+        raise SystemExit(f"device error {rc} ({detail})")
+    if pg is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    if prefill:
+        value = world * units["flops"] / (ms / 1e3) / 1e12
+        unit = "TFLOP/s"
+    else:
+        value = world * units["bytes"] / (ms / 1e3) / 1e9
+        unit = "GB/s"
+    tokens_s = world * units["tokens"] / (ms / 1e3)
+
+    # roofline of the dominant kernel (the attention main pass), timed by events on its stream
+    avg_att = att_ms / max(att_n, 1)
+    if prefill:
+        achieved = units["attend_flops"] / (avg_att / 1e3) / 1e12
+        peak = peaks.get("bf16_tflops_sustained", 1700.0)
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None, "peak_kind": f"{peak_src} bf16 sustained", "kernel": "mla_attend_kernel",
+                "avg_launch_ms": avg_att}
+    else:
+        achieved = units["attend_bytes"] / (avg_att / 1e3) / 1e9
+        peak = peaks.get("hbm_gbs", 6800.0)
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None, "peak_kind": f"{peak_src} HBM copy", "kernel": "mla_attend_kernel",
+                "avg_launch_ms": avg_att}
+
+    # end to end through the C-ABI with host buffers: queries and new rows in, outputs out
+    e2e = None
+    if not args.no_e2e:
+        hq = [q.cpu().pin_memory() for q in qs]
+        hrows = [(a.cpu().pin_memory(), b.cpu().pin_memory()) for a, b in cur]
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        dq = [torch.empty_like(q) for q in qs]
+        drows = [(torch.empty_like(a), torch.empty_like(b)) for a, b in cur]
+
+        def e2e_step():
+            for c in range(w.num_caches):
+                dq[c].copy_(hq[c], non_blocking=True)
+                drows[c][0].copy_(hrows[c][0], non_blocking=True)
+                drows[c][1].copy_(hrows[c][1], non_blocking=True)
+            step(dq, drows)
+            hout.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        barrier()
+        e2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            e2[i][0].record()
+            e2e_step()
+            e2[i][1].record()
+        barrier()
+        e_ms = sum(a.elapsed_time(b) for a, b in e2) / args.steps
+        if pg is not None:
+            t = torch.tensor([e_ms], dtype=torch.float64, device="cuda")
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = sum(q.numel() * 2 for q in qs) + sum(a.numel() * 2 + b.numel() * 2 for a, b in cur)
+        d2h = out.numel() * 2 + lse.numel() * 4
+        ev_ = world * (units["flops"] / 1e12 if prefill else units["bytes"] / 1e9) / (e_ms / 1e3)
+        e2e = {"value": ev_, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_prefill_rate(w, args.cpu_seconds) if prefill else cpu_oracle_rate(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": w.name, "S": w.S, "R": w.R, "H": w.H, "caches": w.num_caches,
+                           "lens_sum": int(np.sum(w.lens)), "kv_bytes": units["kv"],
+                           "l2": "flushed between steps" if flush is not None else "inputs larger than L2",
+                           "parallelism": f"replicas x{world}", "tokens_per_step": units["tokens"]},
+                "tokens_per_s": tokens_s, "gpu_launches": launches, "roofline": roof, "cpu_baseline": cpu,
+                "e2e": e2e, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,617 @@
+// Absorbed-query attention over a paged latent cache (decode with 1-2 causal MTP
+// rows, and prefill chunks), for sm_103a.
+//
+// What is computed (issue #1313, step 2 decode bullet: every head's absorbed query
+// against one shared latent; issue #1142 "What stays as it is": the same key chunks
+// merged in the same order whatever the pages):
+//   out[s,r,h,:] = softmax_j(scale * q[s,r,h,:] . K_j) . C_j,  j <= len[s]-R+r
+// with K_j = (latent C_j, rope Kr_j), 576 wide, and the value the 512-wide latent.
+//
+// Work unit (one CTA): one stream, a group of up to 64 (row, head) columns, and a
+// split of the stream's keys.  Keys stream through 64-row tiles: 9 boxes of
+// [64 keys x 64 columns] bf16 (8 latent + 1 rope), loaded by TMA with 128-byte
+// swizzle from the tile's pool page into a 2-stage ring.  The same shared-memory
+// tile feeds both contractions on the 5th-generation tensor cores:
+//   S   = Q . K^T   tcgen05.mma M=128 (Q rows; rows 64-127 unused), N=64 keys, K=576,
+//                   Q K-major, the tile K-major; S accumulates in TMEM (2 buffers)
+//   O^T += V^T . P^T  tcgen05.mma M=128 latent columns x 4, N = group columns, K=64 keys,
+//                   the tile read MN-major as V^T, P (bf16, in shared memory) K-major;
+//                   O^T accumulates in TMEM (4 x 64 columns)
+// Softmax is online in fp32 registers, one thread per (row, head) column, with a
+// lazily moved reference maximum (the accumulator is rescaled only when a tile's
+// maximum passes the reference by more than 2^8).  Each split writes fp32
+// partials (unnormalised O, running maximum, sum); a combine kernel merges them in
+// split-index order.  A stream cut into one split writes bf16 output directly.
+//
+// Warp roles (192 threads): warps 0-3 softmax (warps 0-1), rescale and epilogue
+// (all four, one TMEM lane quadrant each); warp 4 the TMA producer; warp 5 TMEM
+// allocation and the single-thread MMA issuer.
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+
+#include "ptx.cuh"
+#include "tf_internal.h"
+
+namespace tf {
+
+namespace attn {
+
+constexpr int BK = 64;                          // keys a tile
+constexpr int NCOL = 64;                        // (row, head) columns a CTA
+constexpr int NBOX = 9;                         // 64-wide boxes of a 576-wide row
+constexpr int BOX_BYTES = BK * 128;             // [64 rows][64 bf16], 128B swizzle
+constexpr int Q_BYTES = NBOX * NCOL * 128;      // 73,728
+constexpr int P_BYTES = NCOL * 128;             // 8,192
+constexpr int STAGE_BYTES = NBOX * BOX_BYTES;   // 73,728
+constexpr int NSTAGE = 2;
+constexpr int SMEM_Q = 0;
+constexpr int SMEM_P = SMEM_Q + Q_BYTES;        // directly after Q: QK^T rows 64-127 of the last box read it
+constexpr int SMEM_KV = SMEM_P + P_BYTES;
+constexpr int SMEM_CTRL = SMEM_KV + NSTAGE * STAGE_BYTES;  // 229,376
+constexpr float TAU = 8.0f;                     // lazy-rescale threshold, log2 units
+constexpr int TMEM_COLS = 512;
+constexpr int TMEM_S = 0;                       // S buffers at columns 0 and 64
+constexpr int TMEM_O = 128;                     // O^T M-tile j at 128 + 64 j
+constexpr int THREADS = 192;
+constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, 64, false, false);
+
+struct Ctrl {
+    uint64_t kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], s_free[2];
+    uint64_t p_full, pv_done, q_full, drain;
+    uint32_t tmem_base;
+    int abort;
+    int flag[2];
+    float alpha[2][NCOL];
+    float row_m[NCOL], row_inv_l[NCOL];
+};
+constexpr int SMEM_TOTAL = SMEM_CTRL + (int)sizeof(Ctrl) + 1024;
+static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
+
+struct StreamPlan {
+    int64_t len;
+    int32_t tps;      // tiles a split
+    int32_t nsplit;   // splits of each column group
+    int32_t item0;    // first work item of this stream
+    int32_t slot0;    // first workspace slot (partials) of this stream
+};
+
+struct Params {
+    CUtensorMap tm_lat;   // 4D {512, 512 rows, pages, caches}
+    CUtensorMap tm_rope;  // 4D {64, 512 rows, pages, caches}
+    CUtensorMap tm_q;     // 2D {576, S*R*H}
+    const int32_t *pt;
+    __nv_bfloat16 *out;
+    float *lse;
+    float *ws_o;          // [slots][64][512]
+    float *ws_ml;         // [slots][64][2]
+    DevErr *err;
+    float scale_log2;
+    int32_t cache, max_pages, num_pages, S, R, H, ncols, groups, nitems, windowed;
+    StreamPlan st[TF_MAX_STREAMS];
+};
+
+__device__ __forceinline__ int find_stream(const Params &p, int item) {
+    int lo = 0, hi = p.S - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (p.st[mid].item0 <= item) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tm, uint64_t *bar, int c0, int c1, int c2,
+                                            int c3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(ptx::smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(ptx::smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "l"(policy)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_constant__ Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ctrl &c = *reinterpret_cast<Ctrl *>(smem + SMEM_CTRL);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- work item ----
+    const int item = blockIdx.x;
+    const int s = find_stream(p, item);
+    const StreamPlan sp = p.st[s];
+    const int local = item - sp.item0;
+    const int g = local / sp.nsplit, j = local - g * sp.nsplit;
+    const int64_t len = sp.len;
+    const int64_t kb = (int64_t)j * sp.tps * BK;
+    const int64_t ke = min(len, kb + (int64_t)sp.tps * BK);
+    const int ntiles = (int)((ke - kb + BK - 1) / BK);
+    const int col0 = g * NCOL;
+    const int ncols = min(NCOL, p.ncols - col0);
+    const int npv = (ncols + 15) & ~15;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NSTAGE; ++i) {
+            ptx::mbar_init(&c.kv_full[i], 1);
+            ptx::mbar_init(&c.kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&c.s_full[i], 1);
+            ptx::mbar_init(&c.s_free[i], 2);
+        }
+        ptx::mbar_init(&c.p_full, 2);
+        ptx::mbar_init(&c.pv_done, 1);
+        ptx::mbar_init(&c.q_full, 1);
+        ptx::mbar_init(&c.drain, 1);
+        c.abort = 0;
+        c.flag[0] = c.flag[1] = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 5) {
+        ptx::tmem_alloc(&c.tmem_base, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = c.tmem_base;
+    volatile int *abort = &c.abort;
+
+    if (warp == 4) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            ptx::prefetch_tmap(&p.tm_lat);
+            ptx::prefetch_tmap(&p.tm_rope);
+            ptx::prefetch_tmap(&p.tm_q);
+            const uint64_t pol_kv = ptx::policy_evict_first();
+            const uint64_t pol_q = ptx::policy_evict_last();
+            const int qrow = (s * p.R * p.H) + col0;
+            ptx::mbar_arrive_expect_tx(&c.q_full, NBOX * NCOL * 128);
+            for (int b = 0; b < NBOX; ++b)
+                ptx::tma_load_2d(smem + SMEM_Q + b * (NCOL * 128), &p.tm_q, &c.q_full, b * 64, qrow, pol_q);
+            int cur_lp = -1, page = 0, issued = 0;
+            for (int t = 0; t < ntiles; ++t) {
+                const int st = t & 1;
+                if (t >= NSTAGE && !ptx::mbar_wait(&c.kv_empty[st], ((t - NSTAGE) >> 1) & 1, abort, p.err, 1)) break;
+                const int64_t k0 = kb + (int64_t)t * BK;
+                const int lp = (int)(k0 >> 9), row = (int)(k0 & 511);
+                if (lp != cur_lp) {
+                    page = p.windowed ? s * p.max_pages + lp : __ldg(p.pt + (int64_t)s * p.max_pages + lp);
+                    cur_lp = lp;
+                    if (page < 0 || page >= p.num_pages) {
+                        ptx::record_error(p.err, TF_E_DEVICE, page);
+                        *abort = 1;
+                        break;
+                    }
+                }
+                uint8_t *dst = smem + SMEM_KV + st * STAGE_BYTES;
+                ptx::mbar_arrive_expect_tx(&c.kv_full[st], STAGE_BYTES);
+                for (int b = 0; b < 8; ++b)
+                    tma_load_4d(dst + b * BOX_BYTES, &p.tm_lat, &c.kv_full[st], b * 64, row, page, p.cache, pol_kv);
+                tma_load_4d(dst + 8 * BOX_BYTES, &p.tm_rope, &c.kv_full[st], 0, row, page, p.cache, pol_kv);
+                issued = t + 1;
+            }
+            // no copy may still be writing shared memory when the CTA exits
+            ptx::mbar_wait(&c.q_full, 0, abort, p.err, 10, 100000000ull);
+            for (int t = issued - 2; t < issued; ++t)
+                if (t >= 0) ptx::mbar_wait(&c.kv_full[t & 1], (t >> 1) & 1, abort, p.err, 11, 100000000ull);
+        }
+    } else if (warp == 5) {
+        // ================= MMA issuer =================
+        const uint32_t idesc_pv = ptx::idesc_bf16_f32(128, npv, true, false);
+        const uint32_t q_base = ptx::smem_u32(smem + SMEM_Q);
+        const uint32_t p_base = ptx::smem_u32(smem + SMEM_P);
+        bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&c.q_full, 0, abort, p.err, 2));
+        for (int t = 0; ok && t <= ntiles; ++t) {
+            if (t < ntiles) {
+                const int st = t & 1;
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait(&c.kv_full[st], (t >> 1) & 1, abort, p.err, 3))) break;
+                const int64_t k0 = kb + (int64_t)t * BK;
+                const int64_t rem = len - k0;
+                const int valid = rem < BK ? (int)rem : BK;
+                if (valid < BK) {
+                    // rows past the stream's end may hold NaN poison: zero them so that
+                    // P = 0 times V stays 0 in the PV contraction
+                    uint4 *base = reinterpret_cast<uint4 *>(smem + SMEM_KV + st * STAGE_BYTES);
+                    const int per_box = (BK - valid) * 8;
+                    for (int k = lane; k < NBOX * per_box; k += 32) {
+                        const int b = k / per_box, w = k - b * per_box;
+                        base[b * (BOX_BYTES / 16) + valid * 8 + w] = make_uint4(0, 0, 0, 0);
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (t >= 2 &&
+                    !__all_sync(0xffffffffu, ptx::mbar_wait(&c.s_free[st], ((t - 2) >> 1) & 1, abort, p.err, 4)))
+                    break;
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t kv = ptx::smem_u32(smem + SMEM_KV + st * STAGE_BYTES);
+                    const uint32_t d = tmem + TMEM_S + st * 64;
+#pragma unroll
+                    for (int b = 0; b < NBOX; ++b)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint64_t a = ptx::sdesc_sw128(q_base + b * (NCOL * 128) + k * 32, 16, 1024);
+                            const uint64_t bb = ptx::sdesc_sw128(kv + b * BOX_BYTES + k * 32, 16, 1024);
+                            ptx::mma_bf16_ss(d, a, bb, IDESC_QK, (b | k) != 0);
+                        }
+                    ptx::mma_commit(&c.s_full[st]);
+                }
+                __syncwarp();
+            }
+            if (t >= 1) {
+                const int tp = t - 1, stp = tp & 1;
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait(&c.p_full, tp & 1, abort, p.err, 5))) break;
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t kv = ptx::smem_u32(smem + SMEM_KV + stp * STAGE_BYTES);
+#pragma unroll
+                    for (int jm = 0; jm < 4; ++jm) {
+                        const uint32_t d = tmem + TMEM_O + jm * 64;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint64_t a = ptx::sdesc_sw128(kv + 2 * jm * BOX_BYTES + k * 2048, BOX_BYTES, 1024);
+                            const uint64_t bb = ptx::sdesc_sw128(p_base + k * 32, 16, 1024);
+                            ptx::mma_bf16_ss(d, a, bb, idesc_pv, (tp > 0 || k > 0) ? 1u : 0u);
+                        }
+                    }
+                    ptx::mma_commit(&c.pv_done);
+                    ptx::mma_commit(&c.kv_empty[stp]);
+                }
+                __syncwarp();
+            }
+        }
+        // drain: no MMA may still run when TMEM is freed
+        if (lane == 0) {
+            ptx::mma_commit(&c.drain);
+            ptx::mbar_wait(&c.drain, 0, abort, p.err, 6, 200000000ull);
+        }
+        __syncwarp();
+    } else {
+        // ================= softmax / rescale / epilogue (warps 0-3) =================
+        const int q = warp;                    // TMEM lane quadrant
+        const int cidx = threadIdx.x;          // column (softmax threads: 0..63)
+        const bool is_sm = warp < 2;
+        const bool active = is_sm && cidx < ncols;
+        const int gc = col0 + cidx;
+        const int rr = active ? gc / p.H : 0;
+        const int64_t pos_c = len - p.R + rr;  // last visible key of this column
+        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int t = 0; t < ntiles && ok; ++t) {
+            const int st = t & 1;
+            const int64_t k0 = kb + (int64_t)t * BK;
+            float x[BK];
+            if (is_sm) {
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait(&c.s_full[st], (t >> 1) & 1, abort, p.err, 7))) {
+                    ok = false;
+                }
+                if (ok) {
+                    ptx::tc_fence_after();
+                    uint32_t r0[32], r1[32];
+                    ptx::tmem_ld32(lane_base + TMEM_S + st * 64, r0);
+                    ptx::tmem_ld32(lane_base + TMEM_S + st * 64 + 32, r1);
+                    ptx::tmem_ld_wait();
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&c.s_free[st]);
+                    const int64_t lim = (pos_c + 1 < ke ? pos_c + 1 : ke) - k0;
+                    const int nvalid = active ? (lim < 0 ? 0 : (lim > BK ? BK : (int)lim)) : 0;
+                    float mt = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        x[i] = i < nvalid ? __uint_as_float(r0[i]) * p.scale_log2 : -INFINITY;
+                        x[i + 32] = i + 32 < nvalid ? __uint_as_float(r1[i]) * p.scale_log2 : -INFINITY;
+                        mt = fmaxf(mt, fmaxf(x[i], x[i + 32]));
+                    }
+                    float alpha = 1.f;
+                    if (mt > m_ref + TAU) {
+                        alpha = (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - mt);
+                        m_ref = mt;
+                        l *= alpha;
+                    }
+                    c.alpha[t & 1][cidx] = alpha;
+                    const bool need = (alpha != 1.f) && t > 0;
+                    if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr(&c.flag[t & 1], 1);
+                }
+            }
+            if (ptx::named_bar_or(1, 128, !ok || *abort)) {
+                ok = false;
+                break;
+            }
+            const bool do_corr = c.flag[t & 1] != 0;
+            if (t >= 1 && (is_sm || do_corr)) {
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait(&c.pv_done, (t - 1) & 1, abort, p.err, 8))) ok = false;
+            }
+            if (ok && do_corr) {
+                ptx::tc_fence_after();
+                for (int jm = 0; jm < 4; ++jm)
+                    for (int h2 = 0; h2 < npv; h2 += 32) {
+                        uint32_t v[32];
+                        const uint32_t a = lane_base + TMEM_O + jm * 64 + h2;
+                        ptx::tmem_ld32(a, v);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            v[k] = __float_as_uint(__uint_as_float(v[k]) * c.alpha[t & 1][h2 + k]);
+                        ptx::tmem_st32(a, v);
+                    }
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before();
+            }
+            const bool stop = ptx::named_bar_or(2, 128, !ok || *abort);
+            if (threadIdx.x == 0) c.flag[t & 1] = 0;
+            if (stop) {
+                ok = false;
+                break;
+            }
+            if (is_sm) {
+                // P row for this column: p_i = 2^(x_i - m_ref), bf16, 128B-swizzled K-major row
+                const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
+                uint8_t *prow = smem + SMEM_P + cidx * 128;
+                float lsum = 0.f;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = ch * 8 + u * 2;
+                        const uint32_t pk = ptx::pack_bf16x2(ptx::ex2(x[i] - mr), ptx::ex2(x[i + 1] - mr));
+                        lsum += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
+                        w[u] = pk;
+                    }
+                    *reinterpret_cast<uint4 *>(prow + ((ch ^ (cidx & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                l += lsum;
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&c.p_full);
+            }
+        }
+        // ---- epilogue ----
+        if (ok && !*abort) {
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&c.pv_done, (ntiles - 1) & 1, abort, p.err, 9))) ok = false;
+        }
+        if (is_sm) {
+            c.row_m[cidx] = m_ref;
+            c.row_inv_l[cidx] = l > 0.f ? 1.f / l : 0.f;
+        }
+        const bool bad = ptx::named_bar_or(1, 128, !ok || *abort);
+        if (!bad) {
+            ptx::tc_fence_after();
+            const bool direct = sp.nsplit == 1;
+            const int slot = sp.slot0 + g * sp.nsplit + j;
+            for (int jm = 0; jm < 4; ++jm)
+                for (int h2 = 0; h2 < npv; h2 += 32) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(lane_base + TMEM_O + jm * 64 + h2, v);
+                    ptx::tmem_ld_wait();
+                    const int dim = jm * 128 + q * 32 + lane;
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const int col = h2 + k;
+                        if (col >= ncols) continue;
+                        const float o = __uint_as_float(v[k]);
+                        if (direct) {
+                            const size_t orow = (size_t)s * p.ncols + col0 + col;
+                            p.out[orow * kLat + dim] = __float2bfloat16_rn(o * c.row_inv_l[col]);
+                        } else {
+                            p.ws_o[((size_t)slot * NCOL + col) * kLat + dim] = o;
+                        }
+                    }
+                }
+            if (is_sm && cidx < ncols) {
+                if (direct) {
+                    if (p.lse) p.lse[(size_t)s * p.ncols + gc] = (m_ref + log2f(l)) * 0.69314718055994531f;
+                } else {
+                    p.ws_ml[((size_t)slot * NCOL + cidx) * 2 + 0] = m_ref;
+                    p.ws_ml[((size_t)slot * NCOL + cidx) * 2 + 1] = l;
+                }
+            }
+        }
+    }
+
+    // ---- teardown ----
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 5) ptx::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// Merge a stream's split partials in split-index order:
+//   M = max_j m_j,  w_j = 2^(m_j - M),  out = sum_j w_j o_j / sum_j w_j l_j,
+//   lse = (M + log2 sum_j w_j l_j) * ln 2.
+// One 128-thread block per (stream, column); each thread owns 4 latent columns.
+__global__ void __launch_bounds__(128) mla_combine_kernel(const __grid_constant__ Params p) {
+    const int s = blockIdx.x / p.ncols;
+    const int gc = blockIdx.x - s * p.ncols;
+    const StreamPlan sp = p.st[s];
+    if (sp.nsplit <= 1) return;
+    const int g = gc / NCOL, col = gc - g * NCOL;
+    const int slot0 = sp.slot0 + g * sp.nsplit;
+    float M = -INFINITY;
+    for (int jx = 0; jx < sp.nsplit; ++jx) M = fmaxf(M, __ldg(p.ws_ml + ((size_t)(slot0 + jx) * NCOL + col) * 2));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+    const int d4 = threadIdx.x;
+    for (int jx = 0; jx < sp.nsplit; ++jx) {
+        const size_t base = (size_t)(slot0 + jx) * NCOL + col;
+        const float mj = __ldg(p.ws_ml + base * 2), lj = __ldg(p.ws_ml + base * 2 + 1);
+        const float w = (mj == -INFINITY) ? 0.f : ptx::ex2(mj - M);
+        const float4 o = __ldg(reinterpret_cast<const float4 *>(p.ws_o + base * kLat) + d4);
+        acc.x += w * o.x;
+        acc.y += w * o.y;
+        acc.z += w * o.z;
+        acc.w += w * o.w;
+        L += w * lj;
+    }
+    const float inv = 1.f / L;
+    const size_t orow = (size_t)s * p.ncols + gc;
+    __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(p.out + orow * kLat) + d4 * 2;
+    o2[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    o2[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    if (threadIdx.x == 0 && p.lse) p.lse[orow] = (M + log2f(L)) * 0.69314718055994531f;
+}
+
+// ---- host-side split plan: a function of the stream's own (len, R, H) only ----
+struct Split {
+    int tiles, tps, nsplit, groups;
+};
+
+inline Split split_of(int64_t len, int R, int H) {
+    Split sp;
+    sp.tiles = (int)((len + BK - 1) / BK);
+    sp.groups = (R * H + NCOL - 1) / NCOL;
+    if (sp.groups >= 128) {
+        sp.tps = sp.tiles;  // enough column groups to fill the GPU: no key split
+    } else {
+        int t = (sp.tiles + 15) / 16;
+        sp.tps = t < 4 ? 4 : (t > 32 ? 32 : t);
+    }
+    if (sp.tps > sp.tiles) sp.tps = sp.tiles;
+    sp.nsplit = (sp.tiles + sp.tps - 1) / sp.tps;
+    return sp;
+}
+
+}  // namespace attn
+
+size_t attend_workspace_bytes(int S, int R, int H, const int64_t *h_len) {
+    size_t slots = 0;
+    for (int s = 0; s < S; ++s) {
+        attn::Split sp = attn::split_of(h_len[s], R, H);
+        if (sp.nsplit > 1) slots += (size_t)sp.groups * sp.nsplit;
+    }
+    if (slots == 0) return 0;
+    const size_t o = slots * attn::NCOL * kLat * sizeof(float);
+    const size_t ml = slots * attn::NCOL * 2 * sizeof(float);
+    return o + ((ml + 255) & ~size_t(255));
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+static bool encode(CUtensorMap *tm, void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                   const cuuint32_t *box) {
+    auto fn = get_encode();
+    if (!fn) return false;
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static int ensure_pool_maps(tf_kvpool *pool) {
+    std::lock_guard<std::mutex> g(pool->mu);
+    if (pool->tmaps_ready) return TF_OK;
+    pool->tm_lat.resize(1);
+    pool->tm_rope.resize(1);
+    const cuuint64_t P = (cuuint64_t)pool->desc.num_pages, C = (cuuint64_t)pool->desc.num_caches;
+    {
+        cuuint64_t dims[4] = {(cuuint64_t)kLat, (cuuint64_t)kPageRows, P, C};
+        cuuint64_t strides[3] = {(cuuint64_t)kLat * 2, (cuuint64_t)kPageBytes, (cuuint64_t)kPageBytes * P};
+        cuuint32_t box[4] = {64, (cuuint32_t)attn::BK, 1, 1};
+        if (!encode(&pool->tm_lat[0], pool->base, 4, dims, strides, box)) return TF_E_CUDA;
+    }
+    {
+        cuuint64_t dims[4] = {(cuuint64_t)kRope, (cuuint64_t)kPageRows, P, C};
+        cuuint64_t strides[3] = {(cuuint64_t)kRope * 2, (cuuint64_t)kPageBytes, (cuuint64_t)kPageBytes * P};
+        cuuint32_t box[4] = {64, (cuuint32_t)attn::BK, 1, 1};
+        if (!encode(&pool->tm_rope[0], pool->base + kLatBlockBytes, 4, dims, strides, box)) return TF_E_CUDA;
+    }
+    pool->tmaps_ready = true;
+    return TF_OK;
+}
+
+int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages, const int64_t *h_len, int S, int R,
+                  int H, const void *d_q, float scale, void *d_out, float *d_lse, void *d_ws, size_t ws_bytes,
+                  cudaStream_t st) {
+    using namespace attn;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(mla_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) !=
+            cudaSuccess)
+            return TF_E_CUDA;
+        attr_set = true;
+    }
+    if (prepare_launch(pool, st) != TF_OK) return TF_E_CUDA;
+    int rc = ensure_pool_maps(pool);
+    if (rc != TF_OK) return rc;
+
+    // Params is large (tensor maps + the per-stream plan); build it on the heap once per thread.
+    thread_local Params *pp = nullptr;
+    if (!pp) pp = new Params();
+    Params &p = *pp;
+    p.tm_lat = pool->tm_lat[0];
+    p.tm_rope = pool->tm_rope[0];
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)kDk, (cuuint64_t)S * R * H};
+        cuuint64_t strides[1] = {(cuuint64_t)kDk * 2};
+        cuuint32_t box[2] = {64, (cuuint32_t)NCOL};
+        if (!encode(&p.tm_q, const_cast<void *>(d_q), 2, dims, strides, box)) return TF_E_CUDA;
+    }
+    p.pt = d_pt;
+    p.out = static_cast<__nv_bfloat16 *>(d_out);
+    p.lse = d_lse;
+    p.err = pool->err;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.cache = cache;
+    p.max_pages = max_pages;
+    p.num_pages = pool->desc.num_pages;
+    p.S = S;
+    p.R = R;
+    p.H = H;
+    p.ncols = R * H;
+    p.groups = (R * H + NCOL - 1) / NCOL;
+    p.windowed = d_pt ? 0 : 1;
+    int items = 0, slots = 0;
+    bool any_multi = false;
+    for (int s = 0; s < S; ++s) {
+        Split sp = split_of(h_len[s], R, H);
+        p.st[s].len = h_len[s];
+        p.st[s].tps = sp.tps;
+        p.st[s].nsplit = sp.nsplit;
+        p.st[s].item0 = items;
+        p.st[s].slot0 = slots;
+        items += sp.groups * sp.nsplit;
+        if (sp.nsplit > 1) {
+            slots += sp.groups * sp.nsplit;
+            any_multi = true;
+        }
+    }
+    p.nitems = items;
+    p.ws_o = static_cast<float *>(d_ws);
+    p.ws_ml = d_ws ? reinterpret_cast<float *>(static_cast<char *>(d_ws) + (size_t)slots * NCOL * kLat * 4) : nullptr;
+    (void)ws_bytes;
+    {
+        ProfScope prof(pool, kProfAttend, st);
+        mla_attend_kernel<<<items, THREADS, SMEM_TOTAL, st>>>(p);
+        launch_counter()++;
+    }
+    if (cudaGetLastError() != cudaSuccess) return TF_E_CUDA;
+    if (any_multi) {
+        ProfScope prof(pool, kProfCombine, st);
+        mla_combine_kernel<<<S * R * H, 128, 0, st>>>(p);
+        launch_counter()++;
+        if (cudaGetLastError() != cudaSuccess) return TF_E_CUDA;
+    }
+    return TF_OK;
+}
+
+}  // namespace tf

@@ -1,0 +1,93 @@
+// Internal declarations shared by the host pool code and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "../../include/tf_paged_mla.h"
+
+namespace tf {
+
+constexpr int kPageRows = TF_PAGE_ROWS;
+constexpr int kLat = TF_LATENT_DIM;
+constexpr int kRope = TF_ROPE_DIM;
+constexpr int kDk = TF_QK_DIM;
+constexpr size_t kLatBlockBytes = size_t(kPageRows) * kLat * 2;   // 524,288
+constexpr size_t kRopeBlockBytes = size_t(kPageRows) * kRope * 2; // 65,536
+constexpr size_t kPageBytes = kLatBlockBytes + kRopeBlockBytes;   // 589,824
+constexpr size_t kCtrlBytes = 256;
+
+// Device error word, in the pool's control block after the last page.
+struct DevErr {
+    int32_t code;   // 0, TF_E_DEVICE or TF_E_TIMEOUT (first error wins)
+    int32_t pad;
+    int64_t detail; // offending page id or wait site
+};
+
+enum ProfKind { kProfAppend = 0, kProfAttend = 1, kProfCombine = 2, kProfCopy = 3, kProfPoison = 4, kProfKinds = 5 };
+
+struct ProfRec {
+    int kind;
+    cudaEvent_t a, b;
+};
+
+}  // namespace tf
+
+struct tf_kvpool {
+    tf_kvpool_desc desc;
+    char *base = nullptr;
+    size_t bytes = 0;
+    tf::DevErr *err = nullptr;  // device address
+    bool err_cleared = false;   // the error word is zeroed on the first launch
+    std::vector<int32_t> refcnt;
+    std::vector<int32_t> free_ring;  // FIFO of free ids
+    size_t free_head = 0, free_count = 0;
+    std::mutex mu;
+    // TMA descriptors over the pool, one pair (latent, rope) per cache, encoded on first use.
+    bool tmaps_ready = false;
+    std::vector<CUtensorMap> tm_lat, tm_rope;
+    // profiling
+    bool prof = false;
+    std::vector<tf::ProfRec> recs;
+    std::vector<cudaEvent_t> spare_events;
+};
+
+namespace tf {
+
+std::atomic<int64_t> &launch_counter();
+
+// Called before every launch: zeroes the device error word once, on the launch stream.
+inline int prepare_launch(tf_kvpool *pool, cudaStream_t st) {
+    if (pool->err_cleared) return TF_OK;
+    if (cudaMemsetAsync(pool->err, 0, sizeof(DevErr), st) != cudaSuccess) return TF_E_CUDA;
+    pool->err_cleared = true;
+    return TF_OK;
+}
+
+// Bracket a launch with profiling events when the pool asks for them.
+struct ProfScope {
+    tf_kvpool *pool;
+    int kind;
+    cudaStream_t stream;
+    cudaEvent_t a = nullptr, b = nullptr;
+    ProfScope(tf_kvpool *p, int k, cudaStream_t s);
+    ~ProfScope();
+};
+
+// Kernel launchers (defined in the .cu files).  Arguments are already validated.
+int launch_append(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages, const int64_t *h_pos,
+                  int S, int n, const void *d_lat, const void *d_rope, cudaStream_t st);
+int launch_state_copy(tf_kvpool *pool, int cache, const int32_t *d_src, const int32_t *d_dst, int64_t at,
+                      cudaStream_t st);
+int launch_poison(tf_kvpool *pool, const int32_t *h_ids, int n, cudaStream_t st);
+size_t attend_workspace_bytes(int S, int R, int H, const int64_t *h_len);
+int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages, const int64_t *h_len, int S,
+                  int R, int H, const void *d_q, float scale, void *d_out, float *d_lse, void *d_ws,
+                  size_t ws_bytes, cudaStream_t st);
+
+}  // namespace tf

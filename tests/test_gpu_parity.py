@@ -1,0 +1,239 @@
+"""GPU parity of the CUDA path against the oracle, through the C-ABI.
+
+Append and kept-state copy are compared byte for byte with the oracle's pool
+image; attention within max-abs 2e-3 / relative-L2 1e-2 of the fp64 oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import paged as OG
+from paged_mla_kv_gb300 import binding as B
+from paged_mla_kv_gb300 import build as BUILD
+from paged_mla_kv_gb300 import synth as Y
+from paged_mla_kv_gb300.harness import Resident, bf16_tensor
+from tests.gpu_common import bits, compare, no_device_error
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    BUILD.build()
+    B.lib()
+
+
+def pool_image(res: Resident) -> np.ndarray:
+    torch.cuda.synchronize()
+    return bits(res.pool.view()).reshape(res.pool.num_caches, res.pool.num_pages, OG.PAGE_WORDS)
+
+
+# ---------------------------------------------------------------- append / copy
+
+
+@pytest.mark.parametrize("windowed", [False, True])
+def test_append_is_bit_exact(windowed):
+    w = Y.custom("append", 11, lens=[1, 511, 512, 513, 1700], R=1, H=16, num_caches=2,
+                 share=[(-1, 0), (-1, 0), (-1, 0), (2, 1), (-1, 0)])
+    if windowed:
+        w.share = [(-1, 0)] * w.S
+    res = Resident(w, poison=True, windowed=windowed)
+    img = pool_image(res)
+    want = OG.new_pool(w.num_caches, res.pool.num_pages)
+    pt = res.pt_host
+    for c in range(w.num_caches):
+        for s in range(w.S):
+            lo = 0 if windowed else w.shared_pages(s) * 512
+            lat, rope = w.stream_rows(c, s, lo, int(w.lens[s]))
+            OG.append(want, c, None if windowed else pt[s:s + 1], res.max_pages if not windowed else
+                      res.max_pages * w.S, [lo + (s * res.max_pages * 512 if windowed else 0)],
+                      lat[None], rope[None])
+    # pages never taken are not compared (their content is the allocator's); taken ones are, in full
+    taken = np.unique(pt[pt >= 0])
+    assert np.array_equal(img[:, taken], want[:, taken])
+    no_device_error(res.pool)
+
+
+def test_append_many_streams_one_call_and_bad_page():
+    w = Y.custom("append2", 12, lens=[700, 1300, 90], R=1, H=16)
+    res = Resident(w, poison=True)
+    # append 3 more rows to every stream in one call
+    n = 3
+    g = np.random.default_rng(1)
+    lat = g.integers(0, 0x7F00, (w.S, n, 512)).astype(np.uint16)
+    rope = g.integers(0, 0x7F00, (w.S, n, 64)).astype(np.uint16)
+    before = pool_image(res)
+    pos = np.array([10, 1100, 50], np.int64)
+    B.tf_paged_append(res.pool, 0, res.pt, res.max_pages, pos, bf16_tensor(lat), bf16_tensor(rope))
+    after = pool_image(res)
+    OG.append(before, 0, res.pt_host, res.max_pages, pos, lat, rope)
+    assert np.array_equal(after, before)
+    no_device_error(res.pool)
+    # a table entry outside the pool is recorded, and the row skipped
+    bad = res.pt.clone()
+    bad[1, 2] = 10_000
+    B.tf_paged_append(res.pool, 0, bad, res.max_pages, np.array([0, 1030, 0], np.int64),
+                      bf16_tensor(lat[:, :1]), bf16_tensor(rope[:, :1]))
+    rc, detail = res.pool.last_error()
+    assert rc == B.TF_E_DEVICE and detail == 10_000
+    assert res.pool.last_error()[0] == 0     # reading clears it
+
+
+@pytest.mark.parametrize("at", [1, 511, 512, 1000, 1536])
+def test_state_copy_moves_only_rows_below_at(at):
+    w = Y.custom("copy", 13, lens=[1600], R=1, H=16, num_caches=3, pool_pages=12)
+    res = Resident(w, poison=True)
+    pages = -(-at // 512)
+    dst = res.pool.take(pages, stream=None)
+    before = pool_image(res)
+    src_t = torch.from_numpy(res.pt_host[0, :pages].copy()).cuda()
+    dst_t = torch.from_numpy(dst.copy()).cuda()
+    for cache in (-1, 1):
+        B.tf_state_copy_rows(res.pool, cache, src_t, dst_t, at)
+        after = pool_image(res)
+        want = before.copy()
+        OG.state_copy_rows(want, cache, res.pt_host[0, :pages], dst, at)
+        assert np.array_equal(after, want)
+        before = after
+    no_device_error(res.pool)
+
+
+# ---------------------------------------------------------------- attention
+
+
+def run(w, **kw):
+    res = Resident(w, **kw)
+    out, lse = res.attend(res.q())
+    torch.cuda.synchronize()
+    no_device_error(res.pool)
+    return res, out, lse
+
+
+def test_tiny_decode_full_size():
+    w = Y.tiny_decode()
+    _, out, lse = run(w)
+    compare(w, out, lse)
+
+
+@pytest.mark.parametrize("H", [8, 16, 64, 128])
+@pytest.mark.parametrize("R", [1, 2])
+def test_decode_ragged_lengths(H, R):
+    lens = [2, 63, 64, 65, 511, 513, 1000, 4097]
+    w = Y.custom(f"ragged_H{H}_R{R}", 100 + H + R, lens=lens, R=R, H=H)
+    _, out, lse = run(w)
+    compare(w, out, lse)
+
+
+@pytest.mark.parametrize("variant", ["sharp", "ramp"])
+def test_decode_score_distributions(variant):
+    kw = dict(q_std=1.0, scale=0.5) if variant == "sharp" else dict(ramp=60.0)
+    w = Y.custom(f"dist_{variant}", 21, lens=[3000, 9000, 700], R=2, H=32, **kw)
+    _, out, lse = run(w)
+    compare(w, out, lse)
+
+
+def test_decode_long_split_stream():
+    w = Y.custom("long", 22, lens=[70000, 40], R=1, H=64)
+    _, out, lse = run(w)
+    compare(w, out, lse)
+
+
+@pytest.mark.parametrize("T,L,H", [(64, 1000, 16), (300, 700, 8), (256, 3000, 64)])
+def test_prefill_chunk(T, L, H):
+    w = Y.chunked_prefill(seed=30 + T, T=T, L=L, H=H)
+    _, out, lse = run(w)
+    compare(w, out, lse)
+
+
+# ---------------------------------------------------------------- invariants
+
+
+def test_paged_equals_windowed_bit_exact():
+    lens = [3000, 700, 5000]
+    w = Y.custom("pw", 40, lens=lens, R=2, H=64)
+    _, o1, l1 = run(w, windowed=False)
+    _, o2, l2 = run(w, windowed=True)
+    assert np.array_equal(bits(o1), bits(o2)) and np.array_equal(l1.cpu().numpy(), l2.cpu().numpy())
+
+
+def test_pool_permutation_invariance_bit_exact():
+    w = Y.custom("perm", 41, lens=[2500, 9000], R=1, H=64, pool_pages=40)
+    _, o1, l1 = run(w, pool_seed=1)
+    _, o2, l2 = run(w, pool_seed=987654)
+    assert np.array_equal(bits(o1), bits(o2)) and np.array_equal(l1.cpu().numpy(), l2.cpu().numpy())
+
+
+def test_poison_is_never_read():
+    # NaN in every taken page before the writes, and in rows past each length
+    w = Y.custom("poison", 42, lens=[777, 1025, 64], R=2, H=16)
+    _, o1, l1 = run(w, poison=True)
+    _, o2, l2 = run(w, poison=False)
+    assert torch.isfinite(o1.float()).all() and torch.isfinite(l1).all()
+    assert np.array_equal(bits(o1), bits(o2)) and np.array_equal(l1.cpu().numpy(), l2.cpu().numpy())
+
+
+def test_concurrent_equals_solo_bit_exact():
+    lens = [5000, 130, 20000, 2]
+    w = Y.custom("conc", 43, lens=lens, R=2, H=64)
+    _, ob, lb = run(w)
+    for s in [0, 2, 3]:
+        ws = Y.custom("solo", 43, lens=[lens[s]], R=2, H=64)
+        # same values: the solo stream's pages and queries must be the batch stream's
+        ws.page_rows = lambda c, ss, p, _s=s: w.page_rows(c, _s, p)
+        qb = w.q()
+        res = Resident(ws)
+        out, lse = res.attend(bf16_tensor(qb[s:s + 1]))
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(out[0]), bits(ob[s]))
+        assert np.array_equal(lse[0].cpu().numpy(), lb[s].cpu().numpy())
+
+
+def test_resumed_equals_fresh_bit_exact():
+    # keep the first `at` rows into fresh pages, append the rest after them, attend
+    L, at = 6000, 2048 + 300
+    w = Y.custom("resume", 44, lens=[L], R=1, H=64, pool_pages=40)
+    res, o_fresh, l_fresh = run(w)
+    pages_at = -(-at // 512)
+    total = -(-L // 512)
+    new = res.pool.take(total)
+    B.tf_state_copy_rows(res.pool, -1, torch.from_numpy(res.pt_host[0, :pages_at].copy()).cuda(),
+                         torch.from_numpy(new[:pages_at].copy()).cuda(), at)
+    res.pt = torch.from_numpy(new[None, :].copy()).cuda()
+    res.pt_host = new[None, :].copy()
+    res.append_rows(0, 0, at, L)
+    out, lse = res.attend(res.q())
+    torch.cuda.synchronize()
+    no_device_error(res.pool)
+    assert np.array_equal(bits(out), bits(o_fresh)) and np.array_equal(lse.cpu().numpy(), l_fresh.cpu().numpy())
+
+
+def test_drafted_row_equals_plain_decode():
+    L = 3333
+    w2 = Y.custom("draft", 45, lens=[L], R=2, H=64)
+    _, o2, l2 = run(w2)
+    w1 = Y.custom("plain", 45, lens=[L - 1], R=1, H=64)
+    w1.page_rows = w2.page_rows
+    res = Resident(w1)
+    q2 = w2.q()
+    o1, l1 = res.attend(bf16_tensor(q2[:, :1]))
+    torch.cuda.synchronize()
+    d = (o1[0, 0].float() - o2[0, 0].float()).abs().max().item()
+    assert d <= 2e-3
+    assert (l1[0, 0] - l2[0, 0]).abs().max().item() <= 2e-3
+
+
+def test_bad_page_table_is_recorded_not_faulted():
+    w = Y.custom("badpt", 46, lens=[3000], R=1, H=16)
+    res = Resident(w)
+    bad = res.pt.clone()
+    bad[0, 3] = 1 << 20
+    out = torch.zeros((1, 1, 16, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((1, 1, 16), dtype=torch.float32, device="cuda")
+    B.tf_paged_mla_attend(res.pool, 0, bad, res.max_pages, res.lens, res.q(), w.scale, out, lse, res.workspace())
+    rc, detail = res.pool.last_error()
+    assert rc == B.TF_E_DEVICE and detail == 1 << 20
+    # the pool stays usable
+    out2, lse2 = res.attend(res.q())
+    torch.cuda.synchronize()
+    no_device_error(res.pool)
+    compare(w, out2, lse2)

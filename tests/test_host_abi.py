@@ -1,0 +1,211 @@
+"""Host-side tests of the C-ABI library: it loads, exports every declared symbol,
+its plan arithmetic equals the oracle's, its pool bookkeeping behaves, and bad
+arguments are refused on the host before any launch.  No GPU is needed: the
+pool is created over a fake (aligned, never dereferenced) device address."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import plan as OP
+from paged_mla_kv_gb300 import binding as B
+from paged_mla_kv_gb300 import build as BUILD
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    BUILD.build()
+    return B.lib()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(tf_\w+)\s*\(", txt))
+    return names
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_symbols()
+    assert "tf_paged_mla_attend" in names and "tf_paged_append" in names
+    assert "tf_kvpool_create" in names and "tf_state_copy_rows" in names
+    for n in sorted(names):
+        assert hasattr(L, n), n
+
+
+def _fake_pool(num_pages=16, caches=1, seed=0, poison=False):
+    desc = B.make_desc(caches, num_pages, poison, seed)
+    nbytes = B.tf_kvpool_bytes(desc)
+    h = ctypes.c_void_p()
+    rc = B.lib().tf_kvpool_create(ctypes.byref(desc), ctypes.c_void_p(1 << 40), nbytes, ctypes.byref(h))
+    assert rc == 0
+    return h, desc
+
+
+def _take(h, n):
+    ids = np.zeros(max(n, 1), np.int32)
+    rc = B.lib().tf_kvpool_take(h, n, ids.ctypes.data_as(ctypes.c_void_p), None)
+    return rc, ids[:n]
+
+
+def _ids(a):
+    a = np.ascontiguousarray(np.asarray(a, np.int32))
+    return a, a.ctypes.data_as(ctypes.c_void_p), len(a)
+
+
+def test_pool_bytes_and_descriptor_checks(L):
+    d = B.make_desc(12, 1344)
+    assert B.tf_kvpool_bytes(d) == 12 * 1344 * 589824 + 256
+    bad = B.make_desc(1, 16)
+    bad.page_rows = 256
+    assert B.tf_kvpool_bytes(bad) == 0
+    h = ctypes.c_void_p()
+    good = B.make_desc(1, 16)
+    n = B.tf_kvpool_bytes(good)
+    assert L.tf_kvpool_create(ctypes.byref(good), ctypes.c_void_p((1 << 40) + 512), n, ctypes.byref(h)) == B.TF_E_ARG
+    assert L.tf_kvpool_create(ctypes.byref(good), ctypes.c_void_p(1 << 40), n - 1, ctypes.byref(h)) == B.TF_E_NOMEM
+
+
+def test_take_ref_release(L):
+    h, _ = _fake_pool(8)
+    rc, a = _take(h, 5)
+    assert rc == 0 and sorted(a) == [0, 1, 2, 3, 4]
+    assert L.tf_kvpool_free_pages(h) == 3
+    rc, _ = _take(h, 4)
+    assert rc == B.TF_E_NOMEM and L.tf_kvpool_free_pages(h) == 3
+    arr, p, n = _ids(a[:2])
+    assert L.tf_kvpool_ref(h, p, n) == 0
+    assert L.tf_kvpool_refcount(h, int(a[0])) == 2
+    assert L.tf_kvpool_release(h, p, n) == 0
+    assert L.tf_kvpool_refcount(h, int(a[0])) == 1 and L.tf_kvpool_free_pages(h) == 3
+    assert L.tf_kvpool_release(h, p, n) == 0
+    assert L.tf_kvpool_free_pages(h) == 5 and L.tf_kvpool_refcount(h, int(a[0])) == 0
+    # releasing a free page, or a page twice in one call beyond its count, changes nothing
+    arr, p, n = _ids([a[0]])
+    assert L.tf_kvpool_release(h, p, n) == B.TF_E_RANGE
+    arr, p, n = _ids([a[2], a[2]])
+    assert L.tf_kvpool_release(h, p, n) == B.TF_E_RANGE and L.tf_kvpool_refcount(h, int(a[2])) == 1
+    arr, p, n = _ids([99])
+    assert L.tf_kvpool_ref(h, p, n) == B.TF_E_RANGE
+    arr, p, n = _ids([a[0]])
+    assert L.tf_kvpool_ref(h, p, n) == B.TF_E_RANGE          # a free page cannot be shared
+    # freed pages come back last (FIFO), so a just-freed page is not reused at once
+    rc, b = _take(h, 3)
+    assert rc == 0 and set(b) == {5, 6, 7}
+    L.tf_kvpool_destroy(h)
+
+
+def test_seeded_free_list_is_a_permutation(L):
+    h1, _ = _fake_pool(64, seed=1234)
+    h2, _ = _fake_pool(64, seed=1234)
+    h3, _ = _fake_pool(64, seed=99)
+    _, a = _take(h1, 64)
+    _, b = _take(h2, 64)
+    _, c = _take(h3, 64)
+    assert sorted(a) == list(range(64)) and np.array_equal(a, b) and not np.array_equal(a, c)
+    assert not np.array_equal(a, np.arange(64))
+    for h in (h1, h2, h3):
+        L.tf_kvpool_destroy(h)
+
+
+def test_page_ptr(L):
+    h, _ = _fake_pool(10, caches=3)
+    assert L.tf_kvpool_page_ptr(h, 2, 7) == (1 << 40) + (2 * 10 + 7) * 589824
+    assert not L.tf_kvpool_page_ptr(h, 3, 0)
+    assert not L.tf_kvpool_page_ptr(h, 0, 10)
+    L.tf_kvpool_destroy(h)
+
+
+GiB, MiB = 1 << 30, 1 << 20
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_plan_equals_oracle(L, paged):
+    rng = np.random.default_rng(5)
+    for _ in range(400):
+        kw = dict(room_bytes=int(rng.integers(0, 300 * GiB)), context_tokens=int(rng.integers(1, 2_000_000)),
+                  lanes=int(rng.integers(1, 65)), bytes_per_token=int(rng.choice([1152, 13056, 13824, 6912])),
+                  fixed_bytes=int(rng.integers(0, 400 * MiB)), cache_budget_bytes=int(rng.integers(0, 32 * GiB)),
+                  engine_paged=paged)
+        got = B.tf_kvpool_plan(**kw)
+        want = OP.plan(OP.PlanIn(kw["room_bytes"], kw["context_tokens"], kw["lanes"], kw["bytes_per_token"],
+                                 kw["fixed_bytes"], kw["cache_budget_bytes"], engine_paged=paged))
+        if want is None:
+            assert got is None
+            continue
+        assert (got.n_windows, got.window_pages, got.stream_pages, got.cache_bytes, got.other_pages,
+                got.pool_pages, got.pool_tokens) == (want.n_windows, want.window_pages, want.stream_pages,
+                                                     want.cache_bytes, want.other_pages, want.pool_pages,
+                                                     want.pool_tokens)
+
+
+def test_plan_worked_example(L):
+    room = int(round(2.33 * GiB)) + 1048576 * 13056 + 180 * MiB
+    out = B.tf_kvpool_plan(room_bytes=room, context_tokens=1048576, lanes=8, bytes_per_token=13056,
+                           fixed_bytes=180 * MiB, cache_budget_bytes=16 * GiB)
+    assert out.pool_pages == 2056 and out.pool_tokens == 1052672
+
+
+def _args_refused(L, h, fn, *args):
+    before = L.tf_launch_count()
+    rc = fn(h, *args)
+    assert L.tf_launch_count() == before
+    return rc
+
+
+def test_bad_arguments_are_refused_before_launch(L):
+    h, _ = _fake_pool(8, caches=2)
+    fake = ctypes.c_void_p(1 << 41)
+    lens = np.array([100, 5000], np.int64)
+    lp = lens.ctypes.data_as(ctypes.c_void_p)
+    A = L.tf_paged_mla_attend
+    # cache out of range
+    assert _args_refused(L, h, A, 2, fake, 16, lp, 2, 1, 16, fake, 0.1, fake, None, None, 0, None) == B.TF_E_RANGE
+    # length beyond the table
+    assert _args_refused(L, h, A, 0, fake, 4, lp, 2, 1, 16, fake, 0.1, fake, None, None, 0, None) == B.TF_E_RANGE
+    # a length shorter than the query rows
+    short = np.array([1, 50], np.int64)
+    assert _args_refused(L, h, A, 0, fake, 16, short.ctypes.data_as(ctypes.c_void_p), 2, 2, 16, fake, 0.1, fake,
+                         None, None, 0, None) == B.TF_E_RANGE
+    # too many heads, NaN scale, null q
+    assert _args_refused(L, h, A, 0, fake, 16, lp, 2, 1, 129, fake, 0.1, fake, None, None, 0, None) == B.TF_E_ARG
+    assert _args_refused(L, h, A, 0, fake, 16, lp, 2, 1, 16, fake, float("nan"), fake, None, None, 0,
+                         None) == B.TF_E_ARG
+    assert _args_refused(L, h, A, 0, fake, 16, lp, 2, 1, 16, None, 0.1, fake, None, None, 0, None) == B.TF_E_ARG
+    # a null table needs S * max_pages pool pages
+    assert _args_refused(L, h, A, 0, None, 16, lp, 2, 1, 16, fake, 0.1, fake, None, None, 0, None) == B.TF_E_RANGE
+    # workspace missing or too small
+    need = L.tf_paged_mla_workspace_bytes(2, 1, 16, lp)
+    assert need > 0
+    assert _args_refused(L, h, A, 0, fake, 16, lp, 2, 1, 16, fake, 0.1, fake, None, None, 0, None) == B.TF_E_ARG
+    assert _args_refused(L, h, A, 0, fake, 16, lp, 2, 1, 16, fake, 0.1, fake, None, fake, need - 1,
+                         None) == B.TF_E_NOMEM
+    # append: position past the table
+    pos = np.array([16 * 512 - 1], np.int64)
+    assert _args_refused(L, h, L.tf_paged_append, 0, fake, 16, pos.ctypes.data_as(ctypes.c_void_p), 1, 2, fake,
+                         fake, None) == B.TF_E_RANGE
+    assert _args_refused(L, h, L.tf_paged_append, 5, fake, 16, pos.ctypes.data_as(ctypes.c_void_p), 1, 1, fake,
+                         fake, None) == B.TF_E_RANGE
+    # state copy: at past the pool, cache out of range
+    assert _args_refused(L, h, L.tf_state_copy_rows, 0, fake, fake, 8 * 512 + 1, None) == B.TF_E_RANGE
+    assert _args_refused(L, h, L.tf_state_copy_rows, 2, fake, fake, 10, None) == B.TF_E_RANGE
+    assert _args_refused(L, h, L.tf_state_copy_rows, 0, fake, fake, -1, None) == B.TF_E_ARG
+    L.tf_kvpool_destroy(h)
+
+
+def test_workspace_sizes_follow_each_streams_length(L):
+    one = np.array([65536], np.int64)
+    two = np.array([65536, 4096], np.int64)
+    w1 = L.tf_paged_mla_workspace_bytes(1, 1, 64, one.ctypes.data_as(ctypes.c_void_p))
+    w2 = L.tf_paged_mla_workspace_bytes(2, 1, 64, two.ctypes.data_as(ctypes.c_void_p))
+    assert 0 < w1 < w2
+    # a prefill chunk with enough column groups is not split: no workspace
+    pre = np.array([102048], np.int64)
+    assert L.tf_paged_mla_workspace_bytes(1, 2048, 64, pre.ctypes.data_as(ctypes.c_void_p)) == 0
