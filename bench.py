@@ -36,8 +36,8 @@ L2_BYTES = 129 * 1024 * 1024
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=WORKLOADS, default="decode_batch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -132,67 +132,72 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_oracle_rate(w, seconds: float):
-    """Time the oracle, as it stands, on a bounded sample of the workload.
+class OracleSample:
+    """The oracle, as it stands, timed on a bounded sample of the workload.
 
-    The sample is the first k heads of every stream (all query rows), k chosen so
-    the run takes about `seconds`; the rate is reported as KV bytes a second
-    (a stream's rows count once for all its heads, scaled by k / H)."""
-    from oracle import attend as OA
-    threads = os.cpu_count() or 1
-    qall = w.q(0)
-    rows = [w.stream_rows(0, s) for s in range(w.S)]
+    Decode: the first k heads of every stream (all query rows); a stream's rows
+    count once for all its heads, scaled by k / H, so the rate is in KV GB/s.
+    Prefill: n query rows spread over the chunk, all heads; the rate is in
+    TFLOP/s of the causal (row, key) pairs computed.  k or n is calibrated once
+    so that a sample takes about `seconds` on all host cores."""
 
-    def run(k):
+    def __init__(self, w, seconds: float):
+        from oracle import attend as OA
+        self.OA, self.w = OA, w
+        self.threads = os.cpu_count() or 1
+        self.prefill = w.R > 2
+        self.q = w.q(0)
+        self.rows = [w.stream_rows(0, s) for s in range(w.S)]
+        k0 = min(w.R if self.prefill else w.H, max(1, self.threads // (w.R if not self.prefill else 1)))
+        k0 = max(1, min(k0, self.threads))
+        t0, _ = self.run(k0)
+        lim = w.R if self.prefill else w.H
+        self.k = int(max(1, min(lim, k0 * seconds / max(t0, 1e-3))))
+
+    def items(self, k):
+        w = self.w
+        if self.prefill:
+            rows = np.unique(np.linspace(0, w.R - 1, k).round().astype(int))
+            return rows, np.array([r * w.H + h for r in rows for h in range(w.H)], np.int32)
+        return None, np.array([r * w.H + h for r in range(w.R) for h in range(k)], np.int32)
+
+    def run(self, k):
+        w = self.w
+        rows, items = self.items(k)
         t0 = time.perf_counter()
-        nbytes = 0.0
-        for s in range(w.S):
-            items = np.array([r * w.H + h for r in range(w.R) for h in range(k)], np.int32)
-            OA.attend_stream(qall[s], rows[s][0], rows[s][1], w.scale, items, threads)
-            nbytes += int(w.lens[s]) * 1152 * k / w.H
-        return time.perf_counter() - t0, nbytes
+        work = 0.0
+        if self.prefill:
+            self.OA.attend_stream(self.q[0], self.rows[0][0], self.rows[0][1], w.scale, items, self.threads)
+            work = sum(2 * 1088 * (int(w.lens[0]) - w.R + int(r) + 1) for r in rows) * w.H
+        else:
+            for s in range(w.S):
+                self.OA.attend_stream(self.q[s], self.rows[s][0], self.rows[s][1], w.scale, items, self.threads)
+                work += int(w.lens[s]) * 1152 * k / w.H
+        return time.perf_counter() - t0, work
 
-    t1, _ = run(1)
-    k = int(max(1, min(w.H, seconds / max(t1, 1e-3))))
-    t, nbytes = run(k)
-    return dict(value=nbytes / t / 1e9, unit="GB/s", cores=threads, kind="oracle",
-                sample=f"first {k} of {w.H} heads of all {w.S} streams, all {w.R} rows, cache 0 ({t:.1f} s)")
-
-
-def cpu_oracle_prefill_rate(w, seconds: float):
-    from oracle import attend as OA
-    threads = os.cpu_count() or 1
-    qall = w.q(0)
-    lat, rope = w.stream_rows(0, 0)
-    g = np.random.default_rng(0)
-    flops_per = lambda r: 2 * 1088 * (int(w.lens[0]) - w.R + r + 1)
-
-    def run(n):
-        rows = np.sort(g.choice(w.R, size=n, replace=False))
-        items = np.array([r * w.H + h for r in rows for h in range(w.H)], np.int32)
-        t0 = time.perf_counter()
-        OA.attend_stream(qall[0], lat, rope, w.scale, items, threads)
-        return time.perf_counter() - t0, sum(flops_per(r) for r in rows) * w.H, n
-
-    t1, _, _ = run(1)
-    n = int(max(1, min(w.R, seconds / max(t1, 1e-3))))
-    t, fl, n = run(n)
-    return dict(value=fl / t / 1e12, unit="TFLOP/s", cores=threads, kind="oracle",
-                sample=f"{n} of {w.R} query rows (all {w.H} heads), spread over the chunk ({t:.1f} s)")
+    def measure(self):
+        t, work = self.run(self.k)
+        w = self.w
+        if self.prefill:
+            rows, _ = self.items(self.k)
+            return dict(value=work / t / 1e12, unit="TFLOP/s", cores=self.threads, kind="oracle",
+                        sample=f"{len(rows)} of {w.R} query rows spread over the chunk, all {w.H} heads, "
+                               f"cache 0 ({t:.1f} s)")
+        return dict(value=work / t / 1e9, unit="GB/s", cores=self.threads, kind="oracle",
+                    sample=f"first {self.k} of {w.H} heads of all {w.S} streams, all {w.R} rows, cache 0 "
+                           f"({t:.1f} s)")
 
 
 def reference_arm(args, rank, world):
-    """The oracle timed as the reference arm (host cores, bounded sample each step)."""
+    """The oracle timed as the reference arm (host cores, the same bounded sample each step)."""
     if rank != 0:
         return
     w = make_workload(args.workload)
-    prefill = w.R > 2
-    per_step = max(2.0, 120.0 / max(1, args.steps + args.warmup))
-    vals = []
-    for i in range(args.warmup + args.steps):
-        r = cpu_oracle_prefill_rate(w, per_step) if prefill else cpu_oracle_rate(w, per_step)
-        if i >= args.warmup:
-            vals.append(r)
+    per_step = min(20.0, max(1.0, 150.0 / max(1, args.steps + args.warmup)))
+    o = OracleSample(w, per_step)
+    for _ in range(args.warmup):
+        o.run(o.k)
+    vals = [o.measure() for _ in range(args.steps)]
     v = statistics.median(x["value"] for x in vals)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": vals[0]["unit"], "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
@@ -347,7 +352,7 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_prefill_rate(w, args.cpu_seconds) if prefill else cpu_oracle_rate(w, args.cpu_seconds)
+        cpu = OracleSample(w, args.cpu_seconds).measure()
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
