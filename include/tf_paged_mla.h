@@ -183,6 +183,31 @@ int tf_paged_mla_attend(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int
                         const void *d_q, float scale, void *d_out, float *d_lse,
                         void *d_ws, size_t ws_bytes, void *cuda_stream);
 
+/* ---- attention without a caller workspace ----
+ * No counterpart on the TensorFold pages: this entry point exists for callers of
+ * this library that cannot allocate device memory -- an engine that hands the
+ * library only its page pool and per-step tensors from a fixed arena and allows no
+ * further device allocation while it serves, or a host program that has no device
+ * allocator of its own.  It computes exactly what tf_paged_mla_attend computes, with
+ * the same arguments minus the workspace: the split partials go to one scratch
+ * array of TF_STATIC_WS_BYTES (64 MiB) that the library defines in device memory.
+ * Every GPU that loads the library holds that array until the process exits.
+ * - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ * - The first call on each device looks up the array's device address with that
+ *   device current (cudaGetSymbolAddress) and remembers it; make that first call
+ *   before any stream capture.
+ * - A call whose split partials need more than TF_STATIC_WS_BYTES (see
+ *   tf_paged_mla_workspace_bytes) returns TF_E_NOMEM and launches nothing.
+ * - Every call shares the one array and it keeps the last call's contents (each
+ *   call writes every partial it reads, so nothing has to start at zero).  Calls
+ *   that overlap on the GPU -- on two streams, or from two threads -- race on it:
+ *   order them on one stream, or use tf_paged_mla_attend with separate workspaces. */
+#define TF_STATIC_WS_BYTES (64u << 20)
+
+int tf_paged_mla_attend_static(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int32_t max_pages,
+                               const int64_t *h_len, int32_t S, int32_t R, int32_t H,
+                               const void *d_q, float scale, void *d_out, float *d_lse, void *cuda_stream);
+
 /* ---- kept-state copy (issue #1142, piece 1: keepAs / restoreState copy each
  * cache's first `at` rows; rows past `at` are never read) ----
  * Copies rows [0, at) of cache `cache` (every cache when cache < 0) from the

@@ -65,6 +65,7 @@ _SIGS = {
     "tf_paged_append": (ctypes.c_int, [_P, _I32, _P, _I32, _P, _I32, _I32, _P, _P, _P]),
     "tf_paged_mla_workspace_bytes": (_SZ, [_I32, _I32, _I32, _P]),
     "tf_paged_mla_attend": (ctypes.c_int, [_P, _I32, _P, _I32, _P, _I32, _I32, _I32, _P, _F, _P, _P, _P, _SZ, _P]),
+    "tf_paged_mla_attend_static": (ctypes.c_int, [_P, _I32, _P, _I32, _P, _I32, _I32, _I32, _P, _F, _P, _P, _P]),
     "tf_state_copy_rows": (ctypes.c_int, [_P, _I32, _P, _P, _I64, _P]),
     "tf_last_error": (ctypes.c_int, [_P, ctypes.POINTER(_I64)]),
     "tf_launch_count": (_I64, []),
@@ -232,6 +233,19 @@ def tf_paged_mla_attend(pool: KVPool, cache: int, pt, max_pages: int, lens, q, s
     _check(lib().tf_paged_mla_attend(pool.handle, cache, _ptr(pt), max_pages, p, S, R, H, _ptr(q), float(scale),
                                      _ptr(out), _ptr(lse), _ptr(ws), ws_bytes, _stream(stream)),
            "tf_paged_mla_attend")
+
+
+TF_STATIC_WS_BYTES = 64 << 20
+
+
+def tf_paged_mla_attend_static(pool: KVPool, cache: int, pt, max_pages: int, lens, q, scale: float, out, lse=None,
+                               stream=None) -> None:
+    """tf_paged_mla_attend without a workspace: for callers that cannot allocate device memory."""
+    S, R, H = int(q.shape[0]), int(q.shape[1]), int(q.shape[2])
+    a, p = _i64(lens)
+    _check(lib().tf_paged_mla_attend_static(pool.handle, cache, _ptr(pt), max_pages, p, S, R, H, _ptr(q),
+                                            float(scale), _ptr(out), _ptr(lse), _stream(stream)),
+           "tf_paged_mla_attend_static")
 
 
 def tf_state_copy_rows(pool: KVPool, cache: int, src_pages, dst_pages, at: int, stream=None) -> None:
