@@ -10,27 +10,32 @@
 // Work unit (one CTA): one stream, a group of up to 64 (row, head) columns, and a
 // split of the stream's keys.  Keys stream through 64-row tiles: 9 boxes of
 // [64 keys x 64 columns] bf16 (8 latent + 1 rope), loaded by TMA with 128-byte
-// swizzle from the tile's pool page into a 2-stage ring.  The same shared-memory
-// tile feeds both contractions on the 5th-generation tensor cores:
-//   S   = Q . K^T   tcgen05.mma M=128 (Q rows; rows 64-127 unused), N=64 keys, K=576,
-//                   Q K-major, the tile K-major; S accumulates in TMEM (2 buffers)
+// swizzle from the tile's pool page into a 2-stage ring; the producer also
+// prefetches the rows of the tiles four ahead into L2 (cp.async.bulk.prefetch), so
+// the shared-memory loads are L2 hits.  The same shared-memory tile feeds both
+// contractions on the 5th-generation tensor cores:
+//   S   = Q . K^T     tcgen05.mma M=128 (Q rows; rows 64-127 unused), N=64 keys, K=576,
+//                     Q K-major, the tile K-major; S accumulates in TMEM (2 buffers)
 //   O^T += V^T . P^T  tcgen05.mma M=128 latent columns x 4, N = group columns, K=64 keys,
-//                   the tile read MN-major as V^T, P (bf16, in shared memory) K-major;
-//                   O^T accumulates in TMEM (4 x 64 columns)
+//                     the tile read MN-major as V^T, P (bf16, in shared memory) K-major;
+//                     O^T accumulates in TMEM (4 x 64 columns)
 // Softmax is online in fp32 registers, one thread per (row, head) column, with a
-// lazily moved reference maximum (the accumulator is rescaled only when a tile's
-// maximum passes the reference by more than 2^8).  Each split writes fp32
-// partials (unnormalised O, running maximum, sum); a combine kernel merges them in
-// split-index order.  A stream cut into one split writes bf16 output directly.
+// lazily moved reference maximum: O is rescaled only when a tile's maximum passes
+// the reference by more than 2^8, by a separate warp group, so the softmax warps
+// never wait for it.  Each split writes fp32 partials (unnormalised O, running
+// maximum, sum); a combine kernel merges them in split-index order.  A stream cut
+// into one split writes bf16 output directly.
 //
-// Warp roles (192 threads): warps 0-3 softmax (warps 0-1), rescale and epilogue
-// (all four, one TMEM lane quadrant each); warp 4 the TMA producer; warp 5 TMEM
-// allocation and the single-thread MMA issuer.
+// Warp roles (256 threads): warps 0-3 rescale O^T when asked and run the epilogue
+// (one TMEM lane quadrant each); warps 4-5 softmax (quadrants 0-1 = the 64 rows of
+// S); warp 6 the TMA producer; warp 7 TMEM allocation and the single-thread MMA issuer.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <numeric>
 
 #include "ptx.cuh"
 #include "tf_internal.h"
@@ -39,50 +44,59 @@ namespace tf {
 
 namespace attn {
 
-constexpr int BK = 64;                          // keys a tile
+constexpr int BK = 64;                          // keys a tile (N of the QK^T MMA; an MMA
+                                                // costs about the same to issue at N=32 or 64)
 constexpr int NCOL = 64;                        // (row, head) columns a CTA
 constexpr int NBOX = 9;                         // 64-wide boxes of a 576-wide row
 constexpr int BOX_BYTES = BK * 128;             // [64 rows][64 bf16], 128B swizzle
-constexpr int Q_BYTES = NBOX * NCOL * 128;      // 73,728
-constexpr int P_BYTES = NCOL * 128;             // 8,192
+constexpr int QBOX_BYTES = NCOL * 128;          // [64 rows][64 bf16]
+constexpr int Q_BYTES = NBOX * QBOX_BYTES;      // 73,728
+constexpr int P_BYTES = NCOL * 128;             // 64 rows (columns) of 64 keys, bf16
 constexpr int STAGE_BYTES = NBOX * BOX_BYTES;   // 73,728
 constexpr int NSTAGE = 2;
+constexpr int PREFETCH = 4;                     // tiles prefetched into L2 ahead of the load
 constexpr int SMEM_Q = 0;
 constexpr int SMEM_P = SMEM_Q + Q_BYTES;        // directly after Q: QK^T rows 64-127 of the last box read it
 constexpr int SMEM_KV = SMEM_P + P_BYTES;
 constexpr int SMEM_CTRL = SMEM_KV + NSTAGE * STAGE_BYTES;  // 229,376
 constexpr float TAU = 8.0f;                     // lazy-rescale threshold, log2 units
 constexpr int TMEM_COLS = 512;
-constexpr int TMEM_S = 0;                       // S buffers at columns 0 and 64
-constexpr int TMEM_O = 128;                     // O^T M-tile j at 128 + 64 j
-constexpr int THREADS = 192;
-constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, 64, false, false);
+constexpr int TMEM_O = 0;                       // O^T M-tile j at 64 j (j < 4)
+constexpr int TMEM_S = 256;                     // S buffers at 256 and 320
+constexpr int THREADS = 256;
+constexpr int SPLIT_UNIT = 256;                 // split sizes are multiples of this many keys
+constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, BK, false, false);
+static_assert(SPLIT_UNIT % BK == 0, "splits must be tile-aligned");
 
 struct Ctrl {
     uint64_t kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], s_free[2];
-    uint64_t p_full, pv_done, q_full, drain;
+    uint64_t corr_req[2], p_full, pv_done, q_full, stats_full, drain;
     uint32_t tmem_base;
     int abort;
     int flag[2];
     float alpha[2][NCOL];
-    float row_m[NCOL], row_inv_l[NCOL];
+    float row_inv_l[NCOL];
 };
 constexpr int SMEM_TOTAL = SMEM_CTRL + (int)sizeof(Ctrl) + 1024;
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 
+// One entry per stream, in launch order (streams with longer splits first).
 struct StreamPlan {
     int64_t len;
-    int32_t tps;      // tiles a split
+    int32_t sidx;     // the stream's index in the caller's arrays
+    int32_t split;    // keys a split (a multiple of SPLIT_UNIT), or the whole stream
     int32_t nsplit;   // splits of each column group
     int32_t item0;    // first work item of this stream
     int32_t slot0;    // first workspace slot (partials) of this stream
+    int32_t pad;
 };
 
 struct Params {
-    CUtensorMap tm_lat;   // 4D {512, 512 rows, pages, caches}
-    CUtensorMap tm_rope;  // 4D {64, 512 rows, pages, caches}
-    CUtensorMap tm_q;     // 2D {576, S*R*H}
+    CUtensorMap tm_lat;   // 4D {512, 512 rows, pages, caches}, box {64, 32, 1, 1}
+    CUtensorMap tm_rope;  // 4D {64, 512 rows, pages, caches}, box {64, 32, 1, 1}
+    CUtensorMap tm_q;     // 2D {576, S*R*H}, box {64, 64}
     const int32_t *pt;
+    const char *cache_base;   // page 0 of this cache (for the L2 prefetch of raw rows)
     __nv_bfloat16 *out;
     float *lse;
     float *ws_o;          // [slots][64][512]
@@ -93,7 +107,7 @@ struct Params {
     StreamPlan st[TF_MAX_STREAMS];
 };
 
-__device__ __forceinline__ int find_stream(const Params &p, int item) {
+__device__ __forceinline__ int find_entry(const Params &p, int item) {
     int lo = 0, hi = p.S - 1;
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
@@ -112,6 +126,15 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tm, ui
         : "memory");
 }
 
+#define ALLW(x) __all_sync(0xffffffffu, (x))
+
+// Barrier phases: a parity wait only tells the current phase from the one before it,
+// so a barrier may be neither two phases ahead of a waiter nor two phases short of
+// the phase it waits for.  corr_req is double-buffered because softmax may post
+// tiles t and t+1 before the rescale group reads t; the epilogue waits stats_full
+// before the last pv_done for the second reason; every other wait follows the
+// waiter's own previous wait on the same barrier.
+
 __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -120,13 +143,13 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
 
     // ---- work item ----
     const int item = blockIdx.x;
-    const int s = find_stream(p, item);
-    const StreamPlan sp = p.st[s];
+    const StreamPlan sp = p.st[find_entry(p, item)];
+    const int s = sp.sidx;
     const int local = item - sp.item0;
     const int g = local / sp.nsplit, j = local - g * sp.nsplit;
     const int64_t len = sp.len;
-    const int64_t kb = (int64_t)j * sp.tps * BK;
-    const int64_t ke = min(len, kb + (int64_t)sp.tps * BK);
+    const int64_t kb = (int64_t)j * sp.split;
+    const int64_t ke = min(len, kb + (int64_t)sp.split);
     const int ntiles = (int)((ke - kb + BK - 1) / BK);
     const int col0 = g * NCOL;
     const int ncols = min(NCOL, p.ncols - col0);
@@ -141,15 +164,18 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
             ptx::mbar_init(&c.s_full[i], 1);
             ptx::mbar_init(&c.s_free[i], 2);
         }
-        ptx::mbar_init(&c.p_full, 2);
+        ptx::mbar_init(&c.corr_req[0], 2);
+        ptx::mbar_init(&c.corr_req[1], 2);
+        ptx::mbar_init(&c.p_full, 3);
         ptx::mbar_init(&c.pv_done, 1);
         ptx::mbar_init(&c.q_full, 1);
+        ptx::mbar_init(&c.stats_full, 2);
         ptx::mbar_init(&c.drain, 1);
         c.abort = 0;
         c.flag[0] = c.flag[1] = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 7) {
         ptx::tmem_alloc(&c.tmem_base, TMEM_COLS);
         ptx::tmem_relinquish();
     }
@@ -159,7 +185,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
     const uint32_t tmem = c.tmem_base;
     volatile int *abort = &c.abort;
 
-    if (warp == 4) {
+    if (warp == 6) {
         // ================= TMA producer =================
         if (lane == 0) {
             ptx::prefetch_tmap(&p.tm_lat);
@@ -168,20 +194,47 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
             const uint64_t pol_kv = ptx::policy_evict_first();
             const uint64_t pol_q = ptx::policy_evict_last();
             const int qrow = (s * p.R * p.H) + col0;
-            ptx::mbar_arrive_expect_tx(&c.q_full, NBOX * NCOL * 128);
+            ptx::mbar_arrive_expect_tx(&c.q_full, Q_BYTES);
             for (int b = 0; b < NBOX; ++b)
-                ptx::tma_load_2d(smem + SMEM_Q + b * (NCOL * 128), &p.tm_q, &c.q_full, b * 64, qrow, pol_q);
+                ptx::tma_load_2d(smem + SMEM_Q + b * QBOX_BYTES, &p.tm_q, &c.q_full, b * 64, qrow, pol_q);
+            // page id of a tile's logical page; -1 marks an id outside the pool
+            auto page_of = [&](int t) -> int {
+                const int lp = (int)((kb + (int64_t)t * BK) >> 9);
+                const int pg = p.windowed ? s * p.max_pages + lp : __ldg(p.pt + (int64_t)s * p.max_pages + lp);
+                return (pg < 0 || pg >= p.num_pages) ? -1 : pg;
+            };
+            // L2 prefetch of a tile's rows: 64 latent rows (64 KiB) and 64 rope rows (8 KiB), contiguous
+            int pf_next = 0, pf_lp = -1, pf_page = -1;
+            auto prefetch_upto = [&](int last) {
+                for (; pf_next <= last && pf_next < ntiles; ++pf_next) {
+                    const int64_t k0 = kb + (int64_t)pf_next * BK;
+                    const int lp = (int)(k0 >> 9), row = (int)(k0 & 511);
+                    if (lp != pf_lp) {
+                        pf_page = page_of(pf_next);
+                        pf_lp = lp;
+                    }
+                    if (pf_page < 0) continue;
+                    const char *pg = p.cache_base + (size_t)pf_page * kPageBytes;
+                    ptx::prefetch_l2_bulk(pg + (size_t)row * (kLat * 2), BK * kLat * 2);
+                    ptx::prefetch_l2_bulk(pg + kLatBlockBytes + (size_t)row * (kRope * 2), BK * kRope * 2);
+                }
+            };
+            prefetch_upto(PREFETCH + NSTAGE - 1);
             int cur_lp = -1, page = 0, issued = 0;
             for (int t = 0; t < ntiles; ++t) {
-                const int st = t & 1;
-                if (t >= NSTAGE && !ptx::mbar_wait(&c.kv_empty[st], ((t - NSTAGE) >> 1) & 1, abort, p.err, 1)) break;
+                const int st = t % NSTAGE;
+                if (t >= NSTAGE &&
+                    !ptx::mbar_wait(&c.kv_empty[st], ((t / NSTAGE) - 1) & 1, abort, p.err, 1))
+                    break;
+                prefetch_upto(t + PREFETCH + NSTAGE - 1);
                 const int64_t k0 = kb + (int64_t)t * BK;
                 const int lp = (int)(k0 >> 9), row = (int)(k0 & 511);
                 if (lp != cur_lp) {
-                    page = p.windowed ? s * p.max_pages + lp : __ldg(p.pt + (int64_t)s * p.max_pages + lp);
+                    page = page_of(t);
                     cur_lp = lp;
-                    if (page < 0 || page >= p.num_pages) {
-                        ptx::record_error(p.err, TF_E_DEVICE, page);
+                    if (page < 0) {
+                        const int raw = p.windowed ? s * p.max_pages + lp : __ldg(p.pt + (int64_t)s * p.max_pages + lp);
+                        ptx::record_error(p.err, TF_E_DEVICE, raw);
                         *abort = 1;
                         break;
                     }
@@ -194,22 +247,24 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
                 issued = t + 1;
             }
             // no copy may still be writing shared memory when the CTA exits
-            ptx::mbar_wait(&c.q_full, 0, abort, p.err, 10, 100000000ull);
-            for (int t = issued - 2; t < issued; ++t)
-                if (t >= 0) ptx::mbar_wait(&c.kv_full[t & 1], (t >> 1) & 1, abort, p.err, 11, 100000000ull);
+            ptx::mbar_wait(&c.q_full, 0, abort, p.err, 10, 1ll << 28);
+            for (int t = max(0, issued - NSTAGE); t < issued; ++t)
+                ptx::mbar_wait(&c.kv_full[t % NSTAGE], (t / NSTAGE) & 1, abort, p.err, 11, 1ll << 28);
         }
-    } else if (warp == 5) {
+    } else if (warp == 7) {
         // ================= MMA issuer =================
         const uint32_t idesc_pv = ptx::idesc_bf16_f32(128, npv, true, false);
-        const uint32_t q_base = ptx::smem_u32(smem + SMEM_Q);
-        const uint32_t p_base = ptx::smem_u32(smem + SMEM_P);
-        bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(&c.q_full, 0, abort, p.err, 2));
+        // descriptor bases; per MMA only a constant is added to the start-address field
+        const uint64_t q_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_Q), 16, 1024);
+        const uint64_t kv_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_KV), 16, 1024);
+        const uint64_t v_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_KV), BOX_BYTES, 1024);
+        const uint64_t p_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_P), 16, 1024);
+        bool ok = ALLW(ptx::mbar_wait(&c.q_full, 0, abort, p.err, 2));
         for (int t = 0; ok && t <= ntiles; ++t) {
             if (t < ntiles) {
-                const int st = t & 1;
-                if (!__all_sync(0xffffffffu, ptx::mbar_wait(&c.kv_full[st], (t >> 1) & 1, abort, p.err, 3))) break;
-                const int64_t k0 = kb + (int64_t)t * BK;
-                const int64_t rem = len - k0;
+                const int st = t % NSTAGE;
+                if (!ALLW(ptx::mbar_wait(&c.kv_full[st], (t / NSTAGE) & 1, abort, p.err, 3))) break;
+                const int64_t rem = len - (kb + (int64_t)t * BK);
                 const int valid = rem < BK ? (int)rem : BK;
                 if (valid < BK) {
                     // rows past the stream's end may hold NaN poison: zero them so that
@@ -223,41 +278,35 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                 }
-                if (t >= 2 &&
-                    !__all_sync(0xffffffffu, ptx::mbar_wait(&c.s_free[st], ((t - 2) >> 1) & 1, abort, p.err, 4)))
-                    break;
+                if (t >= 2 && !ALLW(ptx::mbar_wait(&c.s_free[t & 1], ((t - 2) >> 1) & 1, abort, p.err, 4))) break;
                 ptx::tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t kv = ptx::smem_u32(smem + SMEM_KV + st * STAGE_BYTES);
-                    const uint32_t d = tmem + TMEM_S + st * 64;
+                    const uint64_t kvd = kv_desc0 + (uint64_t)(st * (STAGE_BYTES >> 4));
+                    const uint32_t d = tmem + TMEM_S + (t & 1) * BK;
 #pragma unroll
                     for (int b = 0; b < NBOX; ++b)
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint64_t a = ptx::sdesc_sw128(q_base + b * (NCOL * 128) + k * 32, 16, 1024);
-                            const uint64_t bb = ptx::sdesc_sw128(kv + b * BOX_BYTES + k * 32, 16, 1024);
-                            ptx::mma_bf16_ss(d, a, bb, IDESC_QK, (b | k) != 0);
-                        }
-                    ptx::mma_commit(&c.s_full[st]);
+                        for (int k = 0; k < 4; ++k)
+                            ptx::mma_bf16_ss(d, q_desc0 + (uint64_t)((b * QBOX_BYTES + k * 32) >> 4),
+                                             kvd + (uint64_t)((b * BOX_BYTES + k * 32) >> 4), IDESC_QK, (b | k) != 0);
+                    ptx::mma_commit(&c.s_full[t & 1]);
                 }
                 __syncwarp();
             }
             if (t >= 1) {
-                const int tp = t - 1, stp = tp & 1;
-                if (!__all_sync(0xffffffffu, ptx::mbar_wait(&c.p_full, tp & 1, abort, p.err, 5))) break;
+                const int tp = t - 1, stp = tp % NSTAGE;
+                if (!ALLW(ptx::mbar_wait(&c.p_full, tp & 1, abort, p.err, 5))) break;
                 ptx::tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t kv = ptx::smem_u32(smem + SMEM_KV + stp * STAGE_BYTES);
+                    const uint64_t vd = v_desc0 + (uint64_t)(stp * (STAGE_BYTES >> 4));
+                    const uint32_t acc0 = tp > 0 ? 1u : 0u;
 #pragma unroll
-                    for (int jm = 0; jm < 4; ++jm) {
-                        const uint32_t d = tmem + TMEM_O + jm * 64;
+                    for (int k = 0; k < BK / 16; ++k)
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint64_t a = ptx::sdesc_sw128(kv + 2 * jm * BOX_BYTES + k * 2048, BOX_BYTES, 1024);
-                            const uint64_t bb = ptx::sdesc_sw128(p_base + k * 32, 16, 1024);
-                            ptx::mma_bf16_ss(d, a, bb, idesc_pv, (tp > 0 || k > 0) ? 1u : 0u);
-                        }
-                    }
+                        for (int jm = 0; jm < 4; ++jm)
+                            ptx::mma_bf16_ss(tmem + TMEM_O + jm * 64,
+                                             vd + (uint64_t)((2 * jm * BOX_BYTES + k * 2048) >> 4),
+                                             p_desc0 + (uint64_t)((k * 32) >> 4), idesc_pv, k > 0 ? 1u : acc0);
                     ptx::mma_commit(&c.pv_done);
                     ptx::mma_commit(&c.kv_empty[stp]);
                 }
@@ -267,118 +316,131 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
         // drain: no MMA may still run when TMEM is freed
         if (lane == 0) {
             ptx::mma_commit(&c.drain);
-            ptx::mbar_wait(&c.drain, 0, abort, p.err, 6, 200000000ull);
+            ptx::mbar_wait(&c.drain, 0, abort, p.err, 6, 1ll << 29);
         }
         __syncwarp();
-    } else {
-        // ================= softmax / rescale / epilogue (warps 0-3) =================
-        const int q = warp;                    // TMEM lane quadrant
-        const int cidx = threadIdx.x;          // column (softmax threads: 0..63)
-        const bool is_sm = warp < 2;
-        const bool active = is_sm && cidx < ncols;
+    } else if (warp >= 4) {
+        // ================= softmax (warps 4-5: S rows 0-63) =================
+        const int q = warp & 3;
+        const int cidx = threadIdx.x - 128;    // column 0..63
+        const bool active = cidx < ncols;
         const int gc = col0 + cidx;
         const int rr = active ? gc / p.H : 0;
         const int64_t pos_c = len - p.R + rr;  // last visible key of this column
         const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int t = 0; t < ntiles && ok; ++t) {
-            const int st = t & 1;
+        for (int t = 0; t < ntiles; ++t) {
             const int64_t k0 = kb + (int64_t)t * BK;
+            if (!ALLW(ptx::mbar_wait(&c.s_full[t & 1], (t >> 1) & 1, abort, p.err, 7))) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            uint32_t r[BK];
+            ptx::tmem_ld32(lane_base + TMEM_S + (t & 1) * BK, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+            ptx::tmem_ld32(lane_base + TMEM_S + (t & 1) * BK + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+            ptx::tmem_ld_wait();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&c.s_free[t & 1]);
+            const int64_t lim = (pos_c + 1 < ke ? pos_c + 1 : ke) - k0;
+            const int nvalid = active ? (lim < 0 ? 0 : (lim > BK ? BK : (int)lim)) : 0;
             float x[BK];
-            if (is_sm) {
-                if (!__all_sync(0xffffffffu, ptx::mbar_wait(&c.s_full[st], (t >> 1) & 1, abort, p.err, 7))) {
-                    ok = false;
-                }
+            float mt = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < BK; ++i) {
+                x[i] = i < nvalid ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+                mt = fmaxf(mt, x[i]);
+            }
+            float alpha = 1.f;
+            if (mt > m_ref + TAU) {
+                alpha = (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - mt);
+                m_ref = mt;
+                l *= alpha;
+            }
+            c.alpha[t & 1][cidx] = alpha;
+            if (__any_sync(0xffffffffu, alpha != 1.f && t > 0) && lane == 0) atomicOr(&c.flag[t & 1], 1);
+            // P row for this column: p_i = 2^(x_i - m_ref) as bf16, 8 x 16 B, 128B-swizzled K-major
+            const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
+            uint32_t pk[BK / 2];
+            float lsum = 0.f;
+#pragma unroll
+            for (int i = 0; i < BK / 2; ++i) {
+                pk[i] = ptx::pack_bf16x2(ptx::ex2(x[2 * i] - mr), ptx::ex2(x[2 * i + 1] - mr));
+                lsum += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+            }
+            l += lsum;
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&c.corr_req[t & 1]);
+            if (t >= 1 && !ALLW(ptx::mbar_wait(&c.pv_done, (t - 1) & 1, abort, p.err, 8))) {
+                ok = false;
+                break;
+            }
+            uint8_t *prow = smem + SMEM_P + cidx * 128;
+#pragma unroll
+            for (int ch = 0; ch < BK / 8; ++ch)
+                *reinterpret_cast<uint4 *>(prow + ((ch ^ (cidx & 7)) << 4)) =
+                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&c.p_full);
+        }
+        // statistics for the epilogue
+        c.row_inv_l[cidx] = l > 0.f ? 1.f / l : 0.f;
+        if (ok && active) {
+            const int slot = sp.slot0 + g * sp.nsplit + j;
+            if (sp.nsplit == 1) {
+                if (p.lse) p.lse[(size_t)s * p.ncols + gc] = (m_ref + log2f(l)) * 0.69314718055994531f;
+            } else {
+                p.ws_ml[((size_t)slot * NCOL + cidx) * 2 + 0] = m_ref;
+                p.ws_ml[((size_t)slot * NCOL + cidx) * 2 + 1] = l;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&c.stats_full);
+    } else {
+        // ================= rescale on request, then the epilogue (warps 0-3) =================
+        const int q = warp;
+        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+        bool ok = true;
+        for (int t = 0; t < ntiles; ++t) {
+            if (!ALLW(ptx::mbar_wait(&c.corr_req[t & 1], (t >> 1) & 1, abort, p.err, 12))) ok = false;
+            const bool do_corr = ok && c.flag[t & 1] != 0;
+            if (do_corr) {
+                if (!ALLW(ptx::mbar_wait(&c.pv_done, (t - 1) & 1, abort, p.err, 13))) ok = false;
                 if (ok) {
                     ptx::tc_fence_after();
-                    uint32_t r0[32], r1[32];
-                    ptx::tmem_ld32(lane_base + TMEM_S + st * 64, r0);
-                    ptx::tmem_ld32(lane_base + TMEM_S + st * 64 + 32, r1);
-                    ptx::tmem_ld_wait();
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&c.s_free[st]);
-                    const int64_t lim = (pos_c + 1 < ke ? pos_c + 1 : ke) - k0;
-                    const int nvalid = active ? (lim < 0 ? 0 : (lim > BK ? BK : (int)lim)) : 0;
-                    float mt = -INFINITY;
+                    for (int jm = 0; jm < 4; ++jm)
+                        for (int h2 = 0; h2 < npv; h2 += 32) {
+                            uint32_t v[32];
+                            const uint32_t a = lane_base + TMEM_O + jm * 64 + h2;
+                            ptx::tmem_ld32(a, v);
+                            ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        x[i] = i < nvalid ? __uint_as_float(r0[i]) * p.scale_log2 : -INFINITY;
-                        x[i + 32] = i + 32 < nvalid ? __uint_as_float(r1[i]) * p.scale_log2 : -INFINITY;
-                        mt = fmaxf(mt, fmaxf(x[i], x[i + 32]));
-                    }
-                    float alpha = 1.f;
-                    if (mt > m_ref + TAU) {
-                        alpha = (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - mt);
-                        m_ref = mt;
-                        l *= alpha;
-                    }
-                    c.alpha[t & 1][cidx] = alpha;
-                    const bool need = (alpha != 1.f) && t > 0;
-                    if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr(&c.flag[t & 1], 1);
+                            for (int k = 0; k < 32; ++k)
+                                v[k] = __float_as_uint(__uint_as_float(v[k]) * c.alpha[t & 1][h2 + k]);
+                            ptx::tmem_st32(a, v);
+                        }
+                    ptx::tmem_st_wait();
+                    ptx::tc_fence_before();
                 }
             }
             if (ptx::named_bar_or(1, 128, !ok || *abort)) {
                 ok = false;
                 break;
             }
-            const bool do_corr = c.flag[t & 1] != 0;
-            if (t >= 1 && (is_sm || do_corr)) {
-                if (!__all_sync(0xffffffffu, ptx::mbar_wait(&c.pv_done, (t - 1) & 1, abort, p.err, 8))) ok = false;
-            }
-            if (ok && do_corr) {
-                ptx::tc_fence_after();
-                for (int jm = 0; jm < 4; ++jm)
-                    for (int h2 = 0; h2 < npv; h2 += 32) {
-                        uint32_t v[32];
-                        const uint32_t a = lane_base + TMEM_O + jm * 64 + h2;
-                        ptx::tmem_ld32(a, v);
-                        ptx::tmem_ld_wait();
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            v[k] = __float_as_uint(__uint_as_float(v[k]) * c.alpha[t & 1][h2 + k]);
-                        ptx::tmem_st32(a, v);
-                    }
-                ptx::tmem_st_wait();
-                ptx::tc_fence_before();
-            }
-            const bool stop = ptx::named_bar_or(2, 128, !ok || *abort);
-            if (threadIdx.x == 0) c.flag[t & 1] = 0;
-            if (stop) {
-                ok = false;
-                break;
-            }
-            if (is_sm) {
-                // P row for this column: p_i = 2^(x_i - m_ref), bf16, 128B-swizzled K-major row
-                const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
-                uint8_t *prow = smem + SMEM_P + cidx * 128;
-                float lsum = 0.f;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int i = ch * 8 + u * 2;
-                        const uint32_t pk = ptx::pack_bf16x2(ptx::ex2(x[i] - mr), ptx::ex2(x[i + 1] - mr));
-                        lsum += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
-                        w[u] = pk;
-                    }
-                    *reinterpret_cast<uint4 *>(prow + ((ch ^ (cidx & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-                l += lsum;
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&c.p_full);
+            if (threadIdx.x == 0) {
+                c.flag[t & 1] = 0;
+                ptx::mbar_arrive(&c.p_full);
             }
         }
-        // ---- epilogue ----
         if (ok && !*abort) {
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&c.pv_done, (ntiles - 1) & 1, abort, p.err, 9))) ok = false;
-        }
-        if (is_sm) {
-            c.row_m[cidx] = m_ref;
-            c.row_inv_l[cidx] = l > 0.f ? 1.f / l : 0.f;
+            // stats_full first: the softmax warps post it only after they saw the
+            // second-to-last PV complete, so pv_done is then at most one phase short of
+            // the last one and its parity wait cannot pass early
+            if (!ALLW(ptx::mbar_wait(&c.stats_full, 0, abort, p.err, 14))) ok = false;
+            if (ok && !ALLW(ptx::mbar_wait(&c.pv_done, (ntiles - 1) & 1, abort, p.err, 9))) ok = false;
         }
         const bool bad = ptx::named_bar_or(1, 128, !ok || *abort);
         if (!bad) {
@@ -404,14 +466,6 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
                         }
                     }
                 }
-            if (is_sm && cidx < ncols) {
-                if (direct) {
-                    if (p.lse) p.lse[(size_t)s * p.ncols + gc] = (m_ref + log2f(l)) * 0.69314718055994531f;
-                } else {
-                    p.ws_ml[((size_t)slot * NCOL + cidx) * 2 + 0] = m_ref;
-                    p.ws_ml[((size_t)slot * NCOL + cidx) * 2 + 1] = l;
-                }
-            }
         }
     }
 
@@ -419,7 +473,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (warp == 5) ptx::tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 7) ptx::tmem_dealloc(tmem, TMEM_COLS);
 }
 
 // Merge a stream's split partials in split-index order:
@@ -427,10 +481,12 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
 //   lse = (M + log2 sum_j w_j l_j) * ln 2.
 // One 128-thread block per (stream, column); each thread owns 4 latent columns.
 __global__ void __launch_bounds__(128) mla_combine_kernel(const __grid_constant__ Params p) {
-    const int s = blockIdx.x / p.ncols;
-    const int gc = blockIdx.x - s * p.ncols;
-    const StreamPlan sp = p.st[s];
+    const int e = blockIdx.y;                 // stream entry (launch order)
+    const StreamPlan sp = p.st[e];
     if (sp.nsplit <= 1) return;
+    const int gc = blockIdx.x;
+    if (gc >= p.ncols) return;
+    const int s = sp.sidx;
     const int g = gc / NCOL, col = gc - g * NCOL;
     const int slot0 = sp.slot0 + g * sp.nsplit;
     float M = -INFINITY;
@@ -458,22 +514,30 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const __grid_constant_
 }
 
 // ---- host-side split plan: a function of the stream's own (len, R, H) only ----
+// Splits are whole multiples of 256 keys: at most 16 splits of 256..1,024 keys for
+// streams up to 16k keys, 1,024-key splits beyond that, and at most 128 splits a
+// stream (a longer split) so the partials stay a few percent of the key bytes.  A
+// prefill chunk with 128 or more column groups is not split at all.
 struct Split {
-    int tiles, tps, nsplit, groups;
+    int64_t split;
+    int nsplit, groups;
 };
 
 inline Split split_of(int64_t len, int R, int H) {
     Split sp;
-    sp.tiles = (int)((len + BK - 1) / BK);
     sp.groups = (R * H + NCOL - 1) / NCOL;
     if (sp.groups >= 128) {
-        sp.tps = sp.tiles;  // enough column groups to fill the GPU: no key split
-    } else {
-        int t = (sp.tiles + 15) / 16;
-        sp.tps = t < 4 ? 4 : (t > 32 ? 32 : t);
+        sp.split = len;
+        sp.nsplit = 1;
+        return sp;
     }
-    if (sp.tps > sp.tiles) sp.tps = sp.tiles;
-    sp.nsplit = (sp.tiles + sp.tps - 1) / sp.tps;
+    const int64_t units = (len + SPLIT_UNIT - 1) / SPLIT_UNIT;
+    int64_t u = (units + 15) / 16;
+    u = u < 1 ? 1 : (u > 4 ? 4 : u);
+    const int64_t cap = (units + 127) / 128;
+    if (cap > u) u = cap;
+    sp.split = u * SPLIT_UNIT;
+    sp.nsplit = (int)((len + sp.split - 1) / sp.split);
     return sp;
 }
 
@@ -543,6 +607,7 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
                   int H, const void *d_q, float scale, void *d_out, float *d_lse, void *d_ws, size_t ws_bytes,
                   cudaStream_t st) {
     using namespace attn;
+    if (prepare_launch(pool, st) != TF_OK) return TF_E_CUDA;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(mla_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) !=
@@ -550,11 +615,10 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
             return TF_E_CUDA;
         attr_set = true;
     }
-    if (prepare_launch(pool, st) != TF_OK) return TF_E_CUDA;
     int rc = ensure_pool_maps(pool);
     if (rc != TF_OK) return rc;
 
-    // Params is large (tensor maps + the per-stream plan); build it on the heap once per thread.
+    // Params is large (tensor maps + the per-stream plan); keep one per host thread.
     thread_local Params *pp = nullptr;
     if (!pp) pp = new Params();
     Params &p = *pp;
@@ -567,6 +631,7 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
         if (!encode(&p.tm_q, const_cast<void *>(d_q), 2, dims, strides, box)) return TF_E_CUDA;
     }
     p.pt = d_pt;
+    p.cache_base = pool->base + (size_t)cache * pool->desc.num_pages * kPageBytes;
     p.out = static_cast<__nv_bfloat16 *>(d_out);
     p.lse = d_lse;
     p.err = pool->err;
@@ -580,18 +645,35 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     p.ncols = R * H;
     p.groups = (R * H + NCOL - 1) / NCOL;
     p.windowed = d_pt ? 0 : 1;
+    // launch order: streams with longer splits first, so short work fills the tail
+    Split sps[TF_MAX_STREAMS];
+    int order[TF_MAX_STREAMS];
+    for (int s = 0; s < S; ++s) {
+        sps[s] = split_of(h_len[s], R, H);
+        order[s] = s;
+    }
+    std::stable_sort(order, order + S, [&](int a, int b) { return sps[a].split > sps[b].split; });
     int items = 0, slots = 0;
     bool any_multi = false;
+    for (int e = 0; e < S; ++e) {
+        const int s = order[e];
+        StreamPlan &sp = p.st[e];
+        sp.len = h_len[s];
+        sp.sidx = s;
+        sp.split = (int32_t)sps[s].split;
+        sp.nsplit = sps[s].nsplit;
+        sp.item0 = items;
+        sp.slot0 = 0;
+        sp.pad = 0;
+        items += sps[s].groups * sps[s].nsplit;
+    }
+    // workspace slots follow the caller's stream order, so their layout does not depend on the launch order
     for (int s = 0; s < S; ++s) {
-        Split sp = split_of(h_len[s], R, H);
-        p.st[s].len = h_len[s];
-        p.st[s].tps = sp.tps;
-        p.st[s].nsplit = sp.nsplit;
-        p.st[s].item0 = items;
-        p.st[s].slot0 = slots;
-        items += sp.groups * sp.nsplit;
-        if (sp.nsplit > 1) {
-            slots += sp.groups * sp.nsplit;
+        int e = 0;
+        while (order[e] != s) ++e;
+        p.st[e].slot0 = slots;
+        if (sps[s].nsplit > 1) {
+            slots += sps[s].groups * sps[s].nsplit;
             any_multi = true;
         }
     }
@@ -607,7 +689,7 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     if (cudaGetLastError() != cudaSuccess) return TF_E_CUDA;
     if (any_multi) {
         ProfScope prof(pool, kProfCombine, st);
-        mla_combine_kernel<<<S * R * H, 128, 0, st>>>(p);
+        mla_combine_kernel<<<dim3(R * H, S), 128, 0, st>>>(p);
         launch_counter()++;
         if (cudaGetLastError() != cudaSuccess) return TF_E_CUDA;
     }

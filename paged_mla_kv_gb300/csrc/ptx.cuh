@@ -54,18 +54,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, for at most ~limit_ns.
-// On expiry: record TF_E_TIMEOUT (detail = site), set *abort, return false.
+// Wait for the phase with the given parity to complete, for at most `limit` SM
+// clock cycles (2^31 by default: about a second at 2 GHz).  The clock is the SM's
+// own cycle counter, read only every 256 polls so the common path is the poll
+// itself.  On expiry: record TF_E_TIMEOUT (detail = site), set *abort, return false.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, DevErr *err,
-                                          int site, uint64_t limit_ns = 1000000000ull) {
+                                          int site, long long limit = (1ll << 31)) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    uint32_t spins = 0;
-    while (true) {
+    const long long t0 = clock64();
+    for (uint32_t spins = 1;; ++spins) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (((++spins) & 63u) == 0) {
+        if ((spins & 255u) == 0) {
             if (*abort) return false;
-            if (globaltimer() - t0 > limit_ns) {
+            if (clock64() - t0 > limit) {
                 record_error(err, TF_E_TIMEOUT, site);
                 *abort = 1;
                 return false;
@@ -136,6 +137,11 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *tm, ui
         " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
         : "memory");
+}
+
+// Prefetch `bytes` (a multiple of 16) of contiguous global memory into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *tm) {
