@@ -175,7 +175,8 @@ int tf_paged_append(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int32_t
  * d_ws: caller workspace of at least tf_paged_mla_workspace_bytes(...) bytes,
  * 256-byte aligned, used for the split partials (fp32); it may be NULL only when
  * that size is 0.  Rows past h_len[s] are never read into the result (they may
- * hold NaN).  Limits: 1 <= S <= TF_MAX_STREAMS, 1 <= H <= TF_MAX_HEADS. */
+ * hold NaN).  Limits: 1 <= S <= TF_MAX_STREAMS, 1 <= H <= TF_MAX_HEADS, scale a
+ * finite number > 0 (TF_E_ARG otherwise). */
 size_t tf_paged_mla_workspace_bytes(int32_t S, int32_t R, int32_t H, const int64_t *h_len);
 
 int tf_paged_mla_attend(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int32_t max_pages,

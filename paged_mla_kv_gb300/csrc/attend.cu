@@ -10,9 +10,9 @@
 // Work unit (one CTA): one stream, a group of up to 64 (row, head) columns, and a
 // split of the stream's keys.  Keys stream through 64-row tiles: 9 boxes of
 // [64 keys x 64 columns] bf16 (8 latent + 1 rope), loaded by TMA with 128-byte
-// swizzle from the tile's pool page into a 2-stage ring; the producer also
-// prefetches the rows of the tiles four ahead into L2 (cp.async.bulk.prefetch), so
-// the shared-memory loads are L2 hits.  The same shared-memory tile feeds both
+// swizzle from the tile's pool page into a 2-stage ring; the rope box is released
+// after QK^T and each latent box pair as soon as its PV M-tile finishes, so the next
+// tile's loads start early.  The same shared-memory tile feeds both
 // contractions on the 5th-generation tensor cores:
 //   S   = Q . K^T     tcgen05.mma M=128 (Q rows; rows 64-127 unused), N=64 keys, K=576,
 //                     Q K-major, the tile K-major; S accumulates in TMEM (2 buffers)
@@ -54,7 +54,6 @@ constexpr int Q_BYTES = NBOX * QBOX_BYTES;      // 73,728
 constexpr int P_BYTES = NCOL * 128;             // 64 rows (columns) of 64 keys, bf16
 constexpr int STAGE_BYTES = NBOX * BOX_BYTES;   // 73,728
 constexpr int NSTAGE = 2;
-constexpr int PREFETCH = 4;                     // tiles prefetched into L2 ahead of the load
 constexpr int SMEM_Q = 0;
 constexpr int SMEM_P = SMEM_Q + Q_BYTES;        // directly after Q: QK^T rows 64-127 of the last box read it
 constexpr int SMEM_KV = SMEM_P + P_BYTES;
@@ -64,12 +63,21 @@ constexpr int TMEM_COLS = 512;
 constexpr int TMEM_O = 0;                       // O^T M-tile j at 64 j (j < 4)
 constexpr int TMEM_S = 256;                     // S buffers at 256 and 320
 constexpr int THREADS = 256;
+// A tile's QK^T runs in two parts: part 0 takes the rope box and latent boxes 0-3,
+// part 1 latent boxes 4-7.  PV of the previous tile is issued between the two parts,
+// so the tensor pipe keeps working while the softmax runs and the previous tile's
+// latent boxes are released (pair by pair) as early as possible for the next loads.
+__device__ __constant__ int kBoxOrder[NBOX] = {8, 0, 1, 2, 3, 4, 5, 6, 7};
+constexpr int kPart0Boxes = 5;
 constexpr int SPLIT_UNIT = 256;                 // split sizes are multiples of this many keys
 constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, BK, false, false);
 static_assert(SPLIT_UNIT % BK == 0, "splits must be tile-aligned");
 
 struct Ctrl {
-    uint64_t kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], s_free[2];
+    uint64_t part_full[NSTAGE][2];     // part 0: rope + latent boxes 0-3 landed; part 1: latent boxes 4-7
+    uint64_t lat_empty[NSTAGE][4];     // latent box pair (2j, 2j+1) free: PV M-tile j done
+    uint64_t rope_empty[NSTAGE];       // rope box free: QK^T done
+    uint64_t s_full[2], s_free[2];
     uint64_t corr_req[2], p_full, pv_done, q_full, stats_full, drain;
     uint32_t tmem_base;
     int abort;
@@ -96,7 +104,6 @@ struct Params {
     CUtensorMap tm_rope;  // 4D {64, 512 rows, pages, caches}, box {64, 32, 1, 1}
     CUtensorMap tm_q;     // 2D {576, S*R*H}, box {64, 64}
     const int32_t *pt;
-    const char *cache_base;   // page 0 of this cache (for the L2 prefetch of raw rows)
     __nv_bfloat16 *out;
     float *lse;
     float *ws_o;          // [slots][64][512]
@@ -154,11 +161,24 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
     const int col0 = g * NCOL;
     const int ncols = min(NCOL, p.ncols - col0);
     const int npv = (ncols + 15) & ~15;
+    // every per-launch scalar the roles use, copied out of the parameter block once
+    const float scale_log2 = p.scale_log2;
+    const int R_ = p.R, H_ = p.H, ncols_all = p.ncols;
+    const int max_pages = p.max_pages, num_pages = p.num_pages, cache = p.cache;
+    const bool windowed = p.windowed != 0;
+    const int32_t *const pt = p.pt;
+    __nv_bfloat16 *const outp = p.out;
+    float *const lsep = p.lse;
+    float *const ws_o = p.ws_o;
+    float *const ws_ml = p.ws_ml;
+    DevErr *const errp = p.err;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSTAGE; ++i) {
-            ptx::mbar_init(&c.kv_full[i], 1);
-            ptx::mbar_init(&c.kv_empty[i], 1);
+            ptx::mbar_init(&c.part_full[i][0], 5);
+            ptx::mbar_init(&c.part_full[i][1], 4);
+            for (int jm = 0; jm < 4; ++jm) ptx::mbar_init(&c.lat_empty[i][jm], 1);
+            ptx::mbar_init(&c.rope_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&c.s_full[i], 1);
@@ -193,130 +213,148 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
             ptx::prefetch_tmap(&p.tm_q);
             const uint64_t pol_kv = ptx::policy_evict_first();
             const uint64_t pol_q = ptx::policy_evict_last();
-            const int qrow = (s * p.R * p.H) + col0;
+            const int qrow = (s * R_ * H_) + col0;
             ptx::mbar_arrive_expect_tx(&c.q_full, Q_BYTES);
             for (int b = 0; b < NBOX; ++b)
                 ptx::tma_load_2d(smem + SMEM_Q + b * QBOX_BYTES, &p.tm_q, &c.q_full, b * 64, qrow, pol_q);
             // page id of a tile's logical page; -1 marks an id outside the pool
             auto page_of = [&](int t) -> int {
                 const int lp = (int)((kb + (int64_t)t * BK) >> 9);
-                const int pg = p.windowed ? s * p.max_pages + lp : __ldg(p.pt + (int64_t)s * p.max_pages + lp);
-                return (pg < 0 || pg >= p.num_pages) ? -1 : pg;
+                const int pg = windowed ? s * max_pages + lp : __ldg(pt + (int64_t)s * max_pages + lp);
+                return (pg < 0 || pg >= num_pages) ? -1 : pg;
             };
-            // L2 prefetch of a tile's rows: 64 latent rows (64 KiB) and 64 rope rows (8 KiB), contiguous
-            int pf_next = 0, pf_lp = -1, pf_page = -1;
-            auto prefetch_upto = [&](int last) {
-                for (; pf_next <= last && pf_next < ntiles; ++pf_next) {
-                    const int64_t k0 = kb + (int64_t)pf_next * BK;
-                    const int lp = (int)(k0 >> 9), row = (int)(k0 & 511);
-                    if (lp != pf_lp) {
-                        pf_page = page_of(pf_next);
-                        pf_lp = lp;
-                    }
-                    if (pf_page < 0) continue;
-                    const char *pg = p.cache_base + (size_t)pf_page * kPageBytes;
-                    ptx::prefetch_l2_bulk(pg + (size_t)row * (kLat * 2), BK * kLat * 2);
-                    ptx::prefetch_l2_bulk(pg + kLatBlockBytes + (size_t)row * (kRope * 2), BK * kRope * 2);
-                }
-            };
-            prefetch_upto(PREFETCH + NSTAGE - 1);
-            int cur_lp = -1, page = 0, issued = 0;
-            for (int t = 0; t < ntiles; ++t) {
+            int armed[NSTAGE][2];   // last tile each part barrier was armed for (-1: never)
+            for (int i = 0; i < NSTAGE; ++i) armed[i][0] = armed[i][1] = -1;
+            int cur_lp = -1, page = 0;
+            bool stop = false;
+            for (int t = 0; t < ntiles && !stop; ++t) {
                 const int st = t % NSTAGE;
-                if (t >= NSTAGE &&
-                    !ptx::mbar_wait(&c.kv_empty[st], ((t / NSTAGE) - 1) & 1, abort, p.err, 1))
-                    break;
-                prefetch_upto(t + PREFETCH + NSTAGE - 1);
+                const uint32_t ph = ((t / NSTAGE) - 1) & 1;
                 const int64_t k0 = kb + (int64_t)t * BK;
                 const int lp = (int)(k0 >> 9), row = (int)(k0 & 511);
                 if (lp != cur_lp) {
                     page = page_of(t);
                     cur_lp = lp;
                     if (page < 0) {
-                        const int raw = p.windowed ? s * p.max_pages + lp : __ldg(p.pt + (int64_t)s * p.max_pages + lp);
-                        ptx::record_error(p.err, TF_E_DEVICE, raw);
+                        const int raw = windowed ? s * max_pages + lp : __ldg(pt + (int64_t)s * max_pages + lp);
+                        ptx::record_error(errp, TF_E_DEVICE, raw);
                         *abort = 1;
                         break;
                     }
                 }
                 uint8_t *dst = smem + SMEM_KV + st * STAGE_BYTES;
-                ptx::mbar_arrive_expect_tx(&c.kv_full[st], STAGE_BYTES);
-                for (int b = 0; b < 8; ++b)
-                    tma_load_4d(dst + b * BOX_BYTES, &p.tm_lat, &c.kv_full[st], b * 64, row, page, p.cache, pol_kv);
-                tma_load_4d(dst + 8 * BOX_BYTES, &p.tm_rope, &c.kv_full[st], 0, row, page, p.cache, pol_kv);
-                issued = t + 1;
+                for (int bi = 0; bi < NBOX; ++bi) {
+                    const int b = kBoxOrder[bi];
+                    if (t >= NSTAGE) {
+                        uint64_t *e = (b == 8) ? &c.rope_empty[st] : &c.lat_empty[st][b >> 1];
+                        if (!ptx::mbar_wait(e, ph, abort, errp, 1)) {
+                            stop = true;
+                            break;
+                        }
+                    }
+                    uint64_t *full = &c.part_full[st][bi < kPart0Boxes ? 0 : 1];
+                    ptx::mbar_arrive_expect_tx(full, BOX_BYTES);
+                    if (b == 8)
+                        tma_load_4d(dst + 8 * BOX_BYTES, &p.tm_rope, full, 0, row, page, cache, pol_kv);
+                    else
+                        tma_load_4d(dst + b * BOX_BYTES, &p.tm_lat, full, b * 64, row, page, cache, pol_kv);
+                    armed[st][bi < kPart0Boxes ? 0 : 1] = t;
+                }
             }
             // no copy may still be writing shared memory when the CTA exits
-            ptx::mbar_wait(&c.q_full, 0, abort, p.err, 10, 1ll << 28);
-            for (int t = max(0, issued - NSTAGE); t < issued; ++t)
-                ptx::mbar_wait(&c.kv_full[t % NSTAGE], (t / NSTAGE) & 1, abort, p.err, 11, 1ll << 28);
+            ptx::mbar_wait(&c.q_full, 0, abort, errp, 10, 1ll << 28);
+            for (int i = 0; i < NSTAGE; ++i)
+                for (int h = 0; h < 2; ++h)
+                    if (armed[i][h] >= 0)
+                        ptx::mbar_wait(&c.part_full[i][h], (armed[i][h] / NSTAGE) & 1, abort, errp, 11, 1ll << 28);
         }
     } else if (warp == 7) {
         // ================= MMA issuer =================
+        // Schedule for tile t:  QK(t+1) part 0  |  PV(t)  |  QK(t+1) part 1.
+        // The order of the contributions inside every accumulator is fixed, so timing
+        // never changes a bit.
         const uint32_t idesc_pv = ptx::idesc_bf16_f32(128, npv, true, false);
         // descriptor bases; per MMA only a constant is added to the start-address field
         const uint64_t q_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_Q), 16, 1024);
         const uint64_t kv_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_KV), 16, 1024);
         const uint64_t v_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_KV), BOX_BYTES, 1024);
         const uint64_t p_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_P), 16, 1024);
-        bool ok = ALLW(ptx::mbar_wait(&c.q_full, 0, abort, p.err, 2));
-        for (int t = 0; ok && t <= ntiles; ++t) {
-            if (t < ntiles) {
-                const int st = t % NSTAGE;
-                if (!ALLW(ptx::mbar_wait(&c.kv_full[st], (t / NSTAGE) & 1, abort, p.err, 3))) break;
-                const int64_t rem = len - (kb + (int64_t)t * BK);
+        // QK^T of tile tq, boxes [b0, b1) of the box order; false if a wait gave up
+        auto qk_part = [&](int tq, int part) -> bool {
+            const int st = tq % NSTAGE;
+            if (part == 0 && tq >= 2 &&
+                !ALLW(ptx::mbar_wait(&c.s_free[tq & 1], ((tq - 2) >> 1) & 1, abort, errp, 4)))
+                return false;
+            if (!ALLW(ptx::mbar_wait(&c.part_full[st][part], (tq / NSTAGE) & 1, abort, errp, 3))) return false;
+            const int b0 = part == 0 ? 0 : kPart0Boxes, b1 = part == 0 ? kPart0Boxes : NBOX;
+            if (tq == ntiles - 1) {
+                const int64_t rem = len - (kb + (int64_t)tq * BK);
                 const int valid = rem < BK ? (int)rem : BK;
                 if (valid < BK) {
                     // rows past the stream's end may hold NaN poison: zero them so that
                     // P = 0 times V stays 0 in the PV contraction
-                    uint4 *base = reinterpret_cast<uint4 *>(smem + SMEM_KV + st * STAGE_BYTES);
-                    const int per_box = (BK - valid) * 8;
-                    for (int k = lane; k < NBOX * per_box; k += 32) {
-                        const int b = k / per_box, w = k - b * per_box;
-                        base[b * (BOX_BYTES / 16) + valid * 8 + w] = make_uint4(0, 0, 0, 0);
+                    for (int bi = b0; bi < b1; ++bi) {
+                        uint4 *bx = reinterpret_cast<uint4 *>(smem + SMEM_KV + st * STAGE_BYTES +
+                                                              kBoxOrder[bi] * BOX_BYTES);
+                        for (int k = lane; k < (BK - valid) * 8; k += 32) bx[valid * 8 + k] = make_uint4(0, 0, 0, 0);
                     }
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                 }
-                if (t >= 2 && !ALLW(ptx::mbar_wait(&c.s_free[t & 1], ((t - 2) >> 1) & 1, abort, p.err, 4))) break;
-                ptx::tc_fence_after();
-                if (lane == 0) {
-                    const uint64_t kvd = kv_desc0 + (uint64_t)(st * (STAGE_BYTES >> 4));
-                    const uint32_t d = tmem + TMEM_S + (t & 1) * BK;
-#pragma unroll
-                    for (int b = 0; b < NBOX; ++b)
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            ptx::mma_bf16_ss(d, q_desc0 + (uint64_t)((b * QBOX_BYTES + k * 32) >> 4),
-                                             kvd + (uint64_t)((b * BOX_BYTES + k * 32) >> 4), IDESC_QK, (b | k) != 0);
-                    ptx::mma_commit(&c.s_full[t & 1]);
-                }
-                __syncwarp();
             }
-            if (t >= 1) {
-                const int tp = t - 1, stp = tp % NSTAGE;
-                if (!ALLW(ptx::mbar_wait(&c.p_full, tp & 1, abort, p.err, 5))) break;
-                ptx::tc_fence_after();
-                if (lane == 0) {
-                    const uint64_t vd = v_desc0 + (uint64_t)(stp * (STAGE_BYTES >> 4));
-                    const uint32_t acc0 = tp > 0 ? 1u : 0u;
+            ptx::tc_fence_after();
+            if (lane == 0) {
+                const uint32_t d = tmem + TMEM_S + (tq & 1) * BK;
+                for (int bi = b0; bi < b1; ++bi) {
+                    const int b = kBoxOrder[bi];
+                    const uint64_t kvd = kv_desc0 + (uint64_t)((st * STAGE_BYTES + b * BOX_BYTES) >> 4);
+                    const uint64_t qd = q_desc0 + (uint64_t)((b * QBOX_BYTES) >> 4);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        ptx::mma_bf16_ss(d, qd + (uint64_t)k * 2, kvd + (uint64_t)k * 2, IDESC_QK,
+                                         (bi == 0 && k == 0) ? 0u : 1u);
+                }
+                if (part == 1) {
+                    ptx::mma_commit(&c.s_full[tq & 1]);
+                    ptx::mma_commit(&c.rope_empty[st]);
+                }
+            }
+            __syncwarp();
+            return true;
+        };
+        // PV of tile tv; the latent box pair of M-tile jm is released as soon as its MMAs finish
+        auto pv = [&](int tv) -> bool {
+            if (!ALLW(ptx::mbar_wait(&c.p_full, tv & 1, abort, errp, 5))) return false;
+            ptx::tc_fence_after();
+            if (lane == 0) {
+                const int st = tv % NSTAGE;
+                const uint64_t vd = v_desc0 + (uint64_t)(st * (STAGE_BYTES >> 4));
+                const uint32_t acc0 = tv > 0 ? 1u : 0u;
+#pragma unroll
+                for (int jm = 0; jm < 4; ++jm) {
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
-#pragma unroll
-                        for (int jm = 0; jm < 4; ++jm)
-                            ptx::mma_bf16_ss(tmem + TMEM_O + jm * 64,
-                                             vd + (uint64_t)((2 * jm * BOX_BYTES + k * 2048) >> 4),
-                                             p_desc0 + (uint64_t)((k * 32) >> 4), idesc_pv, k > 0 ? 1u : acc0);
-                    ptx::mma_commit(&c.pv_done);
-                    ptx::mma_commit(&c.kv_empty[stp]);
+                        ptx::mma_bf16_ss(tmem + TMEM_O + jm * 64, vd + (uint64_t)((2 * jm * BOX_BYTES + k * 2048) >> 4),
+                                         p_desc0 + (uint64_t)((k * 32) >> 4), idesc_pv, k > 0 ? 1u : acc0);
+                    ptx::mma_commit(&c.lat_empty[st][jm]);
                 }
-                __syncwarp();
+                ptx::mma_commit(&c.pv_done);
             }
+            __syncwarp();
+            return true;
+        };
+        bool ok = ALLW(ptx::mbar_wait(&c.q_full, 0, abort, errp, 2));
+        ok = ok && qk_part(0, 0) && qk_part(0, 1);
+        for (int t = 0; ok && t < ntiles; ++t) {
+            const bool next = t + 1 < ntiles;
+            if (next && !qk_part(t + 1, 0)) break;
+            if (!pv(t)) break;
+            if (next && !qk_part(t + 1, 1)) break;
         }
         // drain: no MMA may still run when TMEM is freed
         if (lane == 0) {
             ptx::mma_commit(&c.drain);
-            ptx::mbar_wait(&c.drain, 0, abort, p.err, 6, 1ll << 29);
+            ptx::mbar_wait(&c.drain, 0, abort, errp, 6, 1ll << 29);
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -325,14 +363,14 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
         const int cidx = threadIdx.x - 128;    // column 0..63
         const bool active = cidx < ncols;
         const int gc = col0 + cidx;
-        const int rr = active ? gc / p.H : 0;
-        const int64_t pos_c = len - p.R + rr;  // last visible key of this column
+        const int rr = active ? gc / H_ : 0;
+        const int64_t pos_c = len - R_ + rr;  // last visible key of this column
         const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int t = 0; t < ntiles; ++t) {
             const int64_t k0 = kb + (int64_t)t * BK;
-            if (!ALLW(ptx::mbar_wait(&c.s_full[t & 1], (t >> 1) & 1, abort, p.err, 7))) {
+            if (!ALLW(ptx::mbar_wait(&c.s_full[t & 1], (t >> 1) & 1, abort, errp, 7))) {
                 ok = false;
                 break;
             }
@@ -346,13 +384,17 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
             if (lane == 0) ptx::mbar_arrive(&c.s_free[t & 1]);
             const int64_t lim = (pos_c + 1 < ke ? pos_c + 1 : ke) - k0;
             const int nvalid = active ? (lim < 0 ? 0 : (lim > BK ? BK : (int)lim)) : 0;
+            // raw scores; keys outside this column's range become -inf.  The maximum is
+            // taken before scaling (the scale is positive) and the scale is folded into
+            // the exponent's FFMA: p_i = 2^(s_i * scale*log2(e) - m_ref).
             float x[BK];
-            float mt = -INFINITY;
+            float mraw = -INFINITY;
 #pragma unroll
             for (int i = 0; i < BK; ++i) {
-                x[i] = i < nvalid ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, x[i]);
+                x[i] = i < nvalid ? __uint_as_float(r[i]) : -INFINITY;
+                mraw = fmaxf(mraw, x[i]);
             }
+            const float mt = mraw * scale_log2;
             float alpha = 1.f;
             if (mt > m_ref + TAU) {
                 alpha = (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - mt);
@@ -361,19 +403,22 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
             }
             c.alpha[t & 1][cidx] = alpha;
             if (__any_sync(0xffffffffu, alpha != 1.f && t > 0) && lane == 0) atomicOr(&c.flag[t & 1], 1);
-            // P row for this column: p_i = 2^(x_i - m_ref) as bf16, 8 x 16 B, 128B-swizzled K-major
+            // P row for this column as bf16, 8 x 16 B, 128B-swizzled K-major; l sums the fp32 weights
             const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
             uint32_t pk[BK / 2];
-            float lsum = 0.f;
+            float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
             for (int i = 0; i < BK / 2; ++i) {
-                pk[i] = ptx::pack_bf16x2(ptx::ex2(x[2 * i] - mr), ptx::ex2(x[2 * i + 1] - mr));
-                lsum += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+                const float e0 = ptx::ex2(fmaf(x[2 * i], scale_log2, -mr));
+                const float e1 = ptx::ex2(fmaf(x[2 * i + 1], scale_log2, -mr));
+                ls0 += e0;
+                ls1 += e1;
+                pk[i] = ptx::pack_bf16x2(e0, e1);
             }
-            l += lsum;
+            l += ls0 + ls1;
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&c.corr_req[t & 1]);
-            if (t >= 1 && !ALLW(ptx::mbar_wait(&c.pv_done, (t - 1) & 1, abort, p.err, 8))) {
+            if (t >= 1 && !ALLW(ptx::mbar_wait(&c.pv_done, (t - 1) & 1, abort, errp, 8))) {
                 ok = false;
                 break;
             }
@@ -391,10 +436,10 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
         if (ok && active) {
             const int slot = sp.slot0 + g * sp.nsplit + j;
             if (sp.nsplit == 1) {
-                if (p.lse) p.lse[(size_t)s * p.ncols + gc] = (m_ref + log2f(l)) * 0.69314718055994531f;
+                if (lsep) lsep[(size_t)s * ncols_all + gc] = (m_ref + log2f(l)) * 0.69314718055994531f;
             } else {
-                p.ws_ml[((size_t)slot * NCOL + cidx) * 2 + 0] = m_ref;
-                p.ws_ml[((size_t)slot * NCOL + cidx) * 2 + 1] = l;
+                ws_ml[((size_t)slot * NCOL + cidx) * 2 + 0] = m_ref;
+                ws_ml[((size_t)slot * NCOL + cidx) * 2 + 1] = l;
             }
         }
         __syncwarp();
@@ -405,10 +450,10 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
         const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
         bool ok = true;
         for (int t = 0; t < ntiles; ++t) {
-            if (!ALLW(ptx::mbar_wait(&c.corr_req[t & 1], (t >> 1) & 1, abort, p.err, 12))) ok = false;
+            if (!ALLW(ptx::mbar_wait(&c.corr_req[t & 1], (t >> 1) & 1, abort, errp, 12))) ok = false;
             const bool do_corr = ok && c.flag[t & 1] != 0;
             if (do_corr) {
-                if (!ALLW(ptx::mbar_wait(&c.pv_done, (t - 1) & 1, abort, p.err, 13))) ok = false;
+                if (!ALLW(ptx::mbar_wait(&c.pv_done, (t - 1) & 1, abort, errp, 13))) ok = false;
                 if (ok) {
                     ptx::tc_fence_after();
                     for (int jm = 0; jm < 4; ++jm)
@@ -439,8 +484,8 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
             // stats_full first: the softmax warps post it only after they saw the
             // second-to-last PV complete, so pv_done is then at most one phase short of
             // the last one and its parity wait cannot pass early
-            if (!ALLW(ptx::mbar_wait(&c.stats_full, 0, abort, p.err, 14))) ok = false;
-            if (ok && !ALLW(ptx::mbar_wait(&c.pv_done, (ntiles - 1) & 1, abort, p.err, 9))) ok = false;
+            if (!ALLW(ptx::mbar_wait(&c.stats_full, 0, abort, errp, 14))) ok = false;
+            if (ok && !ALLW(ptx::mbar_wait(&c.pv_done, (ntiles - 1) & 1, abort, errp, 9))) ok = false;
         }
         const bool bad = ptx::named_bar_or(1, 128, !ok || *abort);
         if (!bad) {
@@ -459,10 +504,10 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
                         if (col >= ncols) continue;
                         const float o = __uint_as_float(v[k]);
                         if (direct) {
-                            const size_t orow = (size_t)s * p.ncols + col0 + col;
-                            p.out[orow * kLat + dim] = __float2bfloat16_rn(o * c.row_inv_l[col]);
+                            const size_t orow = (size_t)s * ncols_all + col0 + col;
+                            outp[orow * kLat + dim] = __float2bfloat16_rn(o * c.row_inv_l[col]);
                         } else {
-                            p.ws_o[((size_t)slot * NCOL + col) * kLat + dim] = o;
+                            ws_o[((size_t)slot * NCOL + col) * kLat + dim] = o;
                         }
                     }
                 }
@@ -631,7 +676,6 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
         if (!encode(&p.tm_q, const_cast<void *>(d_q), 2, dims, strides, box)) return TF_E_CUDA;
     }
     p.pt = d_pt;
-    p.cache_base = pool->base + (size_t)cache * pool->desc.num_pages * kPageBytes;
     p.out = static_cast<__nv_bfloat16 *>(d_out);
     p.lse = d_lse;
     p.err = pool->err;

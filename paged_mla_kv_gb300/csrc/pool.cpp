@@ -223,7 +223,7 @@ extern "C" int tf_paged_mla_attend(tf_kvpool *p, int32_t cache, const int32_t *d
     if (!p || !h_len || !d_q || !d_out || S < 1 || S > TF_MAX_STREAMS || R < 1 || H < 1 || H > TF_MAX_HEADS ||
         max_pages < 1)
         return TF_E_ARG;
-    if (!(scale == scale) || scale == 1.0f / 0.0f || scale == -1.0f / 0.0f) return TF_E_ARG;
+    if (!(scale > 0.0f) || scale == 1.0f / 0.0f) return TF_E_ARG;
     if (cache < 0 || cache >= p->desc.num_caches) return TF_E_RANGE;
     if (!d_pt && (int64_t)S * max_pages > p->desc.num_pages) return TF_E_RANGE;
     if ((int64_t)S * R * H > (int64_t)1 << 30) return TF_E_UNSUPPORTED;

@@ -179,6 +179,8 @@ def test_bad_arguments_are_refused_before_launch(L):
     assert _args_refused(L, h, A, 0, fake, 16, lp, 2, 1, 16, fake, float("nan"), fake, None, None, 0,
                          None) == B.TF_E_ARG
     assert _args_refused(L, h, A, 0, fake, 16, lp, 2, 1, 16, None, 0.1, fake, None, None, 0, None) == B.TF_E_ARG
+    assert _args_refused(L, h, A, 0, fake, 16, lp, 2, 1, 16, fake, 0.0, fake, None, None, 0, None) == B.TF_E_ARG
+    assert _args_refused(L, h, A, 0, fake, 16, lp, 2, 1, 16, fake, -0.5, fake, None, None, 0, None) == B.TF_E_ARG
     # a null table needs S * max_pages pool pages
     assert _args_refused(L, h, A, 0, None, 16, lp, 2, 1, 16, fake, 0.1, fake, None, None, 0, None) == B.TF_E_RANGE
     # workspace missing or too small
