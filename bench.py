@@ -53,6 +53,21 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The slowest rank's time: every rank gets the maximum of `value` over the group."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> float:
+    """Units of all ranks (replicas of the same workload) over the slowest rank's time, per second."""
+    return world * units_per_rank / (slowest_ms / 1e3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -282,18 +297,15 @@ def main():
     rc, detail = res.pool.last_error()
     if rc != 0:
         raise SystemExit(f"device error {rc} ({detail})")
-    if pg is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, pg, "cuda")
     ms = total_ms / args.steps
     if prefill:
-        value = world * units["flops"] / (ms / 1e3) / 1e12
+        value = whole_job_rate(units["flops"], world, ms) / 1e12
         unit = "TFLOP/s"
     else:
-        value = world * units["bytes"] / (ms / 1e3) / 1e9
+        value = whole_job_rate(units["bytes"], world, ms) / 1e9
         unit = "GB/s"
-    tokens_s = world * units["tokens"] / (ms / 1e3)
+    tokens_s = whole_job_rate(units["tokens"], world, ms)
 
     # roofline of the dominant kernel (the attention main pass), timed by events on its stream
     avg_att = att_ms / max(att_n, 1)
@@ -340,11 +352,7 @@ def main():
             e2e_step()
             e2[i][1].record()
         barrier()
-        e_ms = sum(a.elapsed_time(b) for a, b in e2) / args.steps
-        if pg is not None:
-            t = torch.tensor([e_ms], dtype=torch.float64, device="cuda")
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2) / args.steps, pg, "cuda")
         h2d = sum(q.numel() * 2 for q in qs) + sum(a.numel() * 2 + b.numel() * 2 for a, b in cur)
         d2h = out.numel() * 2 + lse.numel() * 4
         ev_ = world * (units["flops"] / 1e12 if prefill else units["bytes"] / 1e9) / (e_ms / 1e3)

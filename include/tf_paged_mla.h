@@ -225,6 +225,14 @@ int tf_state_copy_rows(tf_kvpool *pool, int32_t cache, const int32_t *d_src_page
  * offending value (a page id or a wait site). */
 int tf_last_error(tf_kvpool *pool, int64_t *detail);
 
+/* Check that a bounded device wait really ends: launch a one-block kernel that
+ * waits on a barrier nothing completes, with a limit of limit_cycles SM clock
+ * cycles (1 .. 2^32), the same wait every kernel here uses.  The wait gives up,
+ * records TF_E_TIMEOUT (detail 99) in the pool's error word and the kernel returns;
+ * read it with tf_last_error.  No counterpart on the pages: it exercises this
+ * library's own failure path without faulting or hanging the GPU. */
+int tf_diag_wait_timeout(tf_kvpool *pool, int64_t limit_cycles, void *cuda_stream);
+
 /* Kernels this library has launched since the process started. */
 int64_t tf_launch_count(void);
 

@@ -68,6 +68,7 @@ _SIGS = {
     "tf_paged_mla_attend_static": (ctypes.c_int, [_P, _I32, _P, _I32, _P, _I32, _I32, _I32, _P, _F, _P, _P, _P]),
     "tf_state_copy_rows": (ctypes.c_int, [_P, _I32, _P, _P, _I64, _P]),
     "tf_last_error": (ctypes.c_int, [_P, ctypes.POINTER(_I64)]),
+    "tf_diag_wait_timeout": (ctypes.c_int, [_P, _I64, _P]),
     "tf_launch_count": (_I64, []),
     "tf_profile_enable": (ctypes.c_int, [_P, _I32]),
     "tf_profile_read": (ctypes.c_int, [_P, _I32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I64)]),
@@ -252,6 +253,10 @@ def tf_state_copy_rows(pool: KVPool, cache: int, src_pages, dst_pages, at: int, 
     """src_pages / dst_pages: int32 CUDA tensors of ceil(at / 512) page ids."""
     _check(lib().tf_state_copy_rows(pool.handle, cache, _ptr(src_pages), _ptr(dst_pages), int(at),
                                     _stream(stream)), "tf_state_copy_rows")
+
+
+def tf_diag_wait_timeout(pool: KVPool, limit_cycles: int, stream=None) -> None:
+    _check(lib().tf_diag_wait_timeout(pool.handle, int(limit_cycles), _stream(stream)), "tf_diag_wait_timeout")
 
 
 def tf_launch_count() -> int:

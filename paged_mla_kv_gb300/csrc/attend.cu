@@ -152,8 +152,11 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
     const int item = blockIdx.x;
     const StreamPlan sp = p.st[find_entry(p, item)];
     const int s = sp.sidx;
+    // items of a stream run split-major, so the column groups of one split (the rows of
+    // a prefill chunk, the two MTP rows) read the same key tiles at about the same time
+    const int ngroups = (p.ncols + NCOL - 1) / NCOL;
     const int local = item - sp.item0;
-    const int g = local / sp.nsplit, j = local - g * sp.nsplit;
+    const int j = local / ngroups, g = local - j * ngroups;
     const int64_t len = sp.len;
     const int64_t kb = (int64_t)j * sp.split;
     const int64_t ke = min(len, kb + (int64_t)sp.split);
@@ -211,7 +214,9 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
             ptx::prefetch_tmap(&p.tm_lat);
             ptx::prefetch_tmap(&p.tm_rope);
             ptx::prefetch_tmap(&p.tm_q);
-            const uint64_t pol_kv = ptx::policy_evict_first();
+            // a key tile read by one column group streams through L2; tiles that other
+            // groups of the same split read soon after are kept
+            const uint64_t pol_kv = ngroups > 2 ? ptx::policy_evict_last() : ptx::policy_evict_first();
             const uint64_t pol_q = ptx::policy_evict_last();
             const int qrow = (s * R_ * H_) + col0;
             ptx::mbar_arrive_expect_tx(&c.q_full, Q_BYTES);

@@ -152,4 +152,24 @@ int launch_poison(tf_kvpool *pool, const int32_t *h_ids, int n, cudaStream_t st)
     return TF_OK;
 }
 
+// One block waits on a barrier that nothing completes; the bounded wait must give up.
+__global__ void diag_wait_kernel(DevErr *err, long long limit) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        ptx::mbar_init(&bar, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) ptx::mbar_wait(&bar, 0, &abort_flag, err, 99, limit);
+}
+
+int launch_diag_wait(tf_kvpool *pool, long long limit, cudaStream_t st) {
+    if (prepare_launch(pool, st) != TF_OK) return TF_E_CUDA;
+    diag_wait_kernel<<<1, 32, 0, st>>>(pool->err, limit);
+    launch_counter()++;
+    return cudaGetLastError() == cudaSuccess ? TF_OK : TF_E_CUDA;
+}
+
 }  // namespace tf

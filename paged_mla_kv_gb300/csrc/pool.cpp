@@ -262,6 +262,11 @@ extern "C" int tf_last_error(tf_kvpool *p, int64_t *detail) {
     return e.code;
 }
 
+extern "C" int tf_diag_wait_timeout(tf_kvpool *p, int64_t limit_cycles, void *stream) {
+    if (!p || limit_cycles < 1 || limit_cycles > (int64_t(1) << 32)) return TF_E_ARG;
+    return launch_diag_wait(p, (long long)limit_cycles, (cudaStream_t)stream);
+}
+
 extern "C" int64_t tf_launch_count(void) { return launch_counter().load(); }
 
 extern "C" int tf_profile_enable(tf_kvpool *p, int32_t on) {

@@ -255,3 +255,17 @@ def test_repeated_calls_are_bit_identical():
         torch.cuda.synchronize()
         assert np.array_equal(bits(o), ref) and torch.equal(l, l0)
     no_device_error(res.pool)
+
+
+def test_bounded_wait_gives_up_and_the_context_survives():
+    # a wait on a barrier that nothing completes must end, record TF_E_TIMEOUT, and leave
+    # the context usable for the next call
+    w = Y.custom("timeout", 48, lens=[1500], R=1, H=16)
+    res = Resident(w)
+    B.tf_diag_wait_timeout(res.pool, 1 << 20)
+    rc, detail = res.pool.last_error()
+    assert rc == B.TF_E_TIMEOUT and detail == 99
+    out, lse = res.attend(res.q())
+    torch.cuda.synchronize()
+    no_device_error(res.pool)
+    compare(w, out, lse)
