@@ -61,6 +61,8 @@ extern "C" {
 #define TF_MAX_STREAMS 512
 #define TF_MAX_HEADS 128
 #define TF_POOL_POISON 1u      /* fill pages with bf16 NaN (0x7FC0) when they are taken */
+#define TF_POOL_BATCH_INVARIANT 2u  /* attention on this pool: a stream's bits do not depend
+                                       on the other streams of a batch (see tf_paged_mla_attend) */
 
 typedef struct tf_kvpool tf_kvpool;
 
@@ -75,7 +77,7 @@ typedef struct {
     int32_t page_rows;   /* must be 512 */
     int32_t latent_dim;  /* must be 512 */
     int32_t rope_dim;    /* must be 64 */
-    uint32_t flags;      /* TF_POOL_POISON or 0 */
+    uint32_t flags;      /* TF_POOL_POISON | TF_POOL_BATCH_INVARIANT, or 0 */
     uint64_t seed;       /* 0: free pages are handed out in id order; else in a seeded permutation */
 } tf_kvpool_desc;
 
@@ -169,15 +171,24 @@ int tf_paged_append(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int32_t
  * R = 1-2 is decode (MTP drafts); R > 2 is a prefill chunk.  h_len: host int64
  * [S], rows after the current rows were appended, each >= R and <= max_pages * 512.
  * d_q: bf16 [S][R][H][576]; d_out: bf16 [S][R][H][512]; d_lse: fp32 [S][R][H].
- * The keys of a stream are cut into splits whose bounds depend on that stream's
- * length alone, and the splits are merged in index order, so a stream's result
- * does not depend on its pages or on the other streams in the batch.
- * d_ws: caller workspace of at least tf_paged_mla_workspace_bytes(...) bytes,
+ * How the keys are shared out decides the order of the fp32 sums, never which keys
+ * count; a stream's result never depends on which pool pages hold its rows.
+ *  - Default: the key tiles of the batch are cut into near-equal contiguous ranges,
+ *    one a CTA (decode, MTP rows), or whole (stream, head group) units go round
+ *    robin over the CTAs (prefill chunks).  Every SM gets the same work whatever
+ *    the mix of lengths; a stream's bits may differ (within rounding) between
+ *    batches, and are identical between calls on the same batch.
+ *  - Pools made with TF_POOL_BATCH_INVARIANT: each stream's keys are cut into splits
+ *    whose bounds depend on that stream's length alone and merged in split order,
+ *    as the pages' engine does with its fixed key chunks, so a stream attended in a
+ *    batch equals the same stream attended alone, bit for bit.
+ * d_ws: caller workspace of at least tf_paged_mla_workspace_bytes(pool, ...) bytes,
  * 256-byte aligned, used for the split partials (fp32); it may be NULL only when
  * that size is 0.  Rows past h_len[s] are never read into the result (they may
  * hold NaN).  Limits: 1 <= S <= TF_MAX_STREAMS, 1 <= H <= TF_MAX_HEADS, scale a
  * finite number > 0 (TF_E_ARG otherwise). */
-size_t tf_paged_mla_workspace_bytes(int32_t S, int32_t R, int32_t H, const int64_t *h_len);
+size_t tf_paged_mla_workspace_bytes(const tf_kvpool *pool, int32_t S, int32_t R, int32_t H,
+                                    const int64_t *h_len);   /* pool may be NULL: default plan */
 
 int tf_paged_mla_attend(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int32_t max_pages,
                         const int64_t *h_len, int32_t S, int32_t R, int32_t H,
@@ -197,8 +208,11 @@ int tf_paged_mla_attend(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int
  * - The first call on each device looks up the array's device address with that
  *   device current (cudaGetSymbolAddress) and remembers it; make that first call
  *   before any stream capture.
- * - A call whose split partials need more than TF_STATIC_WS_BYTES (see
- *   tf_paged_mla_workspace_bytes) returns TF_E_NOMEM and launches nothing.
+ * - On a default pool the partials are bounded by the launch's CTA ranges (two
+ *   slots of 128 KiB a CTA, at most 240 CTAs), so every valid call fits.  On a
+ *   TF_POOL_BATCH_INVARIANT pool they grow with the lengths; a call that would need
+ *   more than TF_STATIC_WS_BYTES (see tf_paged_mla_workspace_bytes) returns
+ *   TF_E_NOMEM and launches nothing.
  * - Every call shares the one array and it keeps the last call's contents (each
  *   call writes every partial it reads, so nothing has to start at zero).  Calls
  *   that overlap on the GPU -- on two streams, or from two threads -- race on it:

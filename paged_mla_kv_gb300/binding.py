@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libtf_paged_mla.so")
 TF_OK, TF_E_ARG, TF_E_RANGE, TF_E_NOMEM, TF_E_CUDA, TF_E_TIMEOUT, TF_E_UNSUPPORTED, TF_E_DEVICE = \
     0, -1, -2, -3, -4, -5, -6, -7
 TF_POOL_POISON = 1
+TF_POOL_BATCH_INVARIANT = 2
 ERR_NAMES = {0: "TF_OK", -1: "TF_E_ARG", -2: "TF_E_RANGE", -3: "TF_E_NOMEM", -4: "TF_E_CUDA",
              -5: "TF_E_TIMEOUT", -6: "TF_E_UNSUPPORTED", -7: "TF_E_DEVICE"}
 PROF_APPEND, PROF_ATTEND, PROF_COMBINE, PROF_COPY, PROF_POISON = range(5)
@@ -63,7 +64,7 @@ _SIGS = {
     "tf_kvpool_page_ptr": (_P, [_P, _I32, _I32]),
     "tf_kvpool_plan": (ctypes.c_int, [ctypes.POINTER(tf_plan_in), ctypes.POINTER(tf_plan_out)]),
     "tf_paged_append": (ctypes.c_int, [_P, _I32, _P, _I32, _P, _I32, _I32, _P, _P, _P]),
-    "tf_paged_mla_workspace_bytes": (_SZ, [_I32, _I32, _I32, _P]),
+    "tf_paged_mla_workspace_bytes": (_SZ, [_P, _I32, _I32, _I32, _P]),
     "tf_paged_mla_attend": (ctypes.c_int, [_P, _I32, _P, _I32, _P, _I32, _I32, _I32, _P, _F, _P, _P, _P, _SZ, _P]),
     "tf_paged_mla_attend_static": (ctypes.c_int, [_P, _I32, _P, _I32, _P, _I32, _I32, _I32, _P, _F, _P, _P, _P]),
     "tf_state_copy_rows": (ctypes.c_int, [_P, _I32, _P, _P, _I64, _P]),
@@ -114,8 +115,10 @@ def _i64(a):
     return a, a.ctypes.data_as(ctypes.c_void_p)
 
 
-def make_desc(num_caches: int, num_pages: int, poison: bool = False, seed: int = 0) -> tf_kvpool_desc:
-    return tf_kvpool_desc(num_caches, num_pages, 512, 512, 64, TF_POOL_POISON if poison else 0, seed)
+def make_desc(num_caches: int, num_pages: int, poison: bool = False, seed: int = 0,
+              invariant: bool = False) -> tf_kvpool_desc:
+    flags = (TF_POOL_POISON if poison else 0) | (TF_POOL_BATCH_INVARIANT if invariant else 0)
+    return tf_kvpool_desc(num_caches, num_pages, 512, 512, 64, flags, seed)
 
 
 def tf_kvpool_bytes(desc: tf_kvpool_desc) -> int:
@@ -138,8 +141,8 @@ class KVPool:
     """A pool over caller device memory (a torch uint8 tensor kept alive here)."""
 
     def __init__(self, num_caches: int, num_pages: int, poison: bool = False, seed: int = 0, device=None,
-                 memory=None):
-        self.desc = make_desc(num_caches, num_pages, poison, seed)
+                 memory=None, invariant: bool = False):
+        self.desc = make_desc(num_caches, num_pages, poison, seed, invariant)
         self.bytes = tf_kvpool_bytes(self.desc)
         if self.bytes == 0:
             raise TFError(TF_E_ARG, "tf_kvpool_bytes")
@@ -220,9 +223,10 @@ def tf_paged_append(pool: KVPool, cache: int, pt, max_pages: int, pos, latent, r
                                  _stream(stream)), "tf_paged_append")
 
 
-def tf_paged_mla_workspace_bytes(S: int, R: int, H: int, lens) -> int:
+def tf_paged_mla_workspace_bytes(pool, S: int, R: int, H: int, lens) -> int:
+    """Workspace bytes for an attend call on `pool` (a KVPool, or None for the default plan)."""
     a, p = _i64(lens)
-    return int(lib().tf_paged_mla_workspace_bytes(S, R, H, p))
+    return int(lib().tf_paged_mla_workspace_bytes(pool.handle if pool is not None else None, S, R, H, p))
 
 
 def tf_paged_mla_attend(pool: KVPool, cache: int, pt, max_pages: int, lens, q, scale: float, out, lse=None,

@@ -69,39 +69,57 @@ constexpr int THREADS = 256;
 // latent boxes are released (pair by pair) as early as possible for the next loads.
 __device__ __constant__ int kBoxOrder[NBOX] = {8, 0, 1, 2, 3, 4, 5, 6, 7};
 constexpr int kPart0Boxes = 5;
-constexpr int SPLIT_UNIT = 256;                 // split sizes are multiples of this many keys
-constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, BK, false, false);
+constexpr int MIN_TILES = 4;                    // fewest key tiles a CTA is given
+constexpr int SPLIT_UNIT = 256;                 // batch-invariant split sizes are multiples of this
 static_assert(SPLIT_UNIT % BK == 0, "splits must be tile-aligned");
+constexpr int MAX_CTAS = 240;                   // CTAs a launch (one a SM); sizes the workspace
+constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, BK, false, false);
 
 struct Ctrl {
     uint64_t part_full[NSTAGE][2];     // part 0: rope + latent boxes 0-3 landed; part 1: latent boxes 4-7
     uint64_t lat_empty[NSTAGE][4];     // latent box pair (2j, 2j+1) free: PV M-tile j done
     uint64_t rope_empty[NSTAGE];       // rope box free: QK^T done
     uint64_t s_full[2], s_free[2];
-    uint64_t corr_req[2], p_full, pv_done, q_full, stats_full, drain;
+    uint64_t corr_req[2], p_full, pv_done, q_full, q_free, stats_full, drain;
     uint32_t tmem_base;
     int abort;
     int flag[2];
     float alpha[2][NCOL];
-    float row_inv_l[NCOL];
+    float row_inv_l[2][NCOL];          // by segment parity
 };
 constexpr int SMEM_TOTAL = SMEM_CTRL + (int)sizeof(Ctrl) + 1024;
 static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 
-// One entry per stream, in launch order (streams with longer splits first).
+// How the work is dealt out to CTAs (one resident CTA a SM):
+//  - RANGES (few column groups: decode, MTP rows).  The key tiles of the streams are
+//    numbered stream by stream and cut into contiguous, near-equal ranges, so every
+//    SM gets the same number of key tiles whatever the mix of lengths.  Each range is
+//    taken by `rep` = groups CTAs side by side, one column group each, so the groups
+//    of a stream read the same tiles at the same time.  A (stream, group) unit cut by
+//    a range boundary leaves partials that a combine pass merges, in key order.
+//  - UNITS (many column groups: a prefill chunk).  Whole units, round robin over the
+//    CTAs; at any time the CTAs read the same stretch of keys.  No partials.
+//  - SPLITS (a pool made with TF_POOL_BATCH_INVARIANT).  Each stream's keys are cut
+//    into splits whose bounds depend on that stream's length alone, one CTA a
+//    (split, group) item, and the partials are merged in split order, so a stream's
+//    bits do not depend on the other streams of the batch.
+enum { MODE_RANGES = 0, MODE_UNITS = 1, MODE_SPLITS = 2 };
+
+// One entry per stream, in the caller's order.
 struct StreamPlan {
     int64_t len;
-    int32_t sidx;     // the stream's index in the caller's arrays
-    int32_t split;    // keys a split (a multiple of SPLIT_UNIT), or the whole stream
-    int32_t nsplit;   // splits of each column group
-    int32_t item0;    // first work item of this stream
-    int32_t slot0;    // first workspace slot (partials) of this stream
+    int64_t toff;     // RANGES: first numbered key tile of the stream
+    int32_t nt;       // key tiles of the stream
+    int32_t split;    // SPLITS: keys a split (a multiple of SPLIT_UNIT)
+    int32_t nsplit;   // SPLITS: splits of each column group
+    int32_t item0;    // SPLITS: first item of the stream (items are numbered in launch order)
+    int32_t slot0;    // SPLITS: first workspace slot of the stream
     int32_t pad;
 };
 
 struct Params {
-    CUtensorMap tm_lat;   // 4D {512, 512 rows, pages, caches}, box {64, 32, 1, 1}
-    CUtensorMap tm_rope;  // 4D {64, 512 rows, pages, caches}, box {64, 32, 1, 1}
+    CUtensorMap tm_lat;   // 4D {512, 512 rows, pages, caches}, box {64, 64, 1, 1}
+    CUtensorMap tm_rope;  // 4D {64, 512 rows, pages, caches}, box {64, 64, 1, 1}
     CUtensorMap tm_q;     // 2D {576, S*R*H}, box {64, 64}
     const int32_t *pt;
     __nv_bfloat16 *out;
@@ -109,19 +127,111 @@ struct Params {
     float *ws_o;          // [slots][64][512]
     float *ws_ml;         // [slots][64][2]
     DevErr *err;
+    int64_t total;        // RANGES: numbered key tiles; UNITS: units
     float scale_log2;
-    int32_t cache, max_pages, num_pages, S, R, H, ncols, groups, nitems, windowed;
+    int32_t cache, max_pages, num_pages, S, R, H, ncols, groups, windowed;
+    int32_t mode;
+    int32_t nranges;      // RANGES: ranges of the numbering
+    int32_t rep;          // RANGES: CTAs a range (the column groups)
     StreamPlan st[TF_MAX_STREAMS];
+    int16_t order[TF_MAX_STREAMS];   // SPLITS: launch order (streams with longer splits first)
 };
 
-__device__ __forceinline__ int find_entry(const Params &p, int item) {
+// First global tile of CTA i, and the CTA whose range holds global tile x.
+__host__ __device__ __forceinline__ int64_t cta_begin(int64_t i, int64_t total, int n) { return i * total / n; }
+__host__ __device__ __forceinline__ int cta_of(int64_t x, int64_t total, int n) {
+    return (int)(((int64_t)n * (x + 1) - 1) / total);
+}
+
+// A CTA's range, cut at unit boundaries: each piece (a segment) attends one column
+// group of one stream over a contiguous run of key tiles.
+struct Seg {
+    int s, g, nt;
+    int slot;          // workspace slot of a partial result; -1: the segment is its whole unit
+    int64_t kb, ke;    // keys [kb, ke)
+    int64_t len;
+};
+
+__device__ __forceinline__ Seg seg_at(const Params &p, int64_t x, int64_t x0, int64_t x1) {
     int lo = 0, hi = p.S - 1;
     while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (p.st[mid].item0 <= item) lo = mid; else hi = mid - 1;
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.st[mid].toff <= x) lo = mid; else hi = mid - 1;
     }
-    return lo;
+    Seg q;
+    q.s = lo;
+    const int64_t toff = p.st[lo].toff, len = p.st[lo].len;
+    const int nt = p.st[lo].nt;
+    const int64_t u = x - toff;
+    (void)u;
+    q.g = (int)blockIdx.x % p.rep;
+    const int64_t ub = toff, ue = ub + nt;
+    const int64_t tin = x - ub;
+    const int64_t e = ue < x1 ? ue : x1;
+    q.nt = (int)(e - x);
+    q.kb = tin * BK;
+    q.ke = min(len, (tin + q.nt) * BK);
+    q.len = len;
+    // a CTA holds at most two partial segments: its first and its last
+    q.slot = (x == ub && e == ue) ? -1 : 2 * (int)blockIdx.x + (x == x0 ? 0 : 1);
+    return q;
 }
+
+// This CTA's segments, in order, for every mode.
+struct SegIter {
+    int64_t x, x0, x1;
+    int k;
+    __device__ __forceinline__ explicit SegIter(const Params &p) : x(0), x0(0), x1(0), k(0) {
+        if (p.mode == MODE_RANGES) {
+            const int range = (int)blockIdx.x / p.rep;
+            x0 = cta_begin(range, p.total, p.nranges);
+            x1 = cta_begin(range + 1, p.total, p.nranges);
+            x = x0;
+        }
+    }
+    __device__ __forceinline__ bool next(const Params &p, Seg &q) {
+        if (p.mode == MODE_RANGES) {
+            if (x >= x1) return false;
+            q = seg_at(p, x, x0, x1);
+            x += q.nt;
+            return true;
+        }
+        if (p.mode == MODE_UNITS) {
+            const int64_t u = (int64_t)blockIdx.x + (int64_t)k * gridDim.x;
+            if (u >= p.total) return false;
+            ++k;
+            q.s = (int)(u / p.groups);
+            q.g = (int)(u - (int64_t)q.s * p.groups);
+            q.len = p.st[q.s].len;
+            q.nt = p.st[q.s].nt;
+            q.kb = 0;
+            q.ke = q.len;
+            q.slot = -1;
+            return true;
+        }
+        // SPLITS: one item a CTA
+        if (k++ > 0) return false;
+        const int item = (int)blockIdx.x;
+        int lo = 0, hi = p.S - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.st[p.order[mid]].item0 <= item) lo = mid; else hi = mid - 1;
+        }
+        q.s = p.order[lo];
+        const StreamPlan &sp = p.st[q.s];
+        // items of a stream run split-major, so the column groups of one split read the
+        // same key tiles at about the same time
+        const int local = item - sp.item0;
+        const int j = local / p.groups;
+        q.g = local - j * p.groups;
+        q.len = sp.len;
+        q.kb = (int64_t)j * sp.split;
+        q.ke = min(sp.len, q.kb + (int64_t)sp.split);
+        q.nt = (int)((q.ke - q.kb + BK - 1) / BK);
+        q.slot = sp.nsplit > 1 ? sp.slot0 + q.g * sp.nsplit + j : -1;
+        return true;
+    }
+};
 
 __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tm, uint64_t *bar, int c0, int c1, int c2,
                                             int c3, uint64_t policy) {
@@ -137,10 +247,13 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tm, ui
 
 // Barrier phases: a parity wait only tells the current phase from the one before it,
 // so a barrier may be neither two phases ahead of a waiter nor two phases short of
-// the phase it waits for.  corr_req is double-buffered because softmax may post
-// tiles t and t+1 before the rescale group reads t; the epilogue waits stats_full
-// before the last pv_done for the second reason; every other wait follows the
-// waiter's own previous wait on the same barrier.
+// the phase it waits for.  Per-tile barriers count the CTA's tiles across all its
+// segments (gt), per-segment ones (q_full, q_free, stats_full) its segments (si).
+// corr_req is double-buffered because softmax may post tiles t and t+1 before the
+// rescale group reads t; the epilogue waits stats_full before the segment's last
+// pv_done for the second reason; the first PV of a segment cannot start before the
+// rescale group, done with the previous segment's epilogue, posts its p_full, so
+// the accumulator is never overwritten while it is still being read.
 
 __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -148,25 +261,9 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
     Ctrl &c = *reinterpret_cast<Ctrl *>(smem + SMEM_CTRL);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- work item ----
-    const int item = blockIdx.x;
-    const StreamPlan sp = p.st[find_entry(p, item)];
-    const int s = sp.sidx;
-    // items of a stream run split-major, so the column groups of one split (the rows of
-    // a prefill chunk, the two MTP rows) read the same key tiles at about the same time
-    const int ngroups = (p.ncols + NCOL - 1) / NCOL;
-    const int local = item - sp.item0;
-    const int j = local / ngroups, g = local - j * ngroups;
-    const int64_t len = sp.len;
-    const int64_t kb = (int64_t)j * sp.split;
-    const int64_t ke = min(len, kb + (int64_t)sp.split);
-    const int ntiles = (int)((ke - kb + BK - 1) / BK);
-    const int col0 = g * NCOL;
-    const int ncols = min(NCOL, p.ncols - col0);
-    const int npv = (ncols + 15) & ~15;
     // every per-launch scalar the roles use, copied out of the parameter block once
     const float scale_log2 = p.scale_log2;
-    const int R_ = p.R, H_ = p.H, ncols_all = p.ncols;
+    const int R_ = p.R, H_ = p.H, ncols_all = p.ncols, ngroups = p.groups;
     const int max_pages = p.max_pages, num_pages = p.num_pages, cache = p.cache;
     const bool windowed = p.windowed != 0;
     const int32_t *const pt = p.pt;
@@ -192,6 +289,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
         ptx::mbar_init(&c.p_full, 3);
         ptx::mbar_init(&c.pv_done, 1);
         ptx::mbar_init(&c.q_full, 1);
+        ptx::mbar_init(&c.q_free, 1);
         ptx::mbar_init(&c.stats_full, 2);
         ptx::mbar_init(&c.drain, 1);
         c.abort = 0;
@@ -215,59 +313,64 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
             ptx::prefetch_tmap(&p.tm_rope);
             ptx::prefetch_tmap(&p.tm_q);
             // a key tile read by one column group streams through L2; tiles that other
-            // groups of the same split read soon after are kept
+            // groups of the same stream read too are kept
             const uint64_t pol_kv = ngroups > 2 ? ptx::policy_evict_last() : ptx::policy_evict_first();
             const uint64_t pol_q = ptx::policy_evict_last();
-            const int qrow = (s * R_ * H_) + col0;
-            ptx::mbar_arrive_expect_tx(&c.q_full, Q_BYTES);
-            for (int b = 0; b < NBOX; ++b)
-                ptx::tma_load_2d(smem + SMEM_Q + b * QBOX_BYTES, &p.tm_q, &c.q_full, b * 64, qrow, pol_q);
-            // page id of a tile's logical page; -1 marks an id outside the pool
-            auto page_of = [&](int t) -> int {
-                const int lp = (int)((kb + (int64_t)t * BK) >> 9);
-                const int pg = windowed ? s * max_pages + lp : __ldg(pt + (int64_t)s * max_pages + lp);
-                return (pg < 0 || pg >= num_pages) ? -1 : pg;
-            };
-            int armed[NSTAGE][2];   // last tile each part barrier was armed for (-1: never)
+            int armed[NSTAGE][2];   // last global tile each part barrier was armed for (-1: never)
             for (int i = 0; i < NSTAGE; ++i) armed[i][0] = armed[i][1] = -1;
-            int cur_lp = -1, page = 0;
+            int q_armed = -1;       // last segment whose queries were loaded
             bool stop = false;
-            for (int t = 0; t < ntiles && !stop; ++t) {
-                const int st = t % NSTAGE;
-                const uint32_t ph = ((t / NSTAGE) - 1) & 1;
-                const int64_t k0 = kb + (int64_t)t * BK;
-                const int lp = (int)(k0 >> 9), row = (int)(k0 & 511);
-                if (lp != cur_lp) {
-                    page = page_of(t);
-                    cur_lp = lp;
-                    if (page < 0) {
-                        const int raw = windowed ? s * max_pages + lp : __ldg(pt + (int64_t)s * max_pages + lp);
-                        ptx::record_error(errp, TF_E_DEVICE, raw);
-                        *abort = 1;
-                        break;
-                    }
-                }
-                uint8_t *dst = smem + SMEM_KV + st * STAGE_BYTES;
-                for (int bi = 0; bi < NBOX; ++bi) {
-                    const int b = kBoxOrder[bi];
-                    if (t >= NSTAGE) {
-                        uint64_t *e = (b == 8) ? &c.rope_empty[st] : &c.lat_empty[st][b >> 1];
-                        if (!ptx::mbar_wait(e, ph, abort, errp, 1)) {
+            int gt = 0, si = 0;
+            SegIter it(p);
+            Seg q;
+            for (; !stop && it.next(p, q); ++si) {
+                // the query tile is reloaded once the previous segment's QK^T has read it
+                if (si > 0 && !ptx::mbar_wait(&c.q_free, (si - 1) & 1, abort, errp, 15)) break;
+                ptx::mbar_arrive_expect_tx(&c.q_full, Q_BYTES);
+                const int qrow = q.s * R_ * H_ + q.g * NCOL;
+                for (int b = 0; b < NBOX; ++b)
+                    ptx::tma_load_2d(smem + SMEM_Q + b * QBOX_BYTES, &p.tm_q, &c.q_full, b * 64, qrow, pol_q);
+                q_armed = si;
+                int cur_lp = -1, page = 0;
+                for (int tl = 0; tl < q.nt; ++tl, ++gt) {
+                    const int st = gt % NSTAGE;
+                    const uint32_t ph = ((gt / NSTAGE) - 1) & 1;
+                    const int64_t k0 = q.kb + (int64_t)tl * BK;
+                    const int lp = (int)(k0 >> 9), row = (int)(k0 & 511);
+                    if (lp != cur_lp) {
+                        const int raw = windowed ? q.s * max_pages + lp : __ldg(pt + (int64_t)q.s * max_pages + lp);
+                        cur_lp = lp;
+                        if (raw < 0 || raw >= num_pages) {
+                            ptx::record_error(errp, TF_E_DEVICE, raw);
+                            *abort = 1;
                             stop = true;
                             break;
                         }
+                        page = raw;
                     }
-                    uint64_t *full = &c.part_full[st][bi < kPart0Boxes ? 0 : 1];
-                    ptx::mbar_arrive_expect_tx(full, BOX_BYTES);
-                    if (b == 8)
-                        tma_load_4d(dst + 8 * BOX_BYTES, &p.tm_rope, full, 0, row, page, cache, pol_kv);
-                    else
-                        tma_load_4d(dst + b * BOX_BYTES, &p.tm_lat, full, b * 64, row, page, cache, pol_kv);
-                    armed[st][bi < kPart0Boxes ? 0 : 1] = t;
+                    uint8_t *dst = smem + SMEM_KV + st * STAGE_BYTES;
+                    for (int bi = 0; bi < NBOX; ++bi) {
+                        const int b = kBoxOrder[bi];
+                        if (gt >= NSTAGE) {
+                            uint64_t *e = (b == 8) ? &c.rope_empty[st] : &c.lat_empty[st][b >> 1];
+                            if (!ptx::mbar_wait(e, ph, abort, errp, 1)) {
+                                stop = true;
+                                break;
+                            }
+                        }
+                        uint64_t *full = &c.part_full[st][bi < kPart0Boxes ? 0 : 1];
+                        ptx::mbar_arrive_expect_tx(full, BOX_BYTES);
+                        if (b == 8)
+                            tma_load_4d(dst + 8 * BOX_BYTES, &p.tm_rope, full, 0, row, page, cache, pol_kv);
+                        else
+                            tma_load_4d(dst + b * BOX_BYTES, &p.tm_lat, full, b * 64, row, page, cache, pol_kv);
+                        armed[st][bi < kPart0Boxes ? 0 : 1] = gt;
+                    }
+                    if (stop) break;
                 }
             }
             // no copy may still be writing shared memory when the CTA exits
-            ptx::mbar_wait(&c.q_full, 0, abort, errp, 10, 1ll << 28);
+            if (q_armed >= 0) ptx::mbar_wait(&c.q_full, q_armed & 1, abort, errp, 10, 1ll << 28);
             for (int i = 0; i < NSTAGE; ++i)
                 for (int h = 0; h < 2; ++h)
                     if (armed[i][h] >= 0)
@@ -275,37 +378,33 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
         }
     } else if (warp == 7) {
         // ================= MMA issuer =================
-        // Schedule for tile t:  QK(t+1) part 0  |  PV(t)  |  QK(t+1) part 1.
+        // Schedule for tile t of a segment:  QK(t+1) part 0  |  PV(t)  |  QK(t+1) part 1.
         // The order of the contributions inside every accumulator is fixed, so timing
         // never changes a bit.
-        const uint32_t idesc_pv = ptx::idesc_bf16_f32(128, npv, true, false);
-        // descriptor bases; per MMA only a constant is added to the start-address field
         const uint64_t q_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_Q), 16, 1024);
         const uint64_t kv_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_KV), 16, 1024);
         const uint64_t v_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_KV), BOX_BYTES, 1024);
         const uint64_t p_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_P), 16, 1024);
-        // QK^T of tile tq, boxes [b0, b1) of the box order; false if a wait gave up
-        auto qk_part = [&](int tq, int part) -> bool {
+        // QK^T of global tile tq (keys from k0), boxes of one part; `last` marks the
+        // segment's last tile; false if a wait gave up
+        auto qk_part = [&](int tq, int part, int64_t k0, int64_t len, bool last) -> bool {
             const int st = tq % NSTAGE;
             if (part == 0 && tq >= 2 &&
                 !ALLW(ptx::mbar_wait(&c.s_free[tq & 1], ((tq - 2) >> 1) & 1, abort, errp, 4)))
                 return false;
             if (!ALLW(ptx::mbar_wait(&c.part_full[st][part], (tq / NSTAGE) & 1, abort, errp, 3))) return false;
             const int b0 = part == 0 ? 0 : kPart0Boxes, b1 = part == 0 ? kPart0Boxes : NBOX;
-            if (tq == ntiles - 1) {
-                const int64_t rem = len - (kb + (int64_t)tq * BK);
-                const int valid = rem < BK ? (int)rem : BK;
-                if (valid < BK) {
-                    // rows past the stream's end may hold NaN poison: zero them so that
-                    // P = 0 times V stays 0 in the PV contraction
-                    for (int bi = b0; bi < b1; ++bi) {
-                        uint4 *bx = reinterpret_cast<uint4 *>(smem + SMEM_KV + st * STAGE_BYTES +
-                                                              kBoxOrder[bi] * BOX_BYTES);
-                        for (int k = lane; k < (BK - valid) * 8; k += 32) bx[valid * 8 + k] = make_uint4(0, 0, 0, 0);
-                    }
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
+            const int64_t rem = len - k0;
+            if (rem < BK) {
+                // rows past the stream's end may hold NaN poison: zero them so that
+                // P = 0 times V stays 0 in the PV contraction
+                const int valid = (int)rem;
+                for (int bi = b0; bi < b1; ++bi) {
+                    uint4 *bx = reinterpret_cast<uint4 *>(smem + SMEM_KV + st * STAGE_BYTES + kBoxOrder[bi] * BOX_BYTES);
+                    for (int k = lane; k < (BK - valid) * 8; k += 32) bx[valid * 8 + k] = make_uint4(0, 0, 0, 0);
                 }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
             }
             ptx::tc_fence_after();
             if (lane == 0) {
@@ -322,19 +421,21 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
                 if (part == 1) {
                     ptx::mma_commit(&c.s_full[tq & 1]);
                     ptx::mma_commit(&c.rope_empty[st]);
+                    if (last) ptx::mma_commit(&c.q_free);
                 }
             }
             __syncwarp();
             return true;
         };
-        // PV of tile tv; the latent box pair of M-tile jm is released as soon as its MMAs finish
-        auto pv = [&](int tv) -> bool {
+        // PV of global tile tv; the latent box pair of M-tile jm is released as soon as
+        // its MMAs finish; the first tile of a segment starts the accumulator afresh
+        auto pv = [&](int tv, bool first, uint32_t idesc_pv) -> bool {
             if (!ALLW(ptx::mbar_wait(&c.p_full, tv & 1, abort, errp, 5))) return false;
             ptx::tc_fence_after();
             if (lane == 0) {
                 const int st = tv % NSTAGE;
                 const uint64_t vd = v_desc0 + (uint64_t)(st * (STAGE_BYTES >> 4));
-                const uint32_t acc0 = tv > 0 ? 1u : 0u;
+                const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
                 for (int jm = 0; jm < 4; ++jm) {
 #pragma unroll
@@ -348,13 +449,24 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
             __syncwarp();
             return true;
         };
-        bool ok = ALLW(ptx::mbar_wait(&c.q_full, 0, abort, errp, 2));
-        ok = ok && qk_part(0, 0) && qk_part(0, 1);
-        for (int t = 0; ok && t < ntiles; ++t) {
-            const bool next = t + 1 < ntiles;
-            if (next && !qk_part(t + 1, 0)) break;
-            if (!pv(t)) break;
-            if (next && !qk_part(t + 1, 1)) break;
+        bool ok = true;
+        int gt = 0, si = 0;
+        SegIter it(p);
+        Seg q;
+        for (; ok && it.next(p, q); ++si) {
+            const int ncols = min(NCOL, ncols_all - q.g * NCOL);
+            const uint32_t idesc_pv = ptx::idesc_bf16_f32(128, (ncols + 15) & ~15, true, false);
+            ok = ALLW(ptx::mbar_wait(&c.q_full, si & 1, abort, errp, 2));
+            ok = ok && qk_part(gt, 0, q.kb, q.len, q.nt == 1) && qk_part(gt, 1, q.kb, q.len, q.nt == 1);
+            for (int tl = 0; ok && tl < q.nt; ++tl) {
+                const bool next = tl + 1 < q.nt;
+                const int64_t kn = q.kb + (int64_t)(tl + 1) * BK;
+                const bool nlast = tl + 2 == q.nt;
+                if (next && !qk_part(gt + tl + 1, 0, kn, q.len, nlast)) ok = false;
+                if (ok && !pv(gt + tl, tl == 0, idesc_pv)) ok = false;
+                if (ok && next && !qk_part(gt + tl + 1, 1, kn, q.len, nlast)) ok = false;
+            }
+            gt += q.nt;
         }
         // drain: no MMA may still run when TMEM is freed
         if (lane == 0) {
@@ -364,158 +476,178 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
         __syncwarp();
     } else if (warp >= 4) {
         // ================= softmax (warps 4-5: S rows 0-63) =================
-        const int q = warp & 3;
-        const int cidx = threadIdx.x - 128;    // column 0..63
-        const bool active = cidx < ncols;
-        const int gc = col0 + cidx;
-        const int rr = active ? gc / H_ : 0;
-        const int64_t pos_c = len - R_ + rr;  // last visible key of this column
-        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-        float m_ref = -INFINITY, l = 0.f;
+        const int q4 = warp & 3;
+        const int cidx = threadIdx.x - 128;    // column 0..63 of the group
+        const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
         bool ok = true;
-        for (int t = 0; t < ntiles; ++t) {
-            const int64_t k0 = kb + (int64_t)t * BK;
-            if (!ALLW(ptx::mbar_wait(&c.s_full[t & 1], (t >> 1) & 1, abort, errp, 7))) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            uint32_t r[BK];
-            ptx::tmem_ld32(lane_base + TMEM_S + (t & 1) * BK, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-            ptx::tmem_ld32(lane_base + TMEM_S + (t & 1) * BK + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-            ptx::tmem_ld_wait();
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&c.s_free[t & 1]);
-            const int64_t lim = (pos_c + 1 < ke ? pos_c + 1 : ke) - k0;
-            const int nvalid = active ? (lim < 0 ? 0 : (lim > BK ? BK : (int)lim)) : 0;
-            // raw scores; keys outside this column's range become -inf.  The maximum is
-            // taken before scaling (the scale is positive) and the scale is folded into
-            // the exponent's FFMA: p_i = 2^(s_i * scale*log2(e) - m_ref).
-            float x[BK];
-            float mraw = -INFINITY;
+        int gt = 0, si = 0;
+        SegIter it(p);
+        Seg q;
+        for (; ok && it.next(p, q); ++si) {
+            const int col0 = q.g * NCOL;
+            const bool active = cidx < ncols_all - col0;
+            const int gc = col0 + cidx;
+            const int rr = active ? gc / H_ : 0;
+            const int64_t pos_c = q.len - R_ + rr;  // last visible key of this column
+            float m_ref = -INFINITY, l = 0.f;
+            for (int tl = 0; tl < q.nt; ++tl) {
+                const int t = gt + tl;
+                const int64_t k0 = q.kb + (int64_t)tl * BK;
+                if (!ALLW(ptx::mbar_wait(&c.s_full[t & 1], (t >> 1) & 1, abort, errp, 7))) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                uint32_t r[BK];
+                ptx::tmem_ld32(lane_base + TMEM_S + (t & 1) * BK, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                ptx::tmem_ld32(lane_base + TMEM_S + (t & 1) * BK + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                ptx::tmem_ld_wait();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&c.s_free[t & 1]);
+                const int64_t lim = (pos_c + 1 < q.ke ? pos_c + 1 : q.ke) - k0;
+                const int nvalid = active ? (lim < 0 ? 0 : (lim > BK ? BK : (int)lim)) : 0;
+                // raw scores; keys outside this column's range become -inf.  The maximum is
+                // taken before scaling (the scale is positive) and the scale is folded into
+                // the exponent's FFMA: p_i = 2^(s_i * scale*log2(e) - m_ref).
+                float xs[BK];
+                float mraw = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < BK; ++i) {
-                x[i] = i < nvalid ? __uint_as_float(r[i]) : -INFINITY;
-                mraw = fmaxf(mraw, x[i]);
-            }
-            const float mt = mraw * scale_log2;
-            float alpha = 1.f;
-            if (mt > m_ref + TAU) {
-                alpha = (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - mt);
-                m_ref = mt;
-                l *= alpha;
-            }
-            c.alpha[t & 1][cidx] = alpha;
-            if (__any_sync(0xffffffffu, alpha != 1.f && t > 0) && lane == 0) atomicOr(&c.flag[t & 1], 1);
-            // P row for this column as bf16, 8 x 16 B, 128B-swizzled K-major; l sums the fp32 weights
-            const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
-            uint32_t pk[BK / 2];
-            float ls0 = 0.f, ls1 = 0.f;
+                for (int i = 0; i < BK; ++i) {
+                    xs[i] = i < nvalid ? __uint_as_float(r[i]) : -INFINITY;
+                    mraw = fmaxf(mraw, xs[i]);
+                }
+                const float mt = mraw * scale_log2;
+                float alpha = 1.f;
+                if (mt > m_ref + TAU) {
+                    alpha = (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - mt);
+                    m_ref = mt;
+                    l *= alpha;
+                }
+                c.alpha[t & 1][cidx] = alpha;
+                if (__any_sync(0xffffffffu, alpha != 1.f && tl > 0) && lane == 0) atomicOr(&c.flag[t & 1], 1);
+                // P row for this column as bf16, 8 x 16 B, 128B-swizzled K-major; l sums the fp32 weights
+                const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
+                uint32_t pk[BK / 2];
+                float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < BK / 2; ++i) {
-                const float e0 = ptx::ex2(fmaf(x[2 * i], scale_log2, -mr));
-                const float e1 = ptx::ex2(fmaf(x[2 * i + 1], scale_log2, -mr));
-                ls0 += e0;
-                ls1 += e1;
-                pk[i] = ptx::pack_bf16x2(e0, e1);
-            }
-            l += ls0 + ls1;
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&c.corr_req[t & 1]);
-            if (t >= 1 && !ALLW(ptx::mbar_wait(&c.pv_done, (t - 1) & 1, abort, errp, 8))) {
-                ok = false;
-                break;
-            }
-            uint8_t *prow = smem + SMEM_P + cidx * 128;
+                for (int i = 0; i < BK / 2; ++i) {
+                    const float e0 = ptx::ex2(fmaf(xs[2 * i], scale_log2, -mr));
+                    const float e1 = ptx::ex2(fmaf(xs[2 * i + 1], scale_log2, -mr));
+                    ls0 += e0;
+                    ls1 += e1;
+                    pk[i] = ptx::pack_bf16x2(e0, e1);
+                }
+                l += ls0 + ls1;
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&c.corr_req[t & 1]);
+                if (t >= 1 && !ALLW(ptx::mbar_wait(&c.pv_done, (t - 1) & 1, abort, errp, 8))) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *prow = smem + SMEM_P + cidx * 128;
 #pragma unroll
-            for (int ch = 0; ch < BK / 8; ++ch)
-                *reinterpret_cast<uint4 *>(prow + ((ch ^ (cidx & 7)) << 4)) =
-                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            ptx::fence_proxy_async_smem();
+                for (int ch = 0; ch < BK / 8; ++ch)
+                    *reinterpret_cast<uint4 *>(prow + ((ch ^ (cidx & 7)) << 4)) =
+                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&c.p_full);
+            }
+            if (!ok) break;
+            // statistics for the epilogue
+            c.row_inv_l[si & 1][cidx] = l > 0.f ? 1.f / l : 0.f;
+            if (active) {
+                if (q.slot < 0) {
+                    if (lsep) lsep[(size_t)q.s * ncols_all + gc] = (m_ref + log2f(l)) * 0.69314718055994531f;
+                } else {
+                    ws_ml[((size_t)q.slot * NCOL + cidx) * 2 + 0] = m_ref;
+                    ws_ml[((size_t)q.slot * NCOL + cidx) * 2 + 1] = l;
+                }
+            }
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&c.p_full);
+            if (lane == 0) ptx::mbar_arrive(&c.stats_full);
+            gt += q.nt;
         }
-        // statistics for the epilogue
-        c.row_inv_l[cidx] = l > 0.f ? 1.f / l : 0.f;
-        if (ok && active) {
-            const int slot = sp.slot0 + g * sp.nsplit + j;
-            if (sp.nsplit == 1) {
-                if (lsep) lsep[(size_t)s * ncols_all + gc] = (m_ref + log2f(l)) * 0.69314718055994531f;
-            } else {
-                ws_ml[((size_t)slot * NCOL + cidx) * 2 + 0] = m_ref;
-                ws_ml[((size_t)slot * NCOL + cidx) * 2 + 1] = l;
-            }
-        }
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&c.stats_full);
     } else {
         // ================= rescale on request, then the epilogue (warps 0-3) =================
-        const int q = warp;
-        const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+        const int q4 = warp;
+        const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
         bool ok = true;
-        for (int t = 0; t < ntiles; ++t) {
-            if (!ALLW(ptx::mbar_wait(&c.corr_req[t & 1], (t >> 1) & 1, abort, errp, 12))) ok = false;
-            const bool do_corr = ok && c.flag[t & 1] != 0;
-            if (do_corr) {
-                if (!ALLW(ptx::mbar_wait(&c.pv_done, (t - 1) & 1, abort, errp, 13))) ok = false;
-                if (ok) {
-                    ptx::tc_fence_after();
-                    for (int jm = 0; jm < 4; ++jm)
-                        for (int h2 = 0; h2 < npv; h2 += 32) {
-                            uint32_t v[32];
-                            const uint32_t a = lane_base + TMEM_O + jm * 64 + h2;
-                            ptx::tmem_ld32(a, v);
-                            ptx::tmem_ld_wait();
+        int gt = 0, si = 0;
+        SegIter it(p);
+        Seg q;
+        for (; ok && it.next(p, q); ++si) {
+            const int col0 = q.g * NCOL;
+            const int ncols = min(NCOL, ncols_all - col0);
+            const int npv = (ncols + 15) & ~15;
+            for (int tl = 0; tl < q.nt; ++tl) {
+                const int t = gt + tl;
+                if (!ALLW(ptx::mbar_wait(&c.corr_req[t & 1], (t >> 1) & 1, abort, errp, 12))) ok = false;
+                const bool do_corr = ok && c.flag[t & 1] != 0;
+                if (do_corr) {
+                    if (!ALLW(ptx::mbar_wait(&c.pv_done, (t - 1) & 1, abort, errp, 13))) ok = false;
+                    if (ok) {
+                        ptx::tc_fence_after();
+                        for (int jm = 0; jm < 4; ++jm)
+                            for (int h2 = 0; h2 < npv; h2 += 32) {
+                                uint32_t v[32];
+                                const uint32_t a = lane_base + TMEM_O + jm * 64 + h2;
+                                ptx::tmem_ld32(a, v);
+                                ptx::tmem_ld_wait();
 #pragma unroll
-                            for (int k = 0; k < 32; ++k)
-                                v[k] = __float_as_uint(__uint_as_float(v[k]) * c.alpha[t & 1][h2 + k]);
-                            ptx::tmem_st32(a, v);
-                        }
-                    ptx::tmem_st_wait();
-                    ptx::tc_fence_before();
+                                for (int k = 0; k < 32; ++k)
+                                    v[k] = __float_as_uint(__uint_as_float(v[k]) * c.alpha[t & 1][h2 + k]);
+                                ptx::tmem_st32(a, v);
+                            }
+                        ptx::tmem_st_wait();
+                    }
                 }
+                // also orders the previous segment's epilogue reads of the accumulator
+                // before the PV that starts it afresh
+                ptx::tc_fence_before();
+                if (ptx::named_bar_or(1, 128, !ok || *abort)) {
+                    ok = false;
+                    break;
+                }
+                if (threadIdx.x == 0) {
+                    c.flag[t & 1] = 0;
+                    ptx::mbar_arrive(&c.p_full);
+                }
+            }
+            if (ok && !*abort) {
+                // stats_full first: the softmax warps post it only after they saw the
+                // second-to-last PV of the segment complete, so pv_done is then at most one
+                // phase short of the last one and its parity wait cannot pass early
+                if (!ALLW(ptx::mbar_wait(&c.stats_full, si & 1, abort, errp, 14))) ok = false;
+                if (ok && !ALLW(ptx::mbar_wait(&c.pv_done, (gt + q.nt - 1) & 1, abort, errp, 9))) ok = false;
             }
             if (ptx::named_bar_or(1, 128, !ok || *abort)) {
                 ok = false;
                 break;
             }
-            if (threadIdx.x == 0) {
-                c.flag[t & 1] = 0;
-                ptx::mbar_arrive(&c.p_full);
-            }
-        }
-        if (ok && !*abort) {
-            // stats_full first: the softmax warps post it only after they saw the
-            // second-to-last PV complete, so pv_done is then at most one phase short of
-            // the last one and its parity wait cannot pass early
-            if (!ALLW(ptx::mbar_wait(&c.stats_full, 0, abort, errp, 14))) ok = false;
-            if (ok && !ALLW(ptx::mbar_wait(&c.pv_done, (ntiles - 1) & 1, abort, errp, 9))) ok = false;
-        }
-        const bool bad = ptx::named_bar_or(1, 128, !ok || *abort);
-        if (!bad) {
             ptx::tc_fence_after();
-            const bool direct = sp.nsplit == 1;
-            const int slot = sp.slot0 + g * sp.nsplit + j;
+            const float *inv_l = c.row_inv_l[si & 1];
             for (int jm = 0; jm < 4; ++jm)
                 for (int h2 = 0; h2 < npv; h2 += 32) {
                     uint32_t v[32];
                     ptx::tmem_ld32(lane_base + TMEM_O + jm * 64 + h2, v);
                     ptx::tmem_ld_wait();
-                    const int dim = jm * 128 + q * 32 + lane;
+                    const int dim = jm * 128 + q4 * 32 + lane;
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
                         const int col = h2 + k;
                         if (col >= ncols) continue;
                         const float o = __uint_as_float(v[k]);
-                        if (direct) {
-                            const size_t orow = (size_t)s * ncols_all + col0 + col;
-                            outp[orow * kLat + dim] = __float2bfloat16_rn(o * c.row_inv_l[col]);
+                        if (q.slot < 0) {
+                            const size_t orow = (size_t)q.s * ncols_all + col0 + col;
+                            outp[orow * kLat + dim] = __float2bfloat16_rn(o * inv_l[col]);
                         } else {
-                            ws_o[((size_t)slot * NCOL + col) * kLat + dim] = o;
+                            ws_o[((size_t)q.slot * NCOL + col) * kLat + dim] = o;
                         }
                     }
                 }
+            gt += q.nt;
         }
     }
 
@@ -526,26 +658,39 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
     if (warp == 7) ptx::tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// Merge a stream's split partials in split-index order:
+// Merge a unit's partials, CTA range by CTA range (that is, in key order):
 //   M = max_j m_j,  w_j = 2^(m_j - M),  out = sum_j w_j o_j / sum_j w_j l_j,
 //   lse = (M + log2 sum_j w_j l_j) * ln 2.
 // One 128-thread block per (stream, column); each thread owns 4 latent columns.
 __global__ void __launch_bounds__(128) mla_combine_kernel(const __grid_constant__ Params p) {
-    const int e = blockIdx.y;                 // stream entry (launch order)
-    const StreamPlan sp = p.st[e];
-    if (sp.nsplit <= 1) return;
+    const int s = blockIdx.y;
     const int gc = blockIdx.x;
     if (gc >= p.ncols) return;
-    const int s = sp.sidx;
+    const StreamPlan &sp = p.st[s];
     const int g = gc / NCOL, col = gc - g * NCOL;
-    const int slot0 = sp.slot0 + g * sp.nsplit;
+    int c0, c1, first_slot;
+    if (p.mode == MODE_RANGES) {
+        // the ranges that hold the unit; their CTAs' partial slots
+        const int64_t ub = sp.toff, ue = ub + sp.nt;
+        c0 = cta_of(ub, p.total, p.nranges);
+        c1 = cta_of(ue - 1, p.total, p.nranges);
+        first_slot = 2 * (c0 * p.rep + g) + (ub == cta_begin(c0, p.total, p.nranges) ? 0 : 1);
+    } else {
+        if (p.mode != MODE_SPLITS || sp.nsplit <= 1) return;
+        c0 = 0;
+        c1 = sp.nsplit - 1;
+        first_slot = sp.slot0 + g * sp.nsplit;
+    }
+    if (c0 == c1) return;
+    const bool ranges = p.mode == MODE_RANGES;
+    auto slot_of = [&](int cc) { return cc == c0 ? first_slot : ranges ? 2 * (cc * p.rep + g) : first_slot + cc; };
     float M = -INFINITY;
-    for (int jx = 0; jx < sp.nsplit; ++jx) M = fmaxf(M, __ldg(p.ws_ml + ((size_t)(slot0 + jx) * NCOL + col) * 2));
+    for (int cc = c0; cc <= c1; ++cc) M = fmaxf(M, __ldg(p.ws_ml + ((size_t)slot_of(cc) * NCOL + col) * 2));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = 0.f;
     const int d4 = threadIdx.x;
-    for (int jx = 0; jx < sp.nsplit; ++jx) {
-        const size_t base = (size_t)(slot0 + jx) * NCOL + col;
+    for (int cc = c0; cc <= c1; ++cc) {
+        const size_t base = (size_t)slot_of(cc) * NCOL + col;
         const float mj = __ldg(p.ws_ml + base * 2), lj = __ldg(p.ws_ml + base * 2 + 1);
         const float w = (mj == -INFINITY) ? 0.f : ptx::ex2(mj - M);
         const float4 o = __ldg(reinterpret_cast<const float4 *>(p.ws_o + base * kLat) + d4);
@@ -563,20 +708,30 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const __grid_constant_
     if (threadIdx.x == 0 && p.lse) p.lse[orow] = (M + log2f(L)) * 0.69314718055994531f;
 }
 
-// ---- host-side split plan: a function of the stream's own (len, R, H) only ----
-// Splits are whole multiples of 256 keys: at most 16 splits of 256..1,024 keys for
-// streams up to 16k keys, 1,024-key splits beyond that, and at most 128 splits a
-// stream (a longer split) so the partials stay a few percent of the key bytes.  A
-// prefill chunk with 128 or more column groups is not split at all.
-struct Split {
-    int64_t split;
-    int nsplit, groups;
+// ---- host-side plans ----
+// RANGES: a range holds at least MIN_TILES key tiles, and there are at most as many
+// CTAs as the device has SMs.  Launches with more than a quarter as many column
+// groups as SMs run UNITS.
+struct Plan {
+    int mode;
+    int64_t total;
+    int nranges, rep, nctas;
+    size_t slots;   // workspace slots of partials (0: no combine pass)
 };
 
-inline Split split_of(int64_t len, int R, int H) {
+// SPLITS: a function of the stream's own (len, R, H) only.  Splits are whole
+// multiples of 256 keys: at most 16 splits of 256..1,024 keys for streams up to 16k
+// keys, 1,024-key splits beyond that, and at most 128 splits a stream (a longer
+// split) so the partials stay a few percent of the key bytes.  A prefill chunk with
+// 128 or more column groups is not split at all.
+struct Split {
+    int64_t split;
+    int nsplit;
+};
+
+inline Split split_of(int64_t len, int groups) {
     Split sp;
-    sp.groups = (R * H + NCOL - 1) / NCOL;
-    if (sp.groups >= 128) {
+    if (groups >= 128) {
         sp.split = len;
         sp.nsplit = 1;
         return sp;
@@ -591,16 +746,76 @@ inline Split split_of(int64_t len, int R, int H) {
     return sp;
 }
 
+inline Plan plan_of(int S, int R, int H, const int64_t *h_len, int sms, bool invariant) {
+    Plan pl;
+    const int groups = (R * H + NCOL - 1) / NCOL;
+    pl.slots = 0;
+    pl.rep = 1;
+    pl.nranges = 0;
+    if (invariant) {
+        pl.mode = MODE_SPLITS;
+        pl.total = 0;
+        for (int s = 0; s < S; ++s) {
+            const Split sp = split_of(h_len[s], groups);
+            pl.total += (int64_t)groups * sp.nsplit;
+            if (sp.nsplit > 1) pl.slots += (size_t)groups * sp.nsplit;
+        }
+        pl.nctas = (int)pl.total;
+        return pl;
+    }
+    if (groups * 4 > sms) {
+        pl.mode = MODE_UNITS;
+        pl.total = (int64_t)S * groups;
+        pl.nctas = (int)(pl.total < sms ? pl.total : sms);
+        return pl;
+    }
+    pl.mode = MODE_RANGES;
+    pl.rep = groups;
+    pl.total = 0;
+    for (int s = 0; s < S; ++s) pl.total += (h_len[s] + BK - 1) / BK;
+    const int64_t want = (pl.total + MIN_TILES - 1) / MIN_TILES;
+    const int cap = sms / groups;
+    pl.nranges = (int)(want < cap ? want : cap);
+    if (pl.nranges < 1) pl.nranges = 1;
+    pl.nctas = pl.nranges * pl.rep;
+    // a boundary between two ranges cuts a stream unless it falls between streams
+    bool split = false;
+    for (int i = 1; i < pl.nranges && !split; ++i) {
+        const int64_t b = cta_begin(i, pl.total, pl.nranges);
+        int64_t off = 0;
+        for (int s = 0; s < S; ++s) {
+            if (b == off) break;
+            off += (h_len[s] + BK - 1) / BK;
+            if (b < off) {
+                split = true;
+                break;
+            }
+        }
+    }
+    pl.slots = split ? 2 * (size_t)pl.nctas : 0;
+    return pl;
+}
+
+inline size_t slot_bytes() { return (size_t)NCOL * kLat * sizeof(float); }
+
 }  // namespace attn
 
-size_t attend_workspace_bytes(int S, int R, int H, const int64_t *h_len) {
-    size_t slots = 0;
-    for (int s = 0; s < S; ++s) {
-        attn::Split sp = attn::split_of(h_len[s], R, H);
-        if (sp.nsplit > 1) slots += (size_t)sp.groups * sp.nsplit;
+// SMs of the current device, or an upper bound when no device answers.
+static int device_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                   cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return attn::MAX_CTAS;
     }
-    if (slots == 0) return 0;
-    const size_t o = slots * attn::NCOL * kLat * sizeof(float);
+    return n < attn::MAX_CTAS ? n : attn::MAX_CTAS;
+}
+
+size_t attend_workspace_bytes(bool invariant, int S, int R, int H, const int64_t *h_len) {
+    const attn::Plan pl = attn::plan_of(S, R, H, h_len, device_sms(), invariant);
+    if (pl.slots == 0) return 0;
+    const size_t slots = pl.slots;
+    const size_t o = slots * attn::slot_bytes();
     const size_t ml = slots * attn::NCOL * 2 * sizeof(float);
     return o + ((ml + 255) & ~size_t(255));
 }
@@ -694,49 +909,52 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     p.ncols = R * H;
     p.groups = (R * H + NCOL - 1) / NCOL;
     p.windowed = d_pt ? 0 : 1;
-    // launch order: streams with longer splits first, so short work fills the tail
-    Split sps[TF_MAX_STREAMS];
-    int order[TF_MAX_STREAMS];
+    const bool invariant = (pool->desc.flags & TF_POOL_BATCH_INVARIANT) != 0;
+    const Plan pl = plan_of(S, R, H, h_len, device_sms(), invariant);
+    p.mode = pl.mode;
+    p.total = pl.total;
+    p.nranges = pl.nranges;
+    p.rep = pl.rep;
+    int64_t off = 0;
     for (int s = 0; s < S; ++s) {
-        sps[s] = split_of(h_len[s], R, H);
-        order[s] = s;
-    }
-    std::stable_sort(order, order + S, [&](int a, int b) { return sps[a].split > sps[b].split; });
-    int items = 0, slots = 0;
-    bool any_multi = false;
-    for (int e = 0; e < S; ++e) {
-        const int s = order[e];
-        StreamPlan &sp = p.st[e];
+        StreamPlan &sp = p.st[s];
         sp.len = h_len[s];
-        sp.sidx = s;
-        sp.split = (int32_t)sps[s].split;
-        sp.nsplit = sps[s].nsplit;
-        sp.item0 = items;
-        sp.slot0 = 0;
-        sp.pad = 0;
-        items += sps[s].groups * sps[s].nsplit;
+        sp.toff = off;
+        sp.nt = (int32_t)((h_len[s] + BK - 1) / BK);
+        off += sp.nt;
+        const Split spl = split_of(h_len[s], p.groups);
+        sp.split = (int32_t)spl.split;
+        sp.nsplit = spl.nsplit;
+        sp.item0 = sp.slot0 = sp.pad = 0;
     }
-    // workspace slots follow the caller's stream order, so their layout does not depend on the launch order
-    for (int s = 0; s < S; ++s) {
-        int e = 0;
-        while (order[e] != s) ++e;
-        p.st[e].slot0 = slots;
-        if (sps[s].nsplit > 1) {
-            slots += sps[s].groups * sps[s].nsplit;
-            any_multi = true;
+    if (pl.mode == MODE_SPLITS) {
+        // launch order: streams with longer splits first, so short work fills the tail;
+        // workspace slots follow the caller's order, so their layout does not depend on it
+        int order[TF_MAX_STREAMS];
+        for (int s = 0; s < S; ++s) order[s] = s;
+        std::stable_sort(order, order + S, [&](int a, int b) { return p.st[a].split > p.st[b].split; });
+        int items = 0, slots = 0;
+        for (int e = 0; e < S; ++e) {
+            p.order[e] = (int16_t)order[e];
+            p.st[order[e]].item0 = items;
+            items += p.groups * p.st[order[e]].nsplit;
+        }
+        for (int s = 0; s < S; ++s) {
+            p.st[s].slot0 = slots;
+            if (p.st[s].nsplit > 1) slots += p.groups * p.st[s].nsplit;
         }
     }
-    p.nitems = items;
-    p.ws_o = static_cast<float *>(d_ws);
-    p.ws_ml = d_ws ? reinterpret_cast<float *>(static_cast<char *>(d_ws) + (size_t)slots * NCOL * kLat * 4) : nullptr;
+    const size_t slots = pl.slots;
+    p.ws_o = slots ? static_cast<float *>(d_ws) : nullptr;
+    p.ws_ml = slots ? reinterpret_cast<float *>(static_cast<char *>(d_ws) + slots * slot_bytes()) : nullptr;
     (void)ws_bytes;
     {
         ProfScope prof(pool, kProfAttend, st);
-        mla_attend_kernel<<<items, THREADS, SMEM_TOTAL, st>>>(p);
+        mla_attend_kernel<<<pl.nctas, THREADS, SMEM_TOTAL, st>>>(p);
         launch_counter()++;
     }
     if (cudaGetLastError() != cudaSuccess) return TF_E_CUDA;
-    if (any_multi) {
+    if (slots) {
         ProfScope prof(pool, kProfCombine, st);
         mla_combine_kernel<<<dim3(R * H, S), 128, 0, st>>>(p);
         launch_counter()++;

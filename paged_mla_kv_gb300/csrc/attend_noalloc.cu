@@ -38,7 +38,7 @@ extern "C" int tf_paged_mla_attend_static(tf_kvpool *pool, int32_t cache, const 
     if (!pool || !h_len || S < 1 || S > TF_MAX_STREAMS || R < 1 || H < 1 || H > TF_MAX_HEADS) return TF_E_ARG;
     for (int s = 0; s < S; ++s)
         if (h_len[s] < R) return TF_E_RANGE;
-    const size_t need = tf_paged_mla_workspace_bytes(S, R, H, h_len);
+    const size_t need = tf_paged_mla_workspace_bytes(pool, S, R, H, h_len);
     if (need > (size_t)TF_STATIC_WS_BYTES) return TF_E_NOMEM;
     void *ws = nullptr;
     if (need > 0) {

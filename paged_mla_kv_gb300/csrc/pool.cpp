@@ -43,7 +43,7 @@ using namespace tf;
 
 static bool desc_ok(const tf_kvpool_desc *d) {
     return d && d->num_caches >= 1 && d->num_pages >= 1 && d->page_rows == kPageRows && d->latent_dim == kLat &&
-           d->rope_dim == kRope && (d->flags & ~TF_POOL_POISON) == 0 &&
+           d->rope_dim == kRope && (d->flags & ~(TF_POOL_POISON | TF_POOL_BATCH_INVARIANT)) == 0 &&
            (uint64_t)d->num_caches * (uint64_t)d->num_pages < (1ull << 31);
 }
 
@@ -209,11 +209,13 @@ extern "C" int tf_paged_append(tf_kvpool *p, int32_t cache, const int32_t *d_pt,
 }
 
 // ---- attention ----
-extern "C" size_t tf_paged_mla_workspace_bytes(int32_t S, int32_t R, int32_t H, const int64_t *h_len) {
+extern "C" size_t tf_paged_mla_workspace_bytes(const tf_kvpool *p, int32_t S, int32_t R, int32_t H,
+                                               const int64_t *h_len) {
     if (S < 1 || S > TF_MAX_STREAMS || R < 1 || H < 1 || H > TF_MAX_HEADS || !h_len) return 0;
     for (int s = 0; s < S; ++s)
         if (h_len[s] < R) return 0;
-    return attend_workspace_bytes(S, R, H, h_len);
+    const bool invariant = p && (p->desc.flags & TF_POOL_BATCH_INVARIANT);
+    return attend_workspace_bytes(invariant, S, R, H, h_len);
 }
 
 extern "C" int tf_paged_mla_attend(tf_kvpool *p, int32_t cache, const int32_t *d_pt, int32_t max_pages,
@@ -231,7 +233,7 @@ extern "C" int tf_paged_mla_attend(tf_kvpool *p, int32_t cache, const int32_t *d
         if (h_len[s] < R || h_len[s] > (int64_t)max_pages * kPageRows) return TF_E_RANGE;
     if ((reinterpret_cast<uintptr_t>(d_q) & 15u) != 0 || (reinterpret_cast<uintptr_t>(d_out) & 15u) != 0)
         return TF_E_ARG;
-    size_t need = attend_workspace_bytes(S, R, H, h_len);
+    size_t need = attend_workspace_bytes((p->desc.flags & TF_POOL_BATCH_INVARIANT) != 0, S, R, H, h_len);
     if (need > 0 && (!d_ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(d_ws) & 255u) != 0))
         return d_ws && ws_bytes < need ? TF_E_NOMEM : TF_E_ARG;
     return launch_attend(p, cache, d_pt, max_pages, h_len, S, R, H, d_q, scale, d_out, d_lse, d_ws, ws_bytes,

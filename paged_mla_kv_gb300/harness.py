@@ -21,14 +21,15 @@ def bf16_tensor(bits: np.ndarray, device="cuda") -> torch.Tensor:
 
 class Resident:
     def __init__(self, w: Y.Workload, poison: bool = True, pool_seed: int | None = None, windowed: bool = False,
-                 caches=None, chunk_rows: int = 65536, device="cuda", extra_pages: int = 0):
+                 caches=None, chunk_rows: int = 65536, device="cuda", extra_pages: int = 0,
+                 invariant: bool = False):
         self.w = w
         self.windowed = windowed
         self.device = device
         self.max_pages = w.max_pages
         npages = (w.S * self.max_pages if windowed else w.pool_pages) + extra_pages
         seed = (w.seed * 1000003 + 7) if pool_seed is None else pool_seed
-        self.pool = B.KVPool(w.num_caches, npages, poison=poison, seed=seed, device=device)
+        self.pool = B.KVPool(w.num_caches, npages, poison=poison, seed=seed, device=device, invariant=invariant)
         self.caches = list(range(w.num_caches)) if caches is None else list(caches)
         pt = np.full((w.S, self.max_pages), -1, np.int32)
         if windowed:
@@ -87,7 +88,7 @@ class Resident:
         return bf16_tensor(self.w.q(cache), self.device)
 
     def workspace(self) -> torch.Tensor | None:
-        n = B.tf_paged_mla_workspace_bytes(self.w.S, self.w.R, self.w.H, self.lens)
+        n = B.tf_paged_mla_workspace_bytes(self.pool, self.w.S, self.w.R, self.w.H, self.lens)
         return torch.empty(max(n, 256), dtype=torch.uint8, device=self.device) if n else None
 
     def attend(self, q, cache: int = 0, out=None, lse=None, ws=None, scale=None):

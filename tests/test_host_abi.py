@@ -184,7 +184,7 @@ def test_bad_arguments_are_refused_before_launch(L):
     # a null table needs S * max_pages pool pages
     assert _args_refused(L, h, A, 0, None, 16, lp, 2, 1, 16, fake, 0.1, fake, None, None, 0, None) == B.TF_E_RANGE
     # workspace missing or too small
-    need = L.tf_paged_mla_workspace_bytes(2, 1, 16, lp)
+    need = L.tf_paged_mla_workspace_bytes(h, 2, 1, 16, lp)
     assert need > 0
     assert _args_refused(L, h, A, 0, fake, 16, lp, 2, 1, 16, fake, 0.1, fake, None, None, 0, None) == B.TF_E_ARG
     assert _args_refused(L, h, A, 0, fake, 16, lp, 2, 1, 16, fake, 0.1, fake, None, fake, need - 1,
@@ -202,12 +202,15 @@ def test_bad_arguments_are_refused_before_launch(L):
     L.tf_kvpool_destroy(h)
 
 
-def test_workspace_sizes_follow_each_streams_length(L):
-    one = np.array([65536], np.int64)
-    two = np.array([65536, 4096], np.int64)
-    w1 = L.tf_paged_mla_workspace_bytes(1, 1, 64, one.ctypes.data_as(ctypes.c_void_p))
-    w2 = L.tf_paged_mla_workspace_bytes(2, 1, 64, two.ctypes.data_as(ctypes.c_void_p))
-    assert 0 < w1 < w2
-    # a prefill chunk with enough column groups is not split: no workspace
-    pre = np.array([102048], np.int64)
-    assert L.tf_paged_mla_workspace_bytes(1, 2048, 64, pre.ctypes.data_as(ctypes.c_void_p)) == 0
+def test_workspace_is_bounded_by_the_cta_ranges(L):
+    # partials come only from (stream, group) units cut by a CTA range boundary: at most
+    # two a CTA, so the workspace does not grow with the lengths
+    def ws(lens, R=1, H=64):
+        a = np.array(lens, np.int64)
+        return L.tf_paged_mla_workspace_bytes(None, len(a), R, H, a.ctypes.data_as(ctypes.c_void_p))
+    assert ws([256]) == 0                       # four key tiles: one CTA, no partials
+    w1, w2, w3 = ws([65536]), ws([65536, 4096]), ws([1 << 20, 7000, 9])
+    assert 0 < w1 == w2 == w3
+    slot = 64 * 512 * 4
+    assert w1 <= 2 * 240 * slot + 2 * 240 * 64 * 2 * 4 + 255
+    assert w1 <= 64 << 20                       # fits the static scratch of the allocation-free call

@@ -35,9 +35,9 @@ def _static_call(res, q, out, lse):
 def test_static_scratch_matches_workspace_entry_point_twice():
     BUILD.build()
     w = Y.custom("noalloc", 77, lens=[9000, 3000, 65, 40000], R=2, H=64)
-    need = B.tf_paged_mla_workspace_bytes(w.S, w.R, w.H, w.lens)
-    assert 0 < need <= B.TF_STATIC_WS_BYTES          # the case really uses scratch
     res = Resident(w)
+    need = B.tf_paged_mla_workspace_bytes(res.pool, w.S, w.R, w.H, w.lens)
+    assert 0 < need <= B.TF_STATIC_WS_BYTES          # the case really uses scratch
     q1 = res.q()
     g = np.random.default_rng(3)
     q2 = bf16_tensor(Y.f32_to_bf16_bits(g.normal(0, 0.5, (w.S, w.R, w.H, 576)).astype(np.float32)))
@@ -58,16 +58,45 @@ def test_static_scratch_matches_workspace_entry_point_twice():
         assert np.array_equal(bits(out), bits(ref_out))
 
 
+def test_static_scratch_covers_every_default_launch():
+    BUILD.build()
+    # on a default pool, partials come only from units cut by a CTA range boundary, two
+    # a CTA at most, so the scratch serves any batch: many long streams, a 1M-token
+    # window, prefill chunks (whole units, no partials)
+    cases = [(np.full(512, 65536, np.int64), 1, 64), (np.array([1 << 20] + [8192] * 7, np.int64), 2, 64),
+             (np.array([102048], np.int64), 2048, 64), (np.array([209024], np.int64), 1024, 64),
+             (np.full(64, 300000, np.int64), 2, 128)]
+    for lens, R, H in cases:
+        need = B.tf_paged_mla_workspace_bytes(None, len(lens), R, H, lens)
+        assert need <= B.TF_STATIC_WS_BYTES
+    assert B.tf_paged_mla_workspace_bytes(None, 512, 1, 64, cases[0][0]) > 0
+
+
 def test_static_scratch_refuses_oversize_calls():
     BUILD.build()
+    # a batch-invariant pool keeps one partial a split, so long batches outgrow the scratch
     w = Y.custom("noalloc_big", 78, lens=[100], R=1, H=64)
-    res = Resident(w)
-    huge = np.full(512, 65536, np.int64)              # 512 long streams need far more partials
-    assert B.tf_paged_mla_workspace_bytes(512, 1, 64, huge) > B.TF_STATIC_WS_BYTES
+    res = Resident(w, invariant=True)
+    huge = np.full(512, 65536, np.int64)
+    assert B.tf_paged_mla_workspace_bytes(res.pool, 512, 1, 64, huge) > B.TF_STATIC_WS_BYTES
     before = B.tf_launch_count()
     rc = B.lib().tf_paged_mla_attend_static(
         res.pool.handle, 0, None, 128, huge.ctypes.data_as(ctypes.c_void_p), 512, 1, 64,
         ctypes.c_void_p(res.q().data_ptr()), ctypes.c_float(0.1), ctypes.c_void_p(res.q().data_ptr()), None,
         None)
     assert rc == B.TF_E_NOMEM
+    assert B.tf_launch_count() == before
+
+
+def test_static_entry_refuses_bad_arguments():
+    BUILD.build()
+    w = Y.custom("noalloc_bad", 79, lens=[100], R=1, H=64)
+    res = Resident(w)
+    lens = np.ascontiguousarray(res.lens, np.int64)
+    before = B.tf_launch_count()
+    rc = B.lib().tf_paged_mla_attend_static(
+        res.pool.handle, 0, ctypes.c_void_p(res.pt.data_ptr()), res.max_pages, lens.ctypes.data_as(ctypes.c_void_p),
+        1, 1, 64, ctypes.c_void_p(res.q().data_ptr()), ctypes.c_float(0.0), ctypes.c_void_p(res.q().data_ptr()),
+        None, None)
+    assert rc == B.TF_E_ARG
     assert B.tf_launch_count() == before
