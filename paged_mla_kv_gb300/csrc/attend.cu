@@ -62,7 +62,7 @@ constexpr float TAU = 8.0f;                     // lazy-rescale threshold, log2 
 constexpr int TMEM_COLS = 512;
 constexpr int TMEM_O = 0;                       // O^T M-tile j at 64 j (j < 4)
 constexpr int TMEM_S = 256;                     // S buffers at 256 and 320
-constexpr int THREADS = 256;
+constexpr int THREADS = 352;
 // A tile's QK^T runs in two parts: part 0 takes the rope box and latent boxes 0-3,
 // part 1 latent boxes 4-7.  PV of the previous tile is issued between the two parts,
 // so the tensor pipe keeps working while the softmax runs and the previous tile's
@@ -73,7 +73,7 @@ constexpr int MIN_TILES = 4;                    // fewest key tiles a CTA is giv
 constexpr int SPLIT_UNIT = 256;                 // batch-invariant split sizes are multiples of this
 static_assert(SPLIT_UNIT % BK == 0, "splits must be tile-aligned");
 constexpr int MAX_CTAS = 240;                   // CTAs a launch (one a SM); sizes the workspace
-constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, BK, false, false);
+constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(64, BK, false, false);
 
 struct Ctrl {
     uint64_t part_full[NSTAGE][2];     // part 0: rope + latent boxes 0-3 landed; part 1: latent boxes 4-7
@@ -282,21 +282,21 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&c.s_full[i], 1);
-            ptx::mbar_init(&c.s_free[i], 2);
+            ptx::mbar_init(&c.s_free[i], 4);
         }
-        ptx::mbar_init(&c.corr_req[0], 2);
-        ptx::mbar_init(&c.corr_req[1], 2);
-        ptx::mbar_init(&c.p_full, 3);
+        ptx::mbar_init(&c.corr_req[0], 4);
+        ptx::mbar_init(&c.corr_req[1], 4);
+        ptx::mbar_init(&c.p_full, 5);
         ptx::mbar_init(&c.pv_done, 1);
         ptx::mbar_init(&c.q_full, 1);
         ptx::mbar_init(&c.q_free, 1);
-        ptx::mbar_init(&c.stats_full, 2);
-        ptx::mbar_init(&c.drain, 1);
+        ptx::mbar_init(&c.stats_full, 4);
+        ptx::mbar_init(&c.drain, 2);
         c.abort = 0;
         c.flag[0] = c.flag[1] = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 7) {
+    if (warp == 9) {
         ptx::tmem_alloc(&c.tmem_base, TMEM_COLS);
         ptx::tmem_relinquish();
     }
@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
     const uint32_t tmem = c.tmem_base;
     volatile int *abort = &c.abort;
 
-    if (warp == 6) {
+    if (warp == 8) {
         // ================= TMA producer =================
         if (lane == 0) {
             ptx::prefetch_tmap(&p.tm_lat);
@@ -376,95 +376,102 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
                     if (armed[i][h] >= 0)
                         ptx::mbar_wait(&c.part_full[i][h], (armed[i][h] / NSTAGE) & 1, abort, errp, 11, 1ll << 28);
         }
-    } else if (warp == 7) {
-        // ================= MMA issuer =================
-        // Schedule for tile t of a segment:  QK(t+1) part 0  |  PV(t)  |  QK(t+1) part 1.
-        // The order of the contributions inside every accumulator is fixed, so timing
-        // never changes a bit.
+    } else if (warp == 9 || warp == 10) {
+        // ================= MMA issuers =================
+        // Warp 9 issues QK^T tile by tile as key tiles land; warp 10 issues PV as the
+        // softmax publishes P.  Each accumulator gets its contributions in a fixed order,
+        // so timing never changes a bit.
+        const bool qk_role = warp == 9;
         const uint64_t q_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_Q), 16, 1024);
         const uint64_t kv_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_KV), 16, 1024);
         const uint64_t v_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_KV), BOX_BYTES, 1024);
         const uint64_t p_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_P), 16, 1024);
-        // QK^T of global tile tq (keys from k0), boxes of one part; `last` marks the
-        // segment's last tile; false if a wait gave up
-        auto qk_part = [&](int tq, int part, int64_t k0, int64_t len, bool last) -> bool {
-            const int st = tq % NSTAGE;
-            if (part == 0 && tq >= 2 &&
-                !ALLW(ptx::mbar_wait(&c.s_free[tq & 1], ((tq - 2) >> 1) & 1, abort, errp, 4)))
-                return false;
-            if (!ALLW(ptx::mbar_wait(&c.part_full[st][part], (tq / NSTAGE) & 1, abort, errp, 3))) return false;
-            const int b0 = part == 0 ? 0 : kPart0Boxes, b1 = part == 0 ? kPart0Boxes : NBOX;
-            const int64_t rem = len - k0;
-            if (rem < BK) {
-                // rows past the stream's end may hold NaN poison: zero them so that
-                // P = 0 times V stays 0 in the PV contraction
-                const int valid = (int)rem;
-                for (int bi = b0; bi < b1; ++bi) {
-                    uint4 *bx = reinterpret_cast<uint4 *>(smem + SMEM_KV + st * STAGE_BYTES + kBoxOrder[bi] * BOX_BYTES);
-                    for (int k = lane; k < (BK - valid) * 8; k += 32) bx[valid * 8 + k] = make_uint4(0, 0, 0, 0);
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-            }
-            ptx::tc_fence_after();
-            if (lane == 0) {
-                const uint32_t d = tmem + TMEM_S + (tq & 1) * BK;
-                for (int bi = b0; bi < b1; ++bi) {
-                    const int b = kBoxOrder[bi];
-                    const uint64_t kvd = kv_desc0 + (uint64_t)((st * STAGE_BYTES + b * BOX_BYTES) >> 4);
-                    const uint64_t qd = q_desc0 + (uint64_t)((b * QBOX_BYTES) >> 4);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        ptx::mma_bf16_ss(d, qd + (uint64_t)k * 2, kvd + (uint64_t)k * 2, IDESC_QK,
-                                         (bi == 0 && k == 0) ? 0u : 1u);
-                }
-                if (part == 1) {
-                    ptx::mma_commit(&c.s_full[tq & 1]);
-                    ptx::mma_commit(&c.rope_empty[st]);
-                    if (last) ptx::mma_commit(&c.q_free);
-                }
-            }
-            __syncwarp();
-            return true;
-        };
-        // PV of global tile tv; the latent box pair of M-tile jm is released as soon as
-        // its MMAs finish; the first tile of a segment starts the accumulator afresh
-        auto pv = [&](int tv, bool first, uint32_t idesc_pv) -> bool {
-            if (!ALLW(ptx::mbar_wait(&c.p_full, tv & 1, abort, errp, 5))) return false;
-            ptx::tc_fence_after();
-            if (lane == 0) {
-                const int st = tv % NSTAGE;
-                const uint64_t vd = v_desc0 + (uint64_t)(st * (STAGE_BYTES >> 4));
-                const uint32_t acc0 = first ? 0u : 1u;
-#pragma unroll
-                for (int jm = 0; jm < 4; ++jm) {
-#pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        ptx::mma_bf16_ss(tmem + TMEM_O + jm * 64, vd + (uint64_t)((2 * jm * BOX_BYTES + k * 2048) >> 4),
-                                         p_desc0 + (uint64_t)((k * 32) >> 4), idesc_pv, k > 0 ? 1u : acc0);
-                    ptx::mma_commit(&c.lat_empty[st][jm]);
-                }
-                ptx::mma_commit(&c.pv_done);
-            }
-            __syncwarp();
-            return true;
-        };
         bool ok = true;
         int gt = 0, si = 0;
         SegIter it(p);
         Seg q;
         for (; ok && it.next(p, q); ++si) {
-            const int ncols = min(NCOL, ncols_all - q.g * NCOL);
-            const uint32_t idesc_pv = ptx::idesc_bf16_f32(128, (ncols + 15) & ~15, true, false);
-            ok = ALLW(ptx::mbar_wait(&c.q_full, si & 1, abort, errp, 2));
-            ok = ok && qk_part(gt, 0, q.kb, q.len, q.nt == 1) && qk_part(gt, 1, q.kb, q.len, q.nt == 1);
-            for (int tl = 0; ok && tl < q.nt; ++tl) {
-                const bool next = tl + 1 < q.nt;
-                const int64_t kn = q.kb + (int64_t)(tl + 1) * BK;
-                const bool nlast = tl + 2 == q.nt;
-                if (next && !qk_part(gt + tl + 1, 0, kn, q.len, nlast)) ok = false;
-                if (ok && !pv(gt + tl, tl == 0, idesc_pv)) ok = false;
-                if (ok && next && !qk_part(gt + tl + 1, 1, kn, q.len, nlast)) ok = false;
+            if (qk_role) {
+                ok = ALLW(ptx::mbar_wait(&c.q_full, si & 1, abort, errp, 2));
+                for (int tl = 0; ok && tl < q.nt; ++tl) {
+                    // QK^T of global tile tq: S[64 columns][64 keys] (M = 64: rows 16w..16w+15
+                    // in lanes 0-15 of TMEM quadrant w)
+                    const int tq = gt + tl;
+                    const int st = tq % NSTAGE;
+                    if (tq >= 2 && !ALLW(ptx::mbar_wait(&c.s_free[tq & 1], ((tq - 2) >> 1) & 1, abort, errp, 4))) {
+                        ok = false;
+                        break;
+                    }
+                    const int64_t rem = q.len - (q.kb + (int64_t)tl * BK);
+                    for (int part = 0; part < 2; ++part) {
+                        if (!ALLW(ptx::mbar_wait(&c.part_full[st][part], (tq / NSTAGE) & 1, abort, errp, 3))) {
+                            ok = false;
+                            break;
+                        }
+                        const int b0 = part == 0 ? 0 : kPart0Boxes, b1 = part == 0 ? kPart0Boxes : NBOX;
+                        if (rem < BK) {
+                            // rows past the stream's end may hold NaN poison: zero them so that
+                            // P = 0 times V stays 0 in the PV contraction
+                            const int valid = (int)rem;
+                            for (int bi = b0; bi < b1; ++bi) {
+                                uint4 *bx = reinterpret_cast<uint4 *>(smem + SMEM_KV + st * STAGE_BYTES +
+                                                                      kBoxOrder[bi] * BOX_BYTES);
+                                for (int k = lane; k < (BK - valid) * 8; k += 32)
+                                    bx[valid * 8 + k] = make_uint4(0, 0, 0, 0);
+                            }
+                            ptx::fence_proxy_async_smem();
+                            __syncwarp();
+                        }
+                        ptx::tc_fence_after();
+                        if (lane == 0) {
+                            const uint32_t d = tmem + TMEM_S + (tq & 1) * BK;
+                            for (int bi = b0; bi < b1; ++bi) {
+                                const int b = kBoxOrder[bi];
+                                const uint64_t kvd = kv_desc0 + (uint64_t)((st * STAGE_BYTES + b * BOX_BYTES) >> 4);
+                                const uint64_t qd = q_desc0 + (uint64_t)((b * QBOX_BYTES) >> 4);
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    ptx::mma_bf16_ss(d, qd + (uint64_t)k * 2, kvd + (uint64_t)k * 2, IDESC_QK,
+                                                     (bi == 0 && k == 0) ? 0u : 1u);
+                            }
+                            if (part == 1) {
+                                ptx::mma_commit(&c.s_full[tq & 1]);
+                                ptx::mma_commit(&c.rope_empty[st]);
+                                if (tl == q.nt - 1) ptx::mma_commit(&c.q_free);
+                            }
+                        }
+                        __syncwarp();
+                    }
+                }
+            } else {
+                const int ncols = min(NCOL, ncols_all - q.g * NCOL);
+                const uint32_t idesc_pv = ptx::idesc_bf16_f32(128, (ncols + 15) & ~15, true, false);
+                for (int tl = 0; ok && tl < q.nt; ++tl) {
+                    // PV of global tile tv; the latent box pair of M-tile jm is released as
+                    // soon as its MMAs finish; a segment's first tile starts the accumulator
+                    const int tv = gt + tl;
+                    if (!ALLW(ptx::mbar_wait(&c.p_full, tv & 1, abort, errp, 5))) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    if (lane == 0) {
+                        const int st = tv % NSTAGE;
+                        const uint64_t vd = v_desc0 + (uint64_t)(st * (STAGE_BYTES >> 4));
+                        const uint32_t acc0 = tl == 0 ? 0u : 1u;
+#pragma unroll
+                        for (int jm = 0; jm < 4; ++jm) {
+#pragma unroll
+                            for (int k = 0; k < BK / 16; ++k)
+                                ptx::mma_bf16_ss(tmem + TMEM_O + jm * 64,
+                                                 vd + (uint64_t)((2 * jm * BOX_BYTES + k * 2048) >> 4),
+                                                 p_desc0 + (uint64_t)((k * 32) >> 4), idesc_pv, k > 0 ? 1u : acc0);
+                            ptx::mma_commit(&c.lat_empty[st][jm]);
+                        }
+                        ptx::mma_commit(&c.pv_done);
+                    }
+                    __syncwarp();
+                }
             }
             gt += q.nt;
         }
@@ -475,9 +482,12 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
         }
         __syncwarp();
     } else if (warp >= 4) {
-        // ================= softmax (warps 4-5: S rows 0-63) =================
+        // ================= softmax (warps 4-7: TMEM quadrant w holds S rows 16w..16w+15) =================
+        // A 16x256b load gives thread t rows r0 = 16w + t/4 and r1 = r0 + 8, keys
+        // 8j + 2(t%4) + {0, 1} for j < 8: a row's 64 keys are spread over 4 threads.
         const int q4 = warp & 3;
-        const int cidx = threadIdx.x - 128;    // column 0..63 of the group
+        const int r0 = 16 * q4 + (lane >> 2), r1 = r0 + 8;
+        const int kq = 2 * (lane & 3);
         const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
         bool ok = true;
         int gt = 0, si = 0;
@@ -485,11 +495,12 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
         Seg q;
         for (; ok && it.next(p, q); ++si) {
             const int col0 = q.g * NCOL;
-            const bool active = cidx < ncols_all - col0;
-            const int gc = col0 + cidx;
-            const int rr = active ? gc / H_ : 0;
-            const int64_t pos_c = q.len - R_ + rr;  // last visible key of this column
-            float m_ref = -INFINITY, l = 0.f;
+            const int ncols = ncols_all - col0;
+            const bool act0 = r0 < ncols, act1 = r1 < ncols;
+            // last visible key of each row's column
+            const int64_t pos0 = q.len - R_ + (act0 ? (col0 + r0) / H_ : 0);
+            const int64_t pos1 = q.len - R_ + (act1 ? (col0 + r1) / H_ : 0);
+            float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
             for (int tl = 0; tl < q.nt; ++tl) {
                 const int t = gt + tl;
                 const int64_t k0 = q.kb + (int64_t)tl * BK;
@@ -498,71 +509,103 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
                     break;
                 }
                 ptx::tc_fence_after();
-                uint32_t r[BK];
-                ptx::tmem_ld32(lane_base + TMEM_S + (t & 1) * BK, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                ptx::tmem_ld32(lane_base + TMEM_S + (t & 1) * BK + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                uint32_t r[32];
+                ptx::tmem_ld_16x256b_x8(lane_base + TMEM_S + (t & 1) * BK, r);
                 ptx::tmem_ld_wait();
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&c.s_free[t & 1]);
-                const int64_t lim = (pos_c + 1 < q.ke ? pos_c + 1 : q.ke) - k0;
-                const int nvalid = active ? (lim < 0 ? 0 : (lim > BK ? BK : (int)lim)) : 0;
-                // raw scores; keys outside this column's range become -inf.  The maximum is
-                // taken before scaling (the scale is positive) and the scale is folded into
-                // the exponent's FFMA: p_i = 2^(s_i * scale*log2(e) - m_ref).
-                float xs[BK];
-                float mraw = -INFINITY;
+                // keys outside a row's range become -inf; the maximum is taken before
+                // scaling (the scale is positive) and the scale is folded into the
+                // exponent's FFMA: p = 2^(s * scale*log2(e) - m_ref)
+                const int64_t lim0 = (pos0 + 1 < q.ke ? pos0 + 1 : q.ke) - k0;
+                const int64_t lim1 = (pos1 + 1 < q.ke ? pos1 + 1 : q.ke) - k0;
+                const int nv0 = act0 ? (lim0 < 0 ? 0 : (lim0 > BK ? BK : (int)lim0)) : 0;
+                const int nv1 = act1 ? (lim1 < 0 ? 0 : (lim1 > BK ? BK : (int)lim1)) : 0;
+                float x0[16], x1[16];
+                float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < BK; ++i) {
-                    xs[i] = i < nvalid ? __uint_as_float(r[i]) : -INFINITY;
-                    mraw = fmaxf(mraw, xs[i]);
+                for (int j = 0; j < 8; ++j) {
+                    const int key = 8 * j + kq;
+                    x0[2 * j] = key < nv0 ? __uint_as_float(r[4 * j]) : -INFINITY;
+                    x0[2 * j + 1] = key + 1 < nv0 ? __uint_as_float(r[4 * j + 1]) : -INFINITY;
+                    x1[2 * j] = key < nv1 ? __uint_as_float(r[4 * j + 2]) : -INFINITY;
+                    x1[2 * j + 1] = key + 1 < nv1 ? __uint_as_float(r[4 * j + 3]) : -INFINITY;
+                    mx0 = fmaxf(mx0, fmaxf(x0[2 * j], x0[2 * j + 1]));
+                    mx1 = fmaxf(mx1, fmaxf(x1[2 * j], x1[2 * j + 1]));
                 }
-                const float mt = mraw * scale_log2;
-                float alpha = 1.f;
-                if (mt > m_ref + TAU) {
-                    alpha = (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - mt);
-                    m_ref = mt;
-                    l *= alpha;
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                const float mt0 = mx0 * scale_log2, mt1 = mx1 * scale_log2;
+                float a0 = 1.f, a1 = 1.f;
+                if (mt0 > m0 + TAU) {
+                    a0 = (m0 == -INFINITY) ? 0.f : ptx::ex2(m0 - mt0);
+                    m0 = mt0;
+                    l0 *= a0;
                 }
-                c.alpha[t & 1][cidx] = alpha;
-                if (__any_sync(0xffffffffu, alpha != 1.f && tl > 0) && lane == 0) atomicOr(&c.flag[t & 1], 1);
-                // P row for this column as bf16, 8 x 16 B, 128B-swizzled K-major; l sums the fp32 weights
-                const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
-                uint32_t pk[BK / 2];
-                float ls0 = 0.f, ls1 = 0.f;
+                if (mt1 > m1 + TAU) {
+                    a1 = (m1 == -INFINITY) ? 0.f : ptx::ex2(m1 - mt1);
+                    m1 = mt1;
+                    l1 *= a1;
+                }
+                if ((lane & 3) == 0) {
+                    c.alpha[t & 1][r0] = a0;
+                    c.alpha[t & 1][r1] = a1;
+                }
+                if (__any_sync(0xffffffffu, (a0 != 1.f || a1 != 1.f) && tl > 0) && lane == 0)
+                    atomicOr(&c.flag[t & 1], 1);
+                const float mr0 = (m0 == -INFINITY) ? 0.f : m0, mr1 = (m1 == -INFINITY) ? 0.f : m1;
+                uint32_t pk0[8], pk1[8];
 #pragma unroll
-                for (int i = 0; i < BK / 2; ++i) {
-                    const float e0 = ptx::ex2(fmaf(xs[2 * i], scale_log2, -mr));
-                    const float e1 = ptx::ex2(fmaf(xs[2 * i + 1], scale_log2, -mr));
-                    ls0 += e0;
-                    ls1 += e1;
-                    pk[i] = ptx::pack_bf16x2(e0, e1);
+                for (int j = 0; j < 8; ++j) {
+                    const float e00 = ptx::ex2(fmaf(x0[2 * j], scale_log2, -mr0));
+                    const float e01 = ptx::ex2(fmaf(x0[2 * j + 1], scale_log2, -mr0));
+                    const float e10 = ptx::ex2(fmaf(x1[2 * j], scale_log2, -mr1));
+                    const float e11 = ptx::ex2(fmaf(x1[2 * j + 1], scale_log2, -mr1));
+                    l0 += e00 + e01;
+                    l1 += e10 + e11;
+                    pk0[j] = ptx::pack_bf16x2(e00, e01);
+                    pk1[j] = ptx::pack_bf16x2(e10, e11);
                 }
-                l += ls0 + ls1;
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&c.corr_req[t & 1]);
                 if (t >= 1 && !ALLW(ptx::mbar_wait(&c.pv_done, (t - 1) & 1, abort, errp, 8))) {
                     ok = false;
                     break;
                 }
-                uint8_t *prow = smem + SMEM_P + cidx * 128;
+                // P rows as bf16, 128B-swizzled K-major: keys 8j.. of row r in 16-byte chunk j ^ (r & 7)
+                uint8_t *p0 = smem + SMEM_P + r0 * 128 + 2 * kq;
+                uint8_t *p1 = smem + SMEM_P + r1 * 128 + 2 * kq;
 #pragma unroll
-                for (int ch = 0; ch < BK / 8; ++ch)
-                    *reinterpret_cast<uint4 *>(prow + ((ch ^ (cidx & 7)) << 4)) =
-                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                for (int j = 0; j < 8; ++j) {
+                    *reinterpret_cast<uint32_t *>(p0 + ((j ^ (r0 & 7)) << 4)) = pk0[j];
+                    *reinterpret_cast<uint32_t *>(p1 + ((j ^ (r1 & 7)) << 4)) = pk1[j];
+                }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&c.p_full);
             }
             if (!ok) break;
-            // statistics for the epilogue
-            c.row_inv_l[si & 1][cidx] = l > 0.f ? 1.f / l : 0.f;
-            if (active) {
-                if (q.slot < 0) {
-                    if (lsep) lsep[(size_t)q.s * ncols_all + gc] = (m_ref + log2f(l)) * 0.69314718055994531f;
-                } else {
-                    ws_ml[((size_t)q.slot * NCOL + cidx) * 2 + 0] = m_ref;
-                    ws_ml[((size_t)q.slot * NCOL + cidx) * 2 + 1] = l;
+            // the row sums: each thread holds 16 of a row's keys a tile
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+            if ((lane & 3) == 0) {
+                c.row_inv_l[si & 1][r0] = l0 > 0.f ? 1.f / l0 : 0.f;
+                c.row_inv_l[si & 1][r1] = l1 > 0.f ? 1.f / l1 : 0.f;
+                for (int h = 0; h < 2; ++h) {
+                    const int rr = h ? r1 : r0;
+                    const float m = h ? m1 : m0, l = h ? l1 : l0;
+                    if (!(h ? act1 : act0)) continue;
+                    if (q.slot < 0) {
+                        if (lsep) lsep[(size_t)q.s * ncols_all + col0 + rr] = (m + log2f(l)) * 0.69314718055994531f;
+                    } else {
+                        ws_ml[((size_t)q.slot * NCOL + rr) * 2 + 0] = m;
+                        ws_ml[((size_t)q.slot * NCOL + rr) * 2 + 1] = l;
+                    }
                 }
             }
             __syncwarp();
@@ -655,7 +698,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (warp == 7) ptx::tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 9) ptx::tmem_dealloc(tmem, TMEM_COLS);
 }
 
 // Merge a unit's partials, CTA range by CTA range (that is, in key order):

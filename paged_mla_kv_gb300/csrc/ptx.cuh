@@ -286,6 +286,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : TF_R8(0), TF_R8(8), TF_R8(16), TF_R8(24)
         : "r"(taddr));
 }
+// 16 lanes x 256 bits, 8 times along the columns (an M = 64 accumulator): thread t
+// gets lanes t/4 and t/4 + 8, columns 8j + 2(t%4) and +1, in r[4j .. 4j+3] as
+// (lane t/4, col), (lane t/4, col+1), (lane t/4+8, col), (lane t/4+8, col+1).
+__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : TF_R8(0), TF_R8(8), TF_R8(16), TF_R8(24)
+        : "r"(taddr));
+}
 #undef TF_R8
 
 #define TF_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), \
