@@ -386,92 +386,83 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
         const uint64_t kv_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_KV), 16, 1024);
         const uint64_t v_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_KV), BOX_BYTES, 1024);
         const uint64_t p_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_P), 16, 1024);
+        // QK^T of global tile tq (tile tl of segment q), parts [p0, p1): S[64 columns][64 keys]
+        // (M = 64: rows 16w..16w+15 in lanes 0-15 of TMEM quadrant w)
+        auto qk_tile = [&](int tq, int tl, const Seg &q, int p0, int p1) -> bool {
+            const int st = tq % NSTAGE;
+            if (p0 == 0 && tq >= 2 && !ALLW(ptx::mbar_wait(&c.s_free[tq & 1], ((tq - 2) >> 1) & 1, abort, errp, 4)))
+                return false;
+            const int64_t rem = q.len - (q.kb + (int64_t)tl * BK);
+            for (int part = p0; part < p1; ++part) {
+                if (!ALLW(ptx::mbar_wait(&c.part_full[st][part], (tq / NSTAGE) & 1, abort, errp, 3))) return false;
+                const int b0 = part == 0 ? 0 : kPart0Boxes, b1 = part == 0 ? kPart0Boxes : NBOX;
+                if (rem < BK) {
+                    // rows past the stream's end may hold NaN poison: zero them so that
+                    // P = 0 times V stays 0 in the PV contraction
+                    const int valid = (int)rem;
+                    for (int bi = b0; bi < b1; ++bi) {
+                        uint4 *bx = reinterpret_cast<uint4 *>(smem + SMEM_KV + st * STAGE_BYTES + kBoxOrder[bi] * BOX_BYTES);
+                        for (int k = lane; k < (BK - valid) * 8; k += 32) bx[valid * 8 + k] = make_uint4(0, 0, 0, 0);
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t d = tmem + TMEM_S + (tq & 1) * BK;
+                    for (int bi = b0; bi < b1; ++bi) {
+                        const int b = kBoxOrder[bi];
+                        const uint64_t kvd = kv_desc0 + (uint64_t)((st * STAGE_BYTES + b * BOX_BYTES) >> 4);
+                        const uint64_t qd = q_desc0 + (uint64_t)((b * QBOX_BYTES) >> 4);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            ptx::mma_bf16_ss(d, qd + (uint64_t)k * 2, kvd + (uint64_t)k * 2, IDESC_QK,
+                                             (bi == 0 && k == 0) ? 0u : 1u);
+                    }
+                    if (part == 1) {
+                        ptx::mma_commit(&c.s_full[tq & 1]);
+                        ptx::mma_commit(&c.rope_empty[st]);
+                        if (tl == q.nt - 1) ptx::mma_commit(&c.q_free);
+                    }
+                }
+                __syncwarp();
+            }
+            return true;
+        };
+        // PV of global tile tv (tile tl of segment q); the latent box pair of M-tile jm is
+        // released as soon as its MMAs finish; a segment's first tile starts the accumulator
+        auto pv_tile = [&](int tv, int tl, uint32_t idesc_pv) -> bool {
+            if (!ALLW(ptx::mbar_wait(&c.p_full, tv & 1, abort, errp, 5))) return false;
+            ptx::tc_fence_after();
+            if (lane == 0) {
+                const int st = tv % NSTAGE;
+                const uint64_t vd = v_desc0 + (uint64_t)(st * (STAGE_BYTES >> 4));
+                const uint32_t acc0 = tl == 0 ? 0u : 1u;
+#pragma unroll
+                for (int jm = 0; jm < 4; ++jm) {
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        ptx::mma_bf16_ss(tmem + TMEM_O + jm * 64, vd + (uint64_t)((2 * jm * BOX_BYTES + k * 2048) >> 4),
+                                         p_desc0 + (uint64_t)((k * 32) >> 4), idesc_pv, k > 0 ? 1u : acc0);
+                    ptx::mma_commit(&c.lat_empty[st][jm]);
+                }
+                ptx::mma_commit(&c.pv_done);
+            }
+            __syncwarp();
+            return true;
+        };
         bool ok = true;
         int gt = 0, si = 0;
         SegIter it(p);
         Seg q;
         for (; ok && it.next(p, q); ++si) {
+            const int ncols = min(NCOL, ncols_all - q.g * NCOL);
+            const uint32_t idesc_pv = ptx::idesc_bf16_f32(128, (ncols + 15) & ~15, true, false);
             if (qk_role) {
                 ok = ALLW(ptx::mbar_wait(&c.q_full, si & 1, abort, errp, 2));
-                for (int tl = 0; ok && tl < q.nt; ++tl) {
-                    // QK^T of global tile tq: S[64 columns][64 keys] (M = 64: rows 16w..16w+15
-                    // in lanes 0-15 of TMEM quadrant w)
-                    const int tq = gt + tl;
-                    const int st = tq % NSTAGE;
-                    if (tq >= 2 && !ALLW(ptx::mbar_wait(&c.s_free[tq & 1], ((tq - 2) >> 1) & 1, abort, errp, 4))) {
-                        ok = false;
-                        break;
-                    }
-                    const int64_t rem = q.len - (q.kb + (int64_t)tl * BK);
-                    for (int part = 0; part < 2; ++part) {
-                        if (!ALLW(ptx::mbar_wait(&c.part_full[st][part], (tq / NSTAGE) & 1, abort, errp, 3))) {
-                            ok = false;
-                            break;
-                        }
-                        const int b0 = part == 0 ? 0 : kPart0Boxes, b1 = part == 0 ? kPart0Boxes : NBOX;
-                        if (rem < BK) {
-                            // rows past the stream's end may hold NaN poison: zero them so that
-                            // P = 0 times V stays 0 in the PV contraction
-                            const int valid = (int)rem;
-                            for (int bi = b0; bi < b1; ++bi) {
-                                uint4 *bx = reinterpret_cast<uint4 *>(smem + SMEM_KV + st * STAGE_BYTES +
-                                                                      kBoxOrder[bi] * BOX_BYTES);
-                                for (int k = lane; k < (BK - valid) * 8; k += 32)
-                                    bx[valid * 8 + k] = make_uint4(0, 0, 0, 0);
-                            }
-                            ptx::fence_proxy_async_smem();
-                            __syncwarp();
-                        }
-                        ptx::tc_fence_after();
-                        if (lane == 0) {
-                            const uint32_t d = tmem + TMEM_S + (tq & 1) * BK;
-                            for (int bi = b0; bi < b1; ++bi) {
-                                const int b = kBoxOrder[bi];
-                                const uint64_t kvd = kv_desc0 + (uint64_t)((st * STAGE_BYTES + b * BOX_BYTES) >> 4);
-                                const uint64_t qd = q_desc0 + (uint64_t)((b * QBOX_BYTES) >> 4);
-#pragma unroll
-                                for (int k = 0; k < 4; ++k)
-                                    ptx::mma_bf16_ss(d, qd + (uint64_t)k * 2, kvd + (uint64_t)k * 2, IDESC_QK,
-                                                     (bi == 0 && k == 0) ? 0u : 1u);
-                            }
-                            if (part == 1) {
-                                ptx::mma_commit(&c.s_full[tq & 1]);
-                                ptx::mma_commit(&c.rope_empty[st]);
-                                if (tl == q.nt - 1) ptx::mma_commit(&c.q_free);
-                            }
-                        }
-                        __syncwarp();
-                    }
-                }
+                for (int tl = 0; ok && tl < q.nt; ++tl) ok = qk_tile(gt + tl, tl, q, 0, 2);
             } else {
-                const int ncols = min(NCOL, ncols_all - q.g * NCOL);
-                const uint32_t idesc_pv = ptx::idesc_bf16_f32(128, (ncols + 15) & ~15, true, false);
-                for (int tl = 0; ok && tl < q.nt; ++tl) {
-                    // PV of global tile tv; the latent box pair of M-tile jm is released as
-                    // soon as its MMAs finish; a segment's first tile starts the accumulator
-                    const int tv = gt + tl;
-                    if (!ALLW(ptx::mbar_wait(&c.p_full, tv & 1, abort, errp, 5))) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    if (lane == 0) {
-                        const int st = tv % NSTAGE;
-                        const uint64_t vd = v_desc0 + (uint64_t)(st * (STAGE_BYTES >> 4));
-                        const uint32_t acc0 = tl == 0 ? 0u : 1u;
-#pragma unroll
-                        for (int jm = 0; jm < 4; ++jm) {
-#pragma unroll
-                            for (int k = 0; k < BK / 16; ++k)
-                                ptx::mma_bf16_ss(tmem + TMEM_O + jm * 64,
-                                                 vd + (uint64_t)((2 * jm * BOX_BYTES + k * 2048) >> 4),
-                                                 p_desc0 + (uint64_t)((k * 32) >> 4), idesc_pv, k > 0 ? 1u : acc0);
-                            ptx::mma_commit(&c.lat_empty[st][jm]);
-                        }
-                        ptx::mma_commit(&c.pv_done);
-                    }
-                    __syncwarp();
-                }
+                for (int tl = 0; ok && tl < q.nt; ++tl) ok = pv_tile(gt + tl, tl, idesc_pv);
             }
             gt += q.nt;
         }
@@ -701,11 +692,16 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
     if (warp == 9) ptx::tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// Merge a unit's partials, CTA range by CTA range (that is, in key order):
+// Merge a unit's partials (m_j, l_j, o_j), j in key order:
 //   M = max_j m_j,  w_j = 2^(m_j - M),  out = sum_j w_j o_j / sum_j w_j l_j,
 //   lse = (M + log2 sum_j w_j l_j) * ln 2.
-// One 128-thread block per (stream, column); each thread owns 4 latent columns.
-__global__ void __launch_bounds__(128) mla_combine_kernel(const __grid_constant__ Params p) {
+// One 256-thread block per (stream, column).  Warp w sums the partials j = w, w + 8,
+// ... (lane: 16 latent columns, four independent 16-byte loads a partial), then the
+// eight warp sums are added in warp order: a fixed order, so the result is the same
+// on every call.
+constexpr int COMBINE_THREADS = 256;
+
+__global__ void __launch_bounds__(COMBINE_THREADS) mla_combine_kernel(const __grid_constant__ Params p) {
     const int s = blockIdx.y;
     const int gc = blockIdx.x;
     if (gc >= p.ncols) return;
@@ -726,29 +722,67 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const __grid_constant_
     }
     if (c0 == c1) return;
     const bool ranges = p.mode == MODE_RANGES;
-    auto slot_of = [&](int cc) { return cc == c0 ? first_slot : ranges ? 2 * (cc * p.rep + g) : first_slot + cc; };
-    float M = -INFINITY;
-    for (int cc = c0; cc <= c1; ++cc) M = fmaxf(M, __ldg(p.ws_ml + ((size_t)slot_of(cc) * NCOL + col) * 2));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int n = c1 - c0 + 1;
+    auto slot_of = [&](int j) { return j == 0 ? first_slot : ranges ? 2 * ((c0 + j) * p.rep + g) : first_slot + j; };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ float red_m[COMBINE_THREADS / 32];
+    __shared__ float red_l[COMBINE_THREADS / 32];
+    __shared__ float4 red_o[COMBINE_THREADS / 32][128];
+    float m = -INFINITY;
+    for (int j = threadIdx.x; j < n; j += COMBINE_THREADS)
+        m = fmaxf(m, __ldg(p.ws_ml + ((size_t)slot_of(j) * NCOL + col) * 2));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red_m[warp] = m;
+    __syncthreads();
+    float M = red_m[0];
+#pragma unroll
+    for (int w = 1; w < COMBINE_THREADS / 32; ++w) M = fmaxf(M, red_m[w]);
+    float4 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = 0.f;
-    const int d4 = threadIdx.x;
-    for (int cc = c0; cc <= c1; ++cc) {
-        const size_t base = (size_t)slot_of(cc) * NCOL + col;
+#pragma unroll 2
+    for (int j = warp; j < n; j += COMBINE_THREADS / 32) {
+        const size_t base = (size_t)slot_of(j) * NCOL + col;
         const float mj = __ldg(p.ws_ml + base * 2), lj = __ldg(p.ws_ml + base * 2 + 1);
         const float w = (mj == -INFINITY) ? 0.f : ptx::ex2(mj - M);
-        const float4 o = __ldg(reinterpret_cast<const float4 *>(p.ws_o + base * kLat) + d4);
-        acc.x += w * o.x;
-        acc.y += w * o.y;
-        acc.z += w * o.z;
-        acc.w += w * o.w;
+        const float4 *o = reinterpret_cast<const float4 *>(p.ws_o + base * kLat);
+        float4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = __ldg(o + lane + 32 * i);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[i].x += w * v[i].x;
+            acc[i].y += w * v[i].y;
+            acc[i].z += w * v[i].z;
+            acc[i].w += w * v[i].w;
+        }
         L += w * lj;
     }
-    const float inv = 1.f / L;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) red_o[warp][lane + 32 * i] = acc[i];
+    if (lane == 0) red_l[warp] = L;
+    __syncthreads();
+    if (threadIdx.x >= 128) return;
+    const int d4 = threadIdx.x;
+    float4 tot = red_o[0][d4];
+    float Lt = red_l[0];
+#pragma unroll
+    for (int w = 1; w < COMBINE_THREADS / 32; ++w) {
+        const float4 x = red_o[w][d4];
+        tot.x += x.x;
+        tot.y += x.y;
+        tot.z += x.z;
+        tot.w += x.w;
+        Lt += red_l[w];
+    }
+    const float inv = 1.f / Lt;
     const size_t orow = (size_t)s * p.ncols + gc;
     __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(p.out + orow * kLat) + d4 * 2;
-    o2[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    o2[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    if (threadIdx.x == 0 && p.lse) p.lse[orow] = (M + log2f(L)) * 0.69314718055994531f;
+    o2[0] = __floats2bfloat162_rn(tot.x * inv, tot.y * inv);
+    o2[1] = __floats2bfloat162_rn(tot.z * inv, tot.w * inv);
+    if (threadIdx.x == 0 && p.lse) p.lse[orow] = (M + log2f(Lt)) * 0.69314718055994531f;
 }
 
 // ---- host-side plans ----
@@ -999,7 +1033,7 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     if (cudaGetLastError() != cudaSuccess) return TF_E_CUDA;
     if (slots) {
         ProfScope prof(pool, kProfCombine, st);
-        mla_combine_kernel<<<dim3(R * H, S), 128, 0, st>>>(p);
+        mla_combine_kernel<<<dim3(R * H, S), COMBINE_THREADS, 0, st>>>(p);
         launch_counter()++;
         if (cudaGetLastError() != cudaSuccess) return TF_E_CUDA;
     }
