@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctrl &c = *reinterpret_cast<Ctrl *>(smem + SMEM_CTRL);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    ptx::griddep_launch_dependents();
 
     // every per-launch scalar the roles use, copied out of the parameter block once
     const float scale_log2 = p.scale_log2;
@@ -305,6 +306,8 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
     ptx::tc_fence_after();
     const uint32_t tmem = c.tmem_base;
     volatile int *abort = &c.abort;
+    // on-chip setup done: from here on global memory (pool, tables, queries, outputs)
+    ptx::griddep_wait();
 
     if (warp == 8) {
         // ================= TMA producer =================
@@ -702,6 +705,8 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
 constexpr int COMBINE_THREADS = 256;
 
 __global__ void __launch_bounds__(COMBINE_THREADS) mla_combine_kernel(const __grid_constant__ Params p) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
     const int s = blockIdx.y;
     const int gc = blockIdx.x;
     if (gc >= p.ncols) return;
@@ -1027,15 +1032,15 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     (void)ws_bytes;
     {
         ProfScope prof(pool, kProfAttend, st);
-        mla_attend_kernel<<<pl.nctas, THREADS, SMEM_TOTAL, st>>>(p);
+        const cudaError_t e = launch_pdl(mla_attend_kernel, dim3(pl.nctas), dim3(THREADS), SMEM_TOTAL, st, p);
         launch_counter()++;
+        if (e != cudaSuccess) return TF_E_CUDA;
     }
-    if (cudaGetLastError() != cudaSuccess) return TF_E_CUDA;
     if (slots) {
         ProfScope prof(pool, kProfCombine, st);
-        mla_combine_kernel<<<dim3(R * H, S), COMBINE_THREADS, 0, st>>>(p);
+        const cudaError_t e = launch_pdl(mla_combine_kernel, dim3(R * H, S), dim3(COMBINE_THREADS), 0, st, p);
         launch_counter()++;
-        if (cudaGetLastError() != cudaSuccess) return TF_E_CUDA;
+        if (e != cudaSuccess) return TF_E_CUDA;
     }
     return TF_OK;
 }

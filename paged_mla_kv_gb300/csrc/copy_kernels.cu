@@ -19,6 +19,8 @@ struct AppendParams {
 
 // One warp per new row: 64 + 8 16-byte chunks.
 __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AppendParams p) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (row >= (int64_t)p.S * p.n) return;
@@ -62,9 +64,9 @@ int launch_append(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     if (blocks > 0x7FFFFFFF) return TF_E_UNSUPPORTED;
     if (prepare_launch(pool, st) != TF_OK) return TF_E_CUDA;
     ProfScope prof(pool, kProfAppend, st);
-    append_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
+    const cudaError_t e = launch_pdl(append_kernel, dim3((unsigned)blocks), dim3(256), 0, st, p);
     launch_counter()++;
-    return cudaGetLastError() == cudaSuccess ? TF_OK : TF_E_CUDA;
+    return e == cudaSuccess ? TF_OK : TF_E_CUDA;
 }
 
 // One block per (page of the state, cache): the latent rows [0, rows) are one
@@ -72,6 +74,8 @@ int launch_append(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
 __global__ void __launch_bounds__(512) state_copy_kernel(char *base, int num_pages, int cache0,
                                                          const int32_t *__restrict__ src,
                                                          const int32_t *__restrict__ dst, int64_t at, DevErr *err) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
     const int pg = blockIdx.x;
     const int cache = cache0 + blockIdx.y;
     const int64_t rem = at - (int64_t)pg * kPageRows;
@@ -111,9 +115,10 @@ int launch_state_copy(tf_kvpool *pool, int cache, const int32_t *d_src, const in
     dim3 grid((unsigned)pages, (unsigned)nc);
     if (prepare_launch(pool, st) != TF_OK) return TF_E_CUDA;
     ProfScope prof(pool, kProfCopy, st);
-    state_copy_kernel<<<grid, 512, 0, st>>>(pool->base, pool->desc.num_pages, c0, d_src, d_dst, at, pool->err);
+    const cudaError_t e = launch_pdl(state_copy_kernel, grid, dim3(512), 0, st, pool->base, pool->desc.num_pages, c0,
+                                     d_src, d_dst, at, pool->err);
     launch_counter()++;
-    return cudaGetLastError() == cudaSuccess ? TF_OK : TF_E_CUDA;
+    return e == cudaSuccess ? TF_OK : TF_E_CUDA;
 }
 
 constexpr int kPoisonIds = 2048;
@@ -125,6 +130,8 @@ struct PoisonParams {
 
 // grid (ids, caches, 16 slices of a page): fill with the bf16 NaN pattern 0x7FC0.
 __global__ void __launch_bounds__(256) poison_kernel(const __grid_constant__ PoisonParams p) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
     const int id = p.ids[blockIdx.x];
     const int cache = blockIdx.y;
     uint4 *pg = reinterpret_cast<uint4 *>(p.base + ((size_t)cache * p.num_pages + id) * kPageBytes);
@@ -145,9 +152,9 @@ int launch_poison(tf_kvpool *pool, const int32_t *h_ids, int n, cudaStream_t st)
         for (int i = 0; i < p.n; ++i) p.ids[i] = h_ids[b + i];
         dim3 grid((unsigned)p.n, (unsigned)p.num_caches, 16);
         ProfScope prof(pool, kProfPoison, st);
-        poison_kernel<<<grid, 256, 0, st>>>(p);
+        const cudaError_t e = launch_pdl(poison_kernel, grid, dim3(256), 0, st, p);
         launch_counter()++;
-        if (cudaGetLastError() != cudaSuccess) return TF_E_CUDA;
+        if (e != cudaSuccess) return TF_E_CUDA;
     }
     return TF_OK;
 }

@@ -91,6 +91,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// A kernel launched with programmatic stream serialization may start while the
+// previous kernel of the stream is still running.  Every kernel of the library lets
+// its successor launch at once and waits for its predecessor (complete, memory
+// visible) before it touches global memory: only the launch and the on-chip setup
+// overlap.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- thread-block clusters (distributed shared memory) ----------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

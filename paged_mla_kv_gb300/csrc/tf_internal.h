@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "../../include/tf_paged_mla.h"
@@ -78,6 +79,23 @@ struct ProfScope {
     ProfScope(tf_kvpool *p, int k, cudaStream_t s);
     ~ProfScope();
 };
+
+// Launch with programmatic stream serialization (see griddep_wait in ptx.cuh).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Kernel launchers (defined in the .cu files).  Arguments are already validated.
 int launch_append(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages, const int64_t *h_pos,
