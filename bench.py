@@ -68,6 +68,25 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> floa
     return world * units_per_rank / (slowest_ms / 1e3)
 
 
+# dram__bytes_read.sum + dram__bytes_write.sum of one mla_attend_kernel launch, from the ncu
+# captures summarised in profiles/ (mla_attend_<workload>.md).  Keyed by the first 16 hex
+# digits of the SHA-256 of the attention kernel's source the capture was taken on: once
+# the kernel changes, the counters no longer describe it and "traffic" is reported null.
+NCU_TRAFFIC = {
+    "dcf182b05d132441": {"decode_batch": 373_832_192 + 3_505_664, "prefill_100k": 1_795_208_000 + 133_645_824},
+}
+
+
+def ncu_traffic(workload: str):
+    import hashlib
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "paged_mla_kv_gb300", "csrc", "attend.cu")
+    try:
+        key = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return NCU_TRAFFIC.get(key, {}).get(workload)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -321,13 +340,15 @@ def main():
         achieved = units["attend_flops"] / (avg_att / 1e3) / 1e12
         peak = peaks.get("bf16_tflops_sustained", 1700.0)
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None, "peak_kind": f"{peak_src} bf16 sustained", "kernel": "mla_attend_kernel",
+                "traffic": ncu_traffic(args.workload), "peak_kind": f"{peak_src} bf16 sustained",
+                "kernel": "mla_attend_kernel",
                 "avg_launch_ms": avg_att}
     else:
         achieved = units["attend_bytes"] / (avg_att / 1e3) / 1e9
         peak = peaks.get("hbm_gbs", 6800.0)
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": None, "peak_kind": f"{peak_src} HBM copy", "kernel": "mla_attend_kernel",
+                "traffic": ncu_traffic(args.workload), "peak_kind": f"{peak_src} HBM copy",
+                "kernel": "mla_attend_kernel",
                 "avg_launch_ms": avg_att}
 
     # end to end through the C-ABI with host buffers: queries and new rows in, outputs out
