@@ -153,6 +153,34 @@ def test_prefill_chunk(T, L, H):
     compare(w, out, lse)
 
 
+def _lens(seed, n, lo, hi):
+    return np.random.default_rng(seed).integers(lo, hi + 1, n).tolist()
+
+
+# Batches shaped to reach every branch of the work plan: many short streams (CTAs walking
+# several segments, with query reloads and mid-range epilogues), the most streams and heads
+# the API takes, column groups side by side (2, 4 and 10 groups, ragged last group), whole
+# units round robin (prefill-like, several streams), and the batch-invariant split plan.
+PLAN_SHAPES = [
+    ("segments", 60, _lens(60, 200, 1, 600), 1, 8, False),
+    ("max_streams", 61, _lens(61, 512, 1, 300), 1, 16, False),
+    ("max_heads_r2", 62, [5000, 17, 900, 12000], 2, 128, False),
+    ("ragged_groups", 63, [3000, 40, 700], 5, 24, False),
+    ("ten_groups", 64, [2500, 1300], 40, 16, False),
+    ("units", 65, [1200, 700, 160], 160, 64, False),
+    ("invariant_groups", 66, [5000, 17, 900, 12000], 2, 128, True),
+    ("invariant_units", 67, [1200, 700, 160], 160, 64, True),
+]
+
+
+@pytest.mark.parametrize("name,seed,lens,R,H,invariant", PLAN_SHAPES, ids=[x[0] for x in PLAN_SHAPES])
+def test_work_plan_shapes(name, seed, lens, R, H, invariant):
+    lens = [max(int(x), R) for x in lens]
+    w = Y.custom(name, seed, lens=lens, R=R, H=H)
+    _, out, lse = run(w, invariant=invariant)
+    compare(w, out, lse)
+
+
 # ---------------------------------------------------------------- invariants
 
 
