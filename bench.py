@@ -277,10 +277,10 @@ def main():
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") \
         if units["kv"] < 2 * L2_BYTES else None
 
-    def step(q_list=qs, rows=cur):
+    def step(q_list=qs, rows=cur, o=out, l=lse):
         for c in range(w.num_caches):
             res.append_current(c, rows[c][0], rows[c][1])
-            B.tf_paged_mla_attend(res.pool, c, res.pt, res.max_pages, res.lens, q_list[c], w.scale, out, lse, ws)
+            B.tf_paged_mla_attend(res.pool, c, res.pt, res.max_pages, res.lens, q_list[c], w.scale, o, l, ws)
         if at:
             B.tf_state_copy_rows(res.pool, -1, src, dst, at)
 
@@ -296,18 +296,28 @@ def main():
     for _ in range(args.warmup):
         step()
     barrier()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     n0 = B.tf_launch_count()
     barrier()
-    for i in range(args.steps):
-        if flush is not None:
+    if flush is None:
+        # inputs larger than L2: K steps back to back between one pair of events
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(args.steps):
+            step()
+        e1.record()
+        barrier()
+        total_ms = e0.elapsed_time(e1)
+    else:
+        # L2 flushed between steps, outside each step's pair of events
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
             flush.zero_()
-        ev[i][0].record()
-        step()
-        ev[i][1].record()
-    barrier()
+            ev[i][0].record()
+            step()
+            ev[i][1].record()
+        barrier()
+        total_ms = sum(a.elapsed_time(b) for a, b in ev)
     launches = B.tf_launch_count() - n0
-    total_ms = sum(a.elapsed_time(b) for a, b in ev)
     # the attention kernel's own duration: CUDA events around each of its launches, on
     # its stream, in a second pass of the same steps (the events cost ~15 us a step and
     # serialise the launches, so they stay out of the timed region above)
@@ -356,32 +366,77 @@ def main():
     if not args.no_e2e:
         hq = [q.cpu().pin_memory() for q in qs]
         hrows = [(a.cpu().pin_memory(), b.cpu().pin_memory()) for a, b in cur]
-        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        dq = [torch.empty_like(q) for q in qs]
-        drows = [(torch.empty_like(a), torch.empty_like(b)) for a, b in cur]
+        nb = 2   # double buffers: step i+1's inputs and step i-1's outputs move while step i runs
+        dq = [[torch.empty_like(q) for q in qs] for _ in range(nb)]
+        drows = [[(torch.empty_like(a), torch.empty_like(b)) for a, b in cur] for _ in range(nb)]
+        dout = [torch.empty_like(out) for _ in range(nb)]
+        dlse = [torch.empty_like(lse) for _ in range(nb)]
+        hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(nb)]
+        hlse = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(nb)]
+        main = torch.cuda.current_stream()
+        cs = torch.cuda.Stream()
+        in_ready = [torch.cuda.Event() for _ in range(nb)]
+        done = [torch.cuda.Event() for _ in range(nb)]
+        out_read = [torch.cuda.Event() for _ in range(nb)]
+        for b_ in range(nb):           # every event recorded once, so the first waits pass
+            done[b_].record(main)
+            out_read[b_].record(main)
 
-        def e2e_step():
-            for c in range(w.num_caches):
-                dq[c].copy_(hq[c], non_blocking=True)
-                drows[c][0].copy_(hrows[c][0], non_blocking=True)
-                drows[c][1].copy_(hrows[c][1], non_blocking=True)
-            step(dq, drows)
-            hout.copy_(out, non_blocking=True)
-            hlse.copy_(lse, non_blocking=True)
+        def h2d(i):
+            b_ = i % nb
+            with torch.cuda.stream(cs):
+                cs.wait_event(done[b_])        # step i-2 has consumed this buffer
+                for c in range(w.num_caches):
+                    dq[b_][c].copy_(hq[c], non_blocking=True)
+                    drows[b_][c][0].copy_(hrows[c][0], non_blocking=True)
+                    drows[b_][c][1].copy_(hrows[c][1], non_blocking=True)
+                in_ready[b_].record(cs)
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+        def compute(i):
+            b_ = i % nb
+            main.wait_event(in_ready[b_])
+            main.wait_event(out_read[b_])      # step i-2's outputs have left this buffer
+            step(dq[b_], drows[b_], dout[b_], dlse[b_])
+            done[b_].record(main)
+
+        def d2h(i):
+            b_ = i % nb
+            with torch.cuda.stream(cs):
+                cs.wait_event(done[b_])
+                hout[b_].copy_(dout[b_], non_blocking=True)
+                hlse[b_].copy_(dlse[b_], non_blocking=True)
+                out_read[b_].record(cs)
+
+        def run_e2e(n):
+            h2d(0)
+            for i in range(n):
+                if i + 1 < n:
+                    h2d(i + 1)
+                compute(i)
+                d2h(i)
+            main.wait_event(out_read[(n - 1) % nb])
+
+        run_e2e(max(2, args.warmup))
         barrier()
-        e2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        for i in range(args.steps):
-            if flush is not None:
+        if flush is None:
+            # inputs larger than L2: the steps run back to back, copies overlapped, one pair of events
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(main)
+            run_e2e(args.steps)
+            e1.record(main)
+            barrier()
+            e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, pg, "cuda")
+        else:
+            # the L2 flush between steps stays outside the events: each step is copied in,
+            # run and copied out on its own
+            e2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+            for i in range(args.steps):
                 flush.zero_()
-            e2[i][0].record()
-            e2e_step()
-            e2[i][1].record()
-        barrier()
-        e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2) / args.steps, pg, "cuda")
+                e2[i][0].record(main)
+                run_e2e(1)
+                e2[i][1].record(main)
+            barrier()
+            e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2) / args.steps, pg, "cuda")
         h2d = sum(q.numel() * 2 for q in qs) + sum(a.numel() * 2 + b.numel() * 2 for a, b in cur)
         d2h = out.numel() * 2 + lse.numel() * 4
         ev_ = world * (units["flops"] / 1e12 if prefill else units["bytes"] / 1e9) / (e_ms / 1e3)
