@@ -133,14 +133,19 @@ struct Params {
     int32_t mode;
     int32_t nranges;      // RANGES: ranges of the numbering
     int32_t rep;          // RANGES: CTAs a range (the column groups)
+    int64_t rb[MAX_CTAS + 1];        // RANGES: range i is tiles [rb[i], rb[i+1])
     StreamPlan st[TF_MAX_STREAMS];
     int16_t order[TF_MAX_STREAMS];   // SPLITS: launch order (streams with longer splits first)
 };
 
-// First global tile of CTA i, and the CTA whose range holds global tile x.
-__host__ __device__ __forceinline__ int64_t cta_begin(int64_t i, int64_t total, int n) { return i * total / n; }
-__host__ __device__ __forceinline__ int cta_of(int64_t x, int64_t total, int n) {
-    return (int)(((int64_t)n * (x + 1) - 1) / total);
+// The range that holds numbered tile x.
+__device__ __forceinline__ int range_of(const Params &p, int64_t x) {
+    int lo = 0, hi = p.nranges - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.rb[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
 }
 
 // A CTA's range, cut at unit boundaries: each piece (a segment) attends one column
@@ -184,8 +189,8 @@ struct SegIter {
     __device__ __forceinline__ explicit SegIter(const Params &p) : x(0), x0(0), x1(0), k(0) {
         if (p.mode == MODE_RANGES) {
             const int range = (int)blockIdx.x / p.rep;
-            x0 = cta_begin(range, p.total, p.nranges);
-            x1 = cta_begin(range + 1, p.total, p.nranges);
+            x0 = p.rb[range];
+            x1 = p.rb[range + 1];
             x = x0;
         }
     }
@@ -716,9 +721,9 @@ __global__ void __launch_bounds__(COMBINE_THREADS) mla_combine_kernel(const __gr
     if (p.mode == MODE_RANGES) {
         // the ranges that hold the unit; their CTAs' partial slots
         const int64_t ub = sp.toff, ue = ub + sp.nt;
-        c0 = cta_of(ub, p.total, p.nranges);
-        c1 = cta_of(ue - 1, p.total, p.nranges);
-        first_slot = 2 * (c0 * p.rep + g) + (ub == cta_begin(c0, p.total, p.nranges) ? 0 : 1);
+        c0 = range_of(p, ub);
+        c1 = range_of(p, ue - 1);
+        first_slot = 2 * (c0 * p.rep + g) + (ub == p.rb[c0] ? 0 : 1);
     } else {
         if (p.mode != MODE_SPLITS || sp.nsplit <= 1) return;
         c0 = 0;
@@ -828,7 +833,9 @@ inline Split split_of(int64_t len, int groups) {
     return sp;
 }
 
-inline Plan plan_of(int S, int R, int H, const int64_t *h_len, int sms, bool invariant) {
+constexpr int64_t SEG_COST = 3;   // a segment start, in key tiles
+
+inline Plan plan_of(int S, int R, int H, const int64_t *h_len, int sms, bool invariant, int64_t *rb = nullptr) {
     Plan pl;
     const int groups = (R * H + NCOL - 1) / NCOL;
     pl.slots = 0;
@@ -860,15 +867,43 @@ inline Plan plan_of(int S, int R, int H, const int64_t *h_len, int sms, bool inv
     pl.nranges = (int)(want < cap ? want : cap);
     if (pl.nranges < 1) pl.nranges = 1;
     pl.nctas = pl.nranges * pl.rep;
-    // a boundary between two ranges cuts a stream unless it falls between streams
+    // Range boundaries.  A range that starts a second stream pays for a query reload
+    // and an extra epilogue, about SEG_COST tiles: a stream's first tile is weighted
+    // 1 + SEG_COST and the ranges cut the weighted sequence into equal parts.  A cut
+    // that lands inside a stream's extra weight moves to the stream's start.
+    int64_t rb_local[MAX_CTAS + 1];
+    int64_t *b = rb ? rb : rb_local;
+    const int64_t U = pl.total + SEG_COST * (int64_t)(S - 1);
+    b[0] = 0;
+    b[pl.nranges] = pl.total;
+    int s = 0;
+    int64_t toff = 0;   // first tile of stream s
+    for (int i = 1; i < pl.nranges; ++i) {
+        const int64_t tau = (int64_t)i * U / pl.nranges;   // weighted position of the cut
+        // advance to the last stream whose weighted start is <= tau
+        while (s + 1 < S) {
+            const int64_t next = toff + (h_len[s] + BK - 1) / BK;
+            if (next + SEG_COST * (int64_t)(s + 1) > tau) break;
+            toff = next;
+            ++s;
+        }
+        const int64_t u0 = toff + SEG_COST * (int64_t)s;   // weighted start of stream s
+        int64_t x = toff + (tau > u0 ? tau - u0 : 0);
+        const int64_t end = toff + (h_len[s] + BK - 1) / BK;
+        if (x > end) x = end;
+        if (x <= b[i - 1]) x = b[i - 1] + 1;
+        const int64_t room = pl.total - (pl.nranges - i);   // leave a tile for every later range
+        if (x > room) x = room;
+        b[i] = x;
+    }
+    // a boundary cuts a stream unless it falls between streams
     bool split = false;
     for (int i = 1; i < pl.nranges && !split; ++i) {
-        const int64_t b = cta_begin(i, pl.total, pl.nranges);
         int64_t off = 0;
-        for (int s = 0; s < S; ++s) {
-            if (b == off) break;
-            off += (h_len[s] + BK - 1) / BK;
-            if (b < off) {
+        for (int ss = 0; ss < S; ++ss) {
+            if (b[i] == off) break;
+            off += (h_len[ss] + BK - 1) / BK;
+            if (b[i] < off) {
                 split = true;
                 break;
             }
@@ -992,7 +1027,7 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     p.groups = (R * H + NCOL - 1) / NCOL;
     p.windowed = d_pt ? 0 : 1;
     const bool invariant = (pool->desc.flags & TF_POOL_BATCH_INVARIANT) != 0;
-    const Plan pl = plan_of(S, R, H, h_len, device_sms(), invariant);
+    const Plan pl = plan_of(S, R, H, h_len, device_sms(), invariant, p.rb);
     p.mode = pl.mode;
     p.total = pl.total;
     p.nranges = pl.nranges;
