@@ -183,11 +183,13 @@ __device__ __forceinline__ Seg seg_at(const Params &p, int64_t x, int64_t x0, in
 }
 
 // This CTA's segments, in order, for every mode.
+// The kernel is compiled once per mode, so each instance carries only its own plan.
+template <int MODE>
 struct SegIter {
     int64_t x, x0, x1;
     int k;
     __device__ __forceinline__ explicit SegIter(const Params &p) : x(0), x0(0), x1(0), k(0) {
-        if (p.mode == MODE_RANGES) {
+        if (MODE == MODE_RANGES) {
             const int range = (int)blockIdx.x / p.rep;
             x0 = p.rb[range];
             x1 = p.rb[range + 1];
@@ -195,13 +197,13 @@ struct SegIter {
         }
     }
     __device__ __forceinline__ bool next(const Params &p, Seg &q) {
-        if (p.mode == MODE_RANGES) {
+        if (MODE == MODE_RANGES) {
             if (x >= x1) return false;
             q = seg_at(p, x, x0, x1);
             x += q.nt;
             return true;
         }
-        if (p.mode == MODE_UNITS) {
+        if (MODE == MODE_UNITS) {
             const int64_t u = (int64_t)blockIdx.x + (int64_t)k * gridDim.x;
             if (u >= p.total) return false;
             ++k;
@@ -260,6 +262,7 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tm, ui
 // rescale group, done with the previous segment's epilogue, posts its p_full, so
 // the accumulator is never overwritten while it is still being read.
 
+template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -329,7 +332,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
             int q_armed = -1;       // last segment whose queries were loaded
             bool stop = false;
             int gt = 0, si = 0;
-            SegIter it(p);
+            SegIter<MODE> it(p);
             Seg q;
             for (; !stop && it.next(p, q); ++si) {
                 // the query tile is reloaded once the previous segment's QK^T has read it
@@ -461,7 +464,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
         };
         bool ok = true;
         int gt = 0, si = 0;
-        SegIter it(p);
+        SegIter<MODE> it(p);
         Seg q;
         for (; ok && it.next(p, q); ++si) {
             const int ncols = min(NCOL, ncols_all - q.g * NCOL);
@@ -490,7 +493,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
         const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
         bool ok = true;
         int gt = 0, si = 0;
-        SegIter it(p);
+        SegIter<MODE> it(p);
         Seg q;
         for (; ok && it.next(p, q); ++si) {
             const int col0 = q.g * NCOL;
@@ -525,11 +528,24 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
                 float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const int key = 8 * j + kq;
-                    x0[2 * j] = key < nv0 ? __uint_as_float(r[4 * j]) : -INFINITY;
-                    x0[2 * j + 1] = key + 1 < nv0 ? __uint_as_float(r[4 * j + 1]) : -INFINITY;
-                    x1[2 * j] = key < nv1 ? __uint_as_float(r[4 * j + 2]) : -INFINITY;
-                    x1[2 * j + 1] = key + 1 < nv1 ? __uint_as_float(r[4 * j + 3]) : -INFINITY;
+                    x0[2 * j] = __uint_as_float(r[4 * j]);
+                    x0[2 * j + 1] = __uint_as_float(r[4 * j + 1]);
+                    x1[2 * j] = __uint_as_float(r[4 * j + 2]);
+                    x1[2 * j + 1] = __uint_as_float(r[4 * j + 3]);
+                }
+                // only a range's or a stream's last tile (and causal rows) hold keys to mask
+                if (!__all_sync(0xffffffffu, (nv0 == BK) & (nv1 == BK))) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int key = 8 * j + kq;
+                        if (key >= nv0) x0[2 * j] = -INFINITY;
+                        if (key + 1 >= nv0) x0[2 * j + 1] = -INFINITY;
+                        if (key >= nv1) x1[2 * j] = -INFINITY;
+                        if (key + 1 >= nv1) x1[2 * j + 1] = -INFINITY;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
                     mx0 = fmaxf(mx0, fmaxf(x0[2 * j], x0[2 * j + 1]));
                     mx1 = fmaxf(mx1, fmaxf(x1[2 * j], x1[2 * j + 1]));
                 }
@@ -617,7 +633,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
         const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
         bool ok = true;
         int gt = 0, si = 0;
-        SegIter it(p);
+        SegIter<MODE> it(p);
         Seg q;
         for (; ok && it.next(p, q); ++si) {
             const int col0 = q.g * NCOL;
@@ -992,8 +1008,12 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     if (prepare_launch(pool, st) != TF_OK) return TF_E_CUDA;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(mla_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(mla_attend_kernel<MODE_RANGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_TOTAL) != cudaSuccess ||
+            cudaFuncSetAttribute(mla_attend_kernel<MODE_UNITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_TOTAL) != cudaSuccess ||
+            cudaFuncSetAttribute(mla_attend_kernel<MODE_SPLITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_TOTAL) != cudaSuccess)
             return TF_E_CUDA;
         attr_set = true;
     }
@@ -1067,7 +1087,10 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     (void)ws_bytes;
     {
         ProfScope prof(pool, kProfAttend, st);
-        const cudaError_t e = launch_pdl(mla_attend_kernel, dim3(pl.nctas), dim3(THREADS), SMEM_TOTAL, st, p);
+        auto *kern = pl.mode == MODE_RANGES  ? mla_attend_kernel<MODE_RANGES>
+                     : pl.mode == MODE_UNITS ? mla_attend_kernel<MODE_UNITS>
+                                             : mla_attend_kernel<MODE_SPLITS>;
+        const cudaError_t e = launch_pdl(kern, dim3(pl.nctas), dim3(THREADS), SMEM_TOTAL, st, p);
         launch_counter()++;
         if (e != cudaSuccess) return TF_E_CUDA;
     }
