@@ -63,12 +63,12 @@ constexpr int TMEM_COLS = 512;
 constexpr int TMEM_O = 0;                       // O^T M-tile j at 64 j (j < 4)
 constexpr int TMEM_S = 256;                     // S buffers at 256 and 320
 constexpr int THREADS = 352;
-// A tile's QK^T runs in two parts: part 0 takes the rope box and latent boxes 0-3,
-// part 1 latent boxes 4-7.  PV of the previous tile is issued between the two parts,
-// so the tensor pipe keeps working while the softmax runs and the previous tile's
-// latent boxes are released (pair by pair) as early as possible for the next loads.
+// A key tile lands in two parts: part 0 the rope box (free once QK^T has read it) and
+// latent boxes 0-1 (the first pair PV releases), part 1 latent boxes 2-7.  QK^T starts
+// on part 0 while the rest of the tile is still loading; the previous tile's latent
+// boxes are released pair by pair as soon as the PV M-tile that reads them is done.
 __device__ __constant__ int kBoxOrder[NBOX] = {8, 0, 1, 2, 3, 4, 5, 6, 7};
-constexpr int kPart0Boxes = 5;
+constexpr int kPart0Boxes = 3;
 constexpr int MIN_TILES = 4;                    // fewest key tiles a CTA is given
 constexpr int SPLIT_UNIT = 256;                 // batch-invariant split sizes are multiples of this
 static_assert(SPLIT_UNIT % BK == 0, "splits must be tile-aligned");
@@ -76,7 +76,7 @@ constexpr int MAX_CTAS = 240;                   // CTAs a launch (one a SM); siz
 constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(64, BK, false, false);
 
 struct Ctrl {
-    uint64_t part_full[NSTAGE][2];     // part 0: rope + latent boxes 0-3 landed; part 1: latent boxes 4-7
+    uint64_t part_full[NSTAGE][2];     // part 0: rope + latent boxes 0-1 landed; part 1: latent boxes 2-7
     uint64_t lat_empty[NSTAGE][4];     // latent box pair (2j, 2j+1) free: PV M-tile j done
     uint64_t rope_empty[NSTAGE];       // rope box free: QK^T done
     uint64_t s_full[2], s_free[2];
@@ -284,8 +284,8 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSTAGE; ++i) {
-            ptx::mbar_init(&c.part_full[i][0], 5);
-            ptx::mbar_init(&c.part_full[i][1], 4);
+            ptx::mbar_init(&c.part_full[i][0], kPart0Boxes);
+            ptx::mbar_init(&c.part_full[i][1], NBOX - kPart0Boxes);
             for (int jm = 0; jm < 4; ++jm) ptx::mbar_init(&c.lat_empty[i][jm], 1);
             ptx::mbar_init(&c.rope_empty[i], 1);
         }
