@@ -28,7 +28,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOADS = ["decode_batch", "tiny_decode", "long_window", "prefill_100k", "prefill_208k", "full_model"]
+WORKLOADS = ["decode_batch", "tiny_decode", "long_window", "prefill_100k", "prefill_208k", "full_model",
+             "sparse_decode"]
 METRIC = "paged MLA decode KV GB/s + tokens/s vs HBM roofline; prefill TFLOP/s"
 L2_BYTES = 129 * 1024 * 1024
 
@@ -104,6 +105,16 @@ def step_units(w):
     """Algorithmic work of one step: bytes, flops, tokens."""
     from paged_mla_kv_gb300 import synth as Y
     S, R, H, C = w.S, w.R, w.H, w.num_caches
+    if "nidx" in w.extra:
+        # attention over listed rows: each stream reads its listed rows once for all heads
+        n = [min(int(w.extra["nidx"]), int(L)) for L in w.lens]
+        kv = sum(n) * Y.ROW_BYTES
+        q = S * H * Y.DK * 2
+        out = S * H * (512 * 2 + 4)
+        app = 2 * S * Y.ROW_BYTES
+        flops = 2 * (Y.DK + 512) * H * sum(n)
+        return dict(bytes=kv + q + out + app, attend_bytes=kv + q + out, flops=flops, attend_flops=flops,
+                    tokens=S, kv=kv)
     kv = int(np.sum(w.lens)) * Y.ROW_BYTES
     q = S * R * H * Y.DK * 2
     out = S * R * H * (512 * 2 + 4)
@@ -182,6 +193,10 @@ class OracleSample:
         self.prefill = w.R > 2
         self.q = w.q(0)
         self.rows = [w.stream_rows(0, s) for s in range(w.S)]
+        self.lists = None
+        if "nidx" in w.extra:
+            from paged_mla_kv_gb300 import synth as Y
+            self.lists = Y.listed_rows(w.seed, w.lens, int(w.extra["nidx"]))
         k0 = min(w.R if self.prefill else w.H, max(1, self.threads // (w.R if not self.prefill else 1)))
         k0 = max(1, min(k0, self.threads))
         t0, _ = self.run(k0)
@@ -203,6 +218,11 @@ class OracleSample:
         if self.prefill:
             self.OA.attend_stream(self.q[0], self.rows[0][0], self.rows[0][1], w.scale, items, self.threads)
             work = sum(2 * 1088 * (int(w.lens[0]) - w.R + int(r) + 1) for r in rows) * w.H
+        elif self.lists is not None:
+            for s in range(w.S):
+                self.OA.attend_sparse(self.q[s, 0, :k], self.rows[s][0], self.rows[s][1], self.lists[s], w.scale,
+                                      self.threads)
+                work += len(self.lists[s]) * 1152 * k / w.H
         else:
             for s in range(w.S):
                 self.OA.attend_stream(self.q[s], self.rows[s][0], self.rows[s][1], w.scale, items, self.threads)
@@ -217,9 +237,9 @@ class OracleSample:
             return dict(value=work / t / 1e12, unit="TFLOP/s", cores=self.threads, kind="oracle",
                         sample=f"{len(rows)} of {w.R} query rows spread over the chunk, all {w.H} heads, "
                                f"cache 0 ({t:.1f} s)")
+        what = "listed rows" if self.lists is not None else f"all {w.R} rows"
         return dict(value=work / t / 1e9, unit="GB/s", cores=self.threads, kind="oracle",
-                    sample=f"first {self.k} of {w.H} heads of all {w.S} streams, all {w.R} rows, cache 0 "
-                           f"({t:.1f} s)")
+                    sample=f"first {self.k} of {w.H} heads of all {w.S} streams, {what}, cache 0 ({t:.1f} s)")
 
 
 def reference_arm(args, rank, world):
@@ -277,10 +297,26 @@ def main():
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") \
         if units["kv"] < 2 * L2_BYTES else None
 
+    sparse = "nidx" in w.extra
+    if sparse:
+        from paged_mla_kv_gb300 import synth as Y
+        lists = Y.listed_rows(w.seed, w.lens, int(w.extra["nidx"]))
+        nidx = np.array([len(x) for x in lists], np.int32)
+        idx_h = np.zeros((w.S, int(nidx.max())), np.int32)
+        for s_, x in enumerate(lists):
+            idx_h[s_, :len(x)] = x
+        idx_d = torch.from_numpy(idx_h).cuda()
+        nws = B.tf_paged_mla_sparse_workspace_bytes(res.pool, w.S, w.H, nidx)
+        ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda") if nws else None
+
     def step(q_list=qs, rows=cur, o=out, l=lse):
         for c in range(w.num_caches):
             res.append_current(c, rows[c][0], rows[c][1])
-            B.tf_paged_mla_attend(res.pool, c, res.pt, res.max_pages, res.lens, q_list[c], w.scale, o, l, ws)
+            if sparse:
+                B.tf_paged_mla_attend_sparse(res.pool, c, res.pt, res.max_pages, res.lens, idx_d, nidx, q_list[c],
+                                             w.scale, o, l, ws)
+            else:
+                B.tf_paged_mla_attend(res.pool, c, res.pt, res.max_pages, res.lens, q_list[c], w.scale, o, l, ws)
         if at:
             B.tf_state_copy_rows(res.pool, -1, src, dst, at)
 

@@ -219,6 +219,28 @@ int tf_paged_mla_attend(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int
  *   order them on one stream, or use tf_paged_mla_attend with separate workspaces. */
 #define TF_STATIC_WS_BYTES (64u << 20)
 
+/* ---- attention over listed rows (issue #1313, step 2: a sparse row reads up to 2,048
+ * latent rows; issue #1142, section 2: the latent kernels for dense chunks and the sparse
+ * gather take the page table; "What stays as it is": the sparse pass gathers the same rows) ----
+ * One query row a stream (R = 1).  Stream s's keys are the rows d_idx[s][0 .. h_nidx[s]) of the
+ * stream (row numbers as in tf_paged_mla_attend, each < h_len[s]), in list order:
+ *   s_j = scale * (q[s][h][0:512] . C_idx[j] + q[s][h][512:576] . Kr_idx[j])
+ *   out[s][h][:] = sum_j softmax(s)_j * C_idx[j];  lse[s][h] = log sum_j exp(s_j).
+ * A row listed twice counts twice.  d_idx: int32 [S][max_idx] device; entries past h_nidx[s] are
+ * not read.  d_q: bf16 [S][H][576]; d_out: bf16 [S][H][512]; d_lse: fp32 [S][H] or NULL.
+ * Each row is fetched through d_pt (or the contiguous windows of a NULL table) with TMA gathers.
+ * A listed row outside [0, h_len[s]) or a table entry outside the pool is recorded as
+ * TF_E_DEVICE and the call's output is undefined.  Limits: 1 <= h_nidx[s] <= max_idx, S and H as
+ * for tf_paged_mla_attend; the pool must have fewer than 2^31 / 4,608 pages over all caches
+ * (TF_E_UNSUPPORTED).  The keys are dealt out as in the default plan of tf_paged_mla_attend
+ * (whatever the pool's flags); d_ws holds the partials as there. */
+size_t tf_paged_mla_sparse_workspace_bytes(const tf_kvpool *pool, int32_t S, int32_t H, const int32_t *h_nidx);
+
+int tf_paged_mla_attend_sparse(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int32_t max_pages,
+                               const int64_t *h_len, const int32_t *d_idx, int32_t max_idx, const int32_t *h_nidx,
+                               int32_t S, int32_t H, const void *d_q, float scale, void *d_out, float *d_lse,
+                               void *d_ws, size_t ws_bytes, void *cuda_stream);
+
 int tf_paged_mla_attend_static(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int32_t max_pages,
                                const int64_t *h_len, int32_t S, int32_t R, int32_t H,
                                const void *d_q, float scale, void *d_out, float *d_lse, void *cuda_stream);

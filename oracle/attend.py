@@ -66,6 +66,22 @@ def attend_stream(q: np.ndarray, lat: np.ndarray, rope: np.ndarray, scale: float
     return out, lse
 
 
+def attend_sparse(q: np.ndarray, lat: np.ndarray, rope: np.ndarray, idx, scale: float,
+                  threads: int | None = None):
+    """Attention of one query row over listed rows of a stream.
+
+    Issue #1313, step 2: a sparse row reads up to 2,048 listed latent rows; issue #1142,
+    "What stays as it is": the sparse pass gathers the same rows.  The keys are the rows
+    idx[0..n) in list order (a row listed twice counts twice), so this is the contiguous
+    definition above applied to the gathered rows.
+    q: bf16 bits [H][576]; lat: [len][512]; rope: [len][64]; idx: n row numbers in [0, len).
+    Returns (out [H][512], lse [H]) in float64.
+    """
+    idx = np.asarray(idx, np.int64)
+    assert idx.ndim == 1 and len(idx) >= 1 and idx.min() >= 0 and idx.max() < lat.shape[0]
+    return attend_stream(np.asarray(q)[None], np.asarray(lat)[idx], np.asarray(rope)[idx], scale, threads=threads)
+
+
 def attend_workload(w, cache: int = 0, items_per_stream=None, threads: int | None = None):
     """Oracle outputs for every stream of a synth.Workload.
 

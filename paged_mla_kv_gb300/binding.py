@@ -67,6 +67,9 @@ _SIGS = {
     "tf_paged_mla_workspace_bytes": (_SZ, [_P, _I32, _I32, _I32, _P]),
     "tf_paged_mla_attend": (ctypes.c_int, [_P, _I32, _P, _I32, _P, _I32, _I32, _I32, _P, _F, _P, _P, _P, _SZ, _P]),
     "tf_paged_mla_attend_static": (ctypes.c_int, [_P, _I32, _P, _I32, _P, _I32, _I32, _I32, _P, _F, _P, _P, _P]),
+    "tf_paged_mla_sparse_workspace_bytes": (_SZ, [_P, _I32, _I32, _P]),
+    "tf_paged_mla_attend_sparse": (ctypes.c_int, [_P, _I32, _P, _I32, _P, _P, _I32, _P, _I32, _I32, _P, _F, _P, _P,
+                                                  _P, _SZ, _P]),
     "tf_state_copy_rows": (ctypes.c_int, [_P, _I32, _P, _P, _I64, _P]),
     "tf_last_error": (ctypes.c_int, [_P, ctypes.POINTER(_I64)]),
     "tf_diag_wait_timeout": (ctypes.c_int, [_P, _I64, _P]),
@@ -251,6 +254,30 @@ def tf_paged_mla_attend_static(pool: KVPool, cache: int, pt, max_pages: int, len
     _check(lib().tf_paged_mla_attend_static(pool.handle, cache, _ptr(pt), max_pages, p, S, R, H, _ptr(q),
                                             float(scale), _ptr(out), _ptr(lse), _stream(stream)),
            "tf_paged_mla_attend_static")
+
+
+def _i32(a):
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+def tf_paged_mla_sparse_workspace_bytes(pool, S: int, H: int, nidx) -> int:
+    a, p = _i32(nidx)
+    return int(lib().tf_paged_mla_sparse_workspace_bytes(pool.handle if pool is not None else None, S, H, p))
+
+
+def tf_paged_mla_attend_sparse(pool: KVPool, cache: int, pt, max_pages: int, lens, idx, nidx, q, scale: float, out,
+                               lse=None, ws=None, stream=None) -> None:
+    """idx: int32 CUDA tensor [S][max_idx] of listed rows; nidx: host counts [S]; q: bf16 [S][H][576] (or
+    [S][1][H][576]); out: bf16 [S][H][512] (same leading shape as q); lse: fp32 [S][H] or None."""
+    S, H = int(q.shape[0]), int(q.shape[-2])
+    a, p = _i64(lens)
+    b, pn = _i32(nidx)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().tf_paged_mla_attend_sparse(pool.handle, cache, _ptr(pt), max_pages, p, _ptr(idx), int(idx.shape[1]),
+                                            pn, S, H, _ptr(q), float(scale), _ptr(out), _ptr(lse), _ptr(ws), ws_bytes,
+                                            _stream(stream)),
+           "tf_paged_mla_attend_sparse")
 
 
 def tf_state_copy_rows(pool: KVPool, cache: int, src_pages, dst_pages, at: int, stream=None) -> None:

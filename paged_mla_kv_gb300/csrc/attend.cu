@@ -103,14 +103,16 @@ static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 //    into splits whose bounds depend on that stream's length alone, one CTA a
 //    (split, group) item, and the partials are merged in split order, so a stream's
 //    bits do not depend on the other streams of the batch.
-enum { MODE_RANGES = 0, MODE_UNITS = 1, MODE_SPLITS = 2 };
+//  - SPARSE (tf_paged_mla_attend_sparse).  RANGES over the tiles of each stream's list
+//    of rows; the key tiles are gathered row by row (TMA gather4) through the table.
+enum { MODE_RANGES = 0, MODE_UNITS = 1, MODE_SPLITS = 2, MODE_SPARSE = 3 };
 
 // One entry per stream, in the caller's order.
 struct StreamPlan {
     int64_t len;
     int64_t toff;     // RANGES: first numbered key tile of the stream
     int32_t nt;       // key tiles of the stream
-    int32_t split;    // SPLITS: keys a split (a multiple of SPLIT_UNIT)
+    int32_t split;    // SPLITS: keys a split (a multiple of SPLIT_UNIT); SPARSE: the stream's rows
     int32_t nsplit;   // SPLITS: splits of each column group
     int32_t item0;    // SPLITS: first item of the stream (items are numbered in launch order)
     int32_t slot0;    // SPLITS: first workspace slot of the stream
@@ -121,6 +123,10 @@ struct Params {
     CUtensorMap tm_lat;   // 4D {512, 512 rows, pages, caches}, box {64, 64, 1, 1}
     CUtensorMap tm_rope;  // 4D {64, 512 rows, pages, caches}, box {64, 64, 1, 1}
     CUtensorMap tm_q;     // 2D {576, S*R*H}, box {64, 64}
+    CUtensorMap tm_lat_rows;    // SPARSE: 2D {512, pool rows}, 1,024-byte rows (576 a page), box {64, 1}
+    CUtensorMap tm_rope_rows;   // SPARSE: 2D {64, pool rows}, 128-byte rows (4,608 a page), box {64, 1}
+    const int32_t *idx;         // SPARSE: [S][max_idx] row numbers of each stream's listed keys
+    int32_t max_idx;
     const int32_t *pt;
     __nv_bfloat16 *out;
     float *lse;
@@ -189,7 +195,7 @@ struct SegIter {
     int64_t x, x0, x1;
     int k;
     __device__ __forceinline__ explicit SegIter(const Params &p) : x(0), x0(0), x1(0), k(0) {
-        if (MODE == MODE_RANGES) {
+        if (MODE == MODE_RANGES || MODE == MODE_SPARSE) {
             const int range = (int)blockIdx.x / p.rep;
             x0 = p.rb[range];
             x1 = p.rb[range + 1];
@@ -197,7 +203,7 @@ struct SegIter {
         }
     }
     __device__ __forceinline__ bool next(const Params &p, Seg &q) {
-        if (MODE == MODE_RANGES) {
+        if (MODE == MODE_RANGES || MODE == MODE_SPARSE) {
             if (x >= x1) return false;
             q = seg_at(p, x, x0, x1);
             x += q.nt;
@@ -319,7 +325,122 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
 
     if (warp == 8) {
         // ================= TMA producer =================
-        if (lane == 0) {
+        if constexpr (MODE == MODE_SPARSE) {
+            // Gathered key tiles: list position k0 + 2l and + 1 belong to lane l; rows 4j..4j+3
+            // of every box are one gather4 by lane j (< 16), from the table's page of each row.
+            if (lane == 0) {
+                ptx::prefetch_tmap(&p.tm_lat_rows);
+                ptx::prefetch_tmap(&p.tm_rope_rows);
+                ptx::prefetch_tmap(&p.tm_q);
+            }
+            const uint64_t pol_kv = ptx::policy_evict_first();
+            const uint64_t pol_q = ptx::policy_evict_last();
+            int armed[NSTAGE][2];
+            for (int i = 0; i < NSTAGE; ++i) armed[i][0] = armed[i][1] = -1;
+            int q_armed = -1;
+            bool stop = false;
+            int gt = 0, si = 0;
+            SegIter<MODE> it(p);
+            Seg q;
+            for (; !stop && it.next(p, q); ++si) {
+                int okq = 1;
+                if (lane == 0) {
+                    if (si > 0 && !ptx::mbar_wait(&c.q_free, (si - 1) & 1, abort, errp, 15)) {
+                        okq = 0;
+                    } else {
+                        ptx::mbar_arrive_expect_tx(&c.q_full, Q_BYTES);
+                        const int qrow = q.s * R_ * H_ + q.g * NCOL;
+                        for (int b = 0; b < NBOX; ++b)
+                            ptx::tma_load_2d(smem + SMEM_Q + b * QBOX_BYTES, &p.tm_q, &c.q_full, b * 64, qrow, pol_q);
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, okq, 0)) break;
+                q_armed = si;
+                const int32_t *list = p.idx + (size_t)q.s * p.max_idx;
+                const int rows = p.st[q.s].split;
+                for (int tl = 0; tl < q.nt; ++tl, ++gt) {
+                    const int st = gt % NSTAGE;
+                    const uint32_t ph = ((gt / NSTAGE) - 1) & 1;
+                    const int64_t k0 = q.kb + (int64_t)tl * BK;
+                    int ylat[2], yrope[2], badv = 0;
+                    bool bad = false;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        // past the list's end a listed row is loaded again; the softmax masks it
+                        const int64_t pos = k0 + 2 * lane + h;
+                        const int r = __ldg(list + (pos < q.len ? pos : 0));
+                        int pg = 0;
+                        if (r < 0 || r >= rows) {
+                            bad = true;
+                            badv = r;
+                        } else {
+                            const int lp = r >> 9;
+                            pg = windowed ? q.s * max_pages + lp : __ldg(pt + (int64_t)q.s * max_pages + lp);
+                            if (pg < 0 || pg >= num_pages) {
+                                bad = true;
+                                badv = pg;
+                                pg = 0;
+                            }
+                        }
+                        const int base = cache * num_pages + pg;
+                        ylat[h] = base * (int)(kPageBytes / (kLat * 2)) + (r & 511);
+                        yrope[h] = base * (int)(kPageBytes / (kRope * 2)) + (r & 511);
+                    }
+                    const unsigned badm = __ballot_sync(0xffffffffu, bad);
+                    if (badm) {
+                        const int v = __shfl_sync(0xffffffffu, badv, __ffs(badm) - 1);
+                        if (lane == 0) {
+                            ptx::record_error(errp, TF_E_DEVICE, v);
+                            *abort = 1;
+                        }
+                        stop = true;
+                        break;
+                    }
+                    const int jl = lane & 15;
+                    const int la0 = __shfl_sync(0xffffffffu, ylat[0], 2 * jl), la1 = __shfl_sync(0xffffffffu, ylat[1], 2 * jl);
+                    const int la2 = __shfl_sync(0xffffffffu, ylat[0], 2 * jl + 1),
+                              la3 = __shfl_sync(0xffffffffu, ylat[1], 2 * jl + 1);
+                    const int ro0 = __shfl_sync(0xffffffffu, yrope[0], 2 * jl), ro1 = __shfl_sync(0xffffffffu, yrope[1], 2 * jl);
+                    const int ro2 = __shfl_sync(0xffffffffu, yrope[0], 2 * jl + 1),
+                              ro3 = __shfl_sync(0xffffffffu, yrope[1], 2 * jl + 1);
+                    uint8_t *dst = smem + SMEM_KV + st * STAGE_BYTES;
+                    for (int bi = 0; bi < NBOX; ++bi) {
+                        const int b = kBoxOrder[bi];
+                        const int part = bi < kPart0Boxes ? 0 : 1;
+                        int okw = 1;
+                        if (lane == 0) {
+                            if (gt >= NSTAGE) {
+                                uint64_t *e = (b == 8) ? &c.rope_empty[st] : &c.lat_empty[st][b >> 1];
+                                if (!ptx::mbar_wait(e, ph, abort, errp, 1)) okw = 0;
+                            }
+                            if (okw) ptx::mbar_arrive_expect_tx(&c.part_full[st][part], BOX_BYTES);
+                        }
+                        if (!__shfl_sync(0xffffffffu, okw, 0)) {
+                            stop = true;
+                            break;
+                        }
+                        if (lane < 16) {
+                            if (b == 8)
+                                ptx::tma_gather4(dst + 8 * BOX_BYTES + lane * 512, &p.tm_rope_rows, &c.part_full[st][part],
+                                                 0, ro0, ro1, ro2, ro3, pol_kv);
+                            else
+                                ptx::tma_gather4(dst + b * BOX_BYTES + lane * 512, &p.tm_lat_rows, &c.part_full[st][part],
+                                                 b * 64, la0, la1, la2, la3, pol_kv);
+                        }
+                        armed[st][part] = gt;
+                    }
+                    if (stop) break;
+                }
+            }
+            // no copy may still be writing shared memory when the CTA exits
+            if (lane == 0) {
+                if (q_armed >= 0) ptx::mbar_wait(&c.q_full, q_armed & 1, abort, errp, 10, 1ll << 28);
+                for (int i = 0; i < NSTAGE; ++i)
+                    for (int h = 0; h < 2; ++h)
+                        if (armed[i][h] >= 0)
+                            ptx::mbar_wait(&c.part_full[i][h], (armed[i][h] / NSTAGE) & 1, abort, errp, 11, 1ll << 28);
+            }
+        } else if (lane == 0) {
             ptx::prefetch_tmap(&p.tm_lat);
             ptx::prefetch_tmap(&p.tm_rope);
             ptx::prefetch_tmap(&p.tm_q);
@@ -734,7 +855,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) mla_combine_kernel(const __gr
     const StreamPlan &sp = p.st[s];
     const int g = gc / NCOL, col = gc - g * NCOL;
     int c0, c1, first_slot;
-    if (p.mode == MODE_RANGES) {
+    if (p.mode == MODE_RANGES || p.mode == MODE_SPARSE) {
         // the ranges that hold the unit; their CTAs' partial slots
         const int64_t ub = sp.toff, ue = ub + sp.nt;
         c0 = range_of(p, ub);
@@ -747,7 +868,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) mla_combine_kernel(const __gr
         first_slot = sp.slot0 + g * sp.nsplit;
     }
     if (c0 == c1) return;
-    const bool ranges = p.mode == MODE_RANGES;
+    const bool ranges = p.mode == MODE_RANGES || p.mode == MODE_SPARSE;
     const int n = c1 - c0 + 1;
     auto slot_of = [&](int j) { return j == 0 ? first_slot : ranges ? 2 * ((c0 + j) * p.rep + g) : first_slot + j; };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -982,8 +1103,8 @@ static bool encode(CUtensorMap *tm, void *base, int rank, const cuuint64_t *dims
 static int ensure_pool_maps(tf_kvpool *pool) {
     std::lock_guard<std::mutex> g(pool->mu);
     if (pool->tmaps_ready) return TF_OK;
-    pool->tm_lat.resize(1);
-    pool->tm_rope.resize(1);
+    pool->tm_lat.resize(2);
+    pool->tm_rope.resize(2);
     const cuuint64_t P = (cuuint64_t)pool->desc.num_pages, C = (cuuint64_t)pool->desc.num_caches;
     {
         cuuint64_t dims[4] = {(cuuint64_t)kLat, (cuuint64_t)kPageRows, P, C};
@@ -997,13 +1118,28 @@ static int ensure_pool_maps(tf_kvpool *pool) {
         cuuint32_t box[4] = {64, (cuuint32_t)attn::BK, 1, 1};
         if (!encode(&pool->tm_rope[0], pool->base + kLatBlockBytes, 4, dims, strides, box)) return TF_E_CUDA;
     }
+    // row views for gathers: latent rows 1,024 B apart (576 a page, the last 64 of them the
+    // rope block, never addressed), rope rows 128 B apart (4,608 a page); one-row boxes
+    const cuuint64_t pages = P * C;
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)kLat, (pages - 1) * (kPageBytes / (kLat * 2)) + kPageRows};
+        cuuint64_t strides[1] = {(cuuint64_t)kLat * 2};
+        cuuint32_t box[2] = {64, 1};
+        if (!encode(&pool->tm_lat[1], pool->base, 2, dims, strides, box)) return TF_E_CUDA;
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)kRope, (pages - 1) * (kPageBytes / (kRope * 2)) + kPageRows};
+        cuuint64_t strides[1] = {(cuuint64_t)kRope * 2};
+        cuuint32_t box[2] = {64, 1};
+        if (!encode(&pool->tm_rope[1], pool->base + kLatBlockBytes, 2, dims, strides, box)) return TF_E_CUDA;
+    }
     pool->tmaps_ready = true;
     return TF_OK;
 }
 
 int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages, const int64_t *h_len, int S, int R,
                   int H, const void *d_q, float scale, void *d_out, float *d_lse, void *d_ws, size_t ws_bytes,
-                  cudaStream_t st) {
+                  cudaStream_t st, const int32_t *d_idx, int max_idx, const int32_t *h_nidx) {
     using namespace attn;
     if (prepare_launch(pool, st) != TF_OK) return TF_E_CUDA;
     static bool attr_set = false;
@@ -1013,6 +1149,8 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
             cudaFuncSetAttribute(mla_attend_kernel<MODE_UNITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_TOTAL) != cudaSuccess ||
             cudaFuncSetAttribute(mla_attend_kernel<MODE_SPLITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_TOTAL) != cudaSuccess ||
+            cudaFuncSetAttribute(mla_attend_kernel<MODE_SPARSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_TOTAL) != cudaSuccess)
             return TF_E_CUDA;
         attr_set = true;
@@ -1026,6 +1164,10 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     Params &p = *pp;
     p.tm_lat = pool->tm_lat[0];
     p.tm_rope = pool->tm_rope[0];
+    p.tm_lat_rows = pool->tm_lat[1];
+    p.tm_rope_rows = pool->tm_rope[1];
+    p.idx = d_idx;
+    p.max_idx = max_idx;
     {
         cuuint64_t dims[2] = {(cuuint64_t)kDk, (cuuint64_t)S * R * H};
         cuuint64_t strides[1] = {(cuuint64_t)kDk * 2};
@@ -1046,8 +1188,17 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     p.ncols = R * H;
     p.groups = (R * H + NCOL - 1) / NCOL;
     p.windowed = d_pt ? 0 : 1;
-    const bool invariant = (pool->desc.flags & TF_POOL_BATCH_INVARIANT) != 0;
-    const Plan pl = plan_of(S, R, H, h_len, device_sms(), invariant, p.rb);
+    const bool sparse = d_idx != nullptr;
+    // the keys of a sparse call are the listed rows: plan over the list lengths
+    int64_t nkeys[TF_MAX_STREAMS];
+    const int64_t *keys = h_len;
+    if (sparse) {
+        for (int s = 0; s < S; ++s) nkeys[s] = h_nidx[s];
+        keys = nkeys;
+    }
+    const bool invariant = !sparse && (pool->desc.flags & TF_POOL_BATCH_INVARIANT) != 0;
+    Plan pl = plan_of(S, R, H, keys, device_sms(), invariant, p.rb);
+    if (sparse) pl.mode = MODE_SPARSE;   // ranges over the lists (few column groups: R = 1, H <= 128)
     p.mode = pl.mode;
     p.total = pl.total;
     p.nranges = pl.nranges;
@@ -1055,12 +1206,12 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     int64_t off = 0;
     for (int s = 0; s < S; ++s) {
         StreamPlan &sp = p.st[s];
-        sp.len = h_len[s];
+        sp.len = keys[s];
         sp.toff = off;
-        sp.nt = (int32_t)((h_len[s] + BK - 1) / BK);
+        sp.nt = (int32_t)((keys[s] + BK - 1) / BK);
         off += sp.nt;
-        const Split spl = split_of(h_len[s], p.groups);
-        sp.split = (int32_t)spl.split;
+        const Split spl = split_of(keys[s], p.groups);
+        sp.split = sparse ? (int32_t)h_len[s] : (int32_t)spl.split;
         sp.nsplit = spl.nsplit;
         sp.item0 = sp.slot0 = sp.pad = 0;
     }
@@ -1087,9 +1238,10 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     (void)ws_bytes;
     {
         ProfScope prof(pool, kProfAttend, st);
-        auto *kern = pl.mode == MODE_RANGES  ? mla_attend_kernel<MODE_RANGES>
-                     : pl.mode == MODE_UNITS ? mla_attend_kernel<MODE_UNITS>
-                                             : mla_attend_kernel<MODE_SPLITS>;
+        auto *kern = pl.mode == MODE_RANGES   ? mla_attend_kernel<MODE_RANGES>
+                     : pl.mode == MODE_UNITS  ? mla_attend_kernel<MODE_UNITS>
+                     : pl.mode == MODE_SPARSE ? mla_attend_kernel<MODE_SPARSE>
+                                              : mla_attend_kernel<MODE_SPLITS>;
         const cudaError_t e = launch_pdl(kern, dim3(pl.nctas), dim3(THREADS), SMEM_TOTAL, st, p);
         launch_counter()++;
         if (e != cudaSuccess) return TF_E_CUDA;

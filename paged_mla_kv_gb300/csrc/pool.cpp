@@ -241,6 +241,47 @@ extern "C" int tf_paged_mla_attend(tf_kvpool *p, int32_t cache, const int32_t *d
 }
 
 // ---- kept-state copy ----
+// ---- attention over listed rows ----
+static int sparse_checks(const tf_kvpool *p, int32_t S, int32_t H, int32_t max_idx, const int32_t *h_nidx) {
+    if (S < 1 || S > TF_MAX_STREAMS || H < 1 || H > TF_MAX_HEADS || max_idx < 1 || !h_nidx) return TF_E_ARG;
+    for (int s = 0; s < S; ++s)
+        if (h_nidx[s] < 1 || h_nidx[s] > max_idx) return TF_E_RANGE;
+    // the gather views number pool rows in int32 (4,608 rope rows a page)
+    if (p && (int64_t)p->desc.num_caches * p->desc.num_pages * (int64_t)(kPageBytes / (kRope * 2)) >= ((int64_t)1 << 31))
+        return TF_E_UNSUPPORTED;
+    return TF_OK;
+}
+
+extern "C" size_t tf_paged_mla_sparse_workspace_bytes(const tf_kvpool *p, int32_t S, int32_t H, const int32_t *h_nidx) {
+    if (sparse_checks(p, S, H, h_nidx ? 1 << 30 : 1, h_nidx) != TF_OK) return 0;
+    int64_t n[TF_MAX_STREAMS];
+    for (int s = 0; s < S; ++s) n[s] = h_nidx[s];
+    return attend_workspace_bytes(false, S, 1, H, n);
+}
+
+extern "C" int tf_paged_mla_attend_sparse(tf_kvpool *p, int32_t cache, const int32_t *d_pt, int32_t max_pages,
+                                          const int64_t *h_len, const int32_t *d_idx, int32_t max_idx,
+                                          const int32_t *h_nidx, int32_t S, int32_t H, const void *d_q, float scale,
+                                          void *d_out, float *d_lse, void *d_ws, size_t ws_bytes, void *stream) {
+    if (!p || !h_len || !d_idx || !d_q || !d_out || max_pages < 1) return TF_E_ARG;
+    const int rc = sparse_checks(p, S, H, max_idx, h_nidx);
+    if (rc != TF_OK) return rc;
+    if (!(scale > 0.0f) || scale == 1.0f / 0.0f) return TF_E_ARG;
+    if (cache < 0 || cache >= p->desc.num_caches) return TF_E_RANGE;
+    if (!d_pt && (int64_t)S * max_pages > p->desc.num_pages) return TF_E_RANGE;
+    for (int s = 0; s < S; ++s)
+        if (h_len[s] < 1 || h_len[s] > (int64_t)max_pages * kPageRows) return TF_E_RANGE;
+    if ((reinterpret_cast<uintptr_t>(d_q) & 15u) != 0 || (reinterpret_cast<uintptr_t>(d_out) & 15u) != 0)
+        return TF_E_ARG;
+    int64_t n[TF_MAX_STREAMS];
+    for (int s = 0; s < S; ++s) n[s] = h_nidx[s];
+    const size_t need = attend_workspace_bytes(false, S, 1, H, n);
+    if (need > 0 && (!d_ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(d_ws) & 255u) != 0))
+        return d_ws && ws_bytes < need ? TF_E_NOMEM : TF_E_ARG;
+    return launch_attend(p, cache, d_pt, max_pages, h_len, S, 1, H, d_q, scale, d_out, d_lse, d_ws, ws_bytes,
+                         (cudaStream_t)stream, d_idx, max_idx, h_nidx);
+}
+
 extern "C" int tf_state_copy_rows(tf_kvpool *p, int32_t cache, const int32_t *d_src, const int32_t *d_dst,
                                   int64_t at, void *stream) {
     if (!p || at < 0) return TF_E_ARG;

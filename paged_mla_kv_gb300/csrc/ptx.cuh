@@ -219,6 +219,18 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *tm, ui
 }
 
 // Prefetch `bytes` (a multiple of 16) of contiguous global memory into L2.
+// Four rows of a 2D tensor (one-row box, 64 bf16 wide with 128-byte swizzle) into four
+// consecutive 128-byte rows of shared memory: coordinates {x, row0, row1, row2, row3}.
+__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *tm, uint64_t *bar, int x, int y0, int y1,
+                                            int y2, int y3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+        "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }

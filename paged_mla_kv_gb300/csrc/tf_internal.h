@@ -105,8 +105,10 @@ int launch_state_copy(tf_kvpool *pool, int cache, const int32_t *d_src, const in
 int launch_poison(tf_kvpool *pool, const int32_t *h_ids, int n, cudaStream_t st);
 int launch_diag_wait(tf_kvpool *pool, long long limit, cudaStream_t st);
 size_t attend_workspace_bytes(bool invariant, int S, int R, int H, const int64_t *h_len);
+// d_idx / max_idx / h_nidx: a sparse call (the keys are the listed rows, R = 1), or null.
 int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages, const int64_t *h_len, int S,
                   int R, int H, const void *d_q, float scale, void *d_out, float *d_lse, void *d_ws,
-                  size_t ws_bytes, cudaStream_t st);
+                  size_t ws_bytes, cudaStream_t st, const int32_t *d_idx = nullptr, int max_idx = 0,
+                  const int32_t *h_nidx = nullptr);
 
 }  // namespace tf

@@ -200,6 +200,32 @@ def custom(name: str, seed: int, lens, R: int, H: int, share=None, pool_pages: i
     return w
 
 
+def listed_rows(seed: int, lens, n: int, repeats: bool = False) -> list:
+    """Seeded lists of rows for attention over listed rows: for stream s, min(n, len_s)
+    distinct rows of [0, len_s) in a random order (or n rows drawn with repeats)."""
+    g = _rng(seed, 4099)
+    out = []
+    for L in np.asarray(lens, np.int64):
+        L = int(L)
+        if repeats:
+            out.append(g.integers(0, L, n).astype(np.int32))
+        else:
+            out.append(g.choice(L, min(n, L), replace=False).astype(np.int32))
+    return out
+
+
+def sparse_decode(seed: int = 6, S: int = 64, H: int = 64, lo: int = 4096, hi: int = 65536,
+                  n: int = 2048) -> Workload:
+    """64 streams, 64 heads, 1 row, lengths U[4,096, 65,536]; each attends 2,048 listed rows."""
+    g = _rng(seed, 17)
+    lens = _lens(g, S, lo, hi)
+    w = Workload("sparse_decode", seed, S=S, R=1, H=H, lens=lens, share=[(-1, 0)] * S, pool_pages=0)
+    w.pool_pages = w.pages_needed() + 2
+    w.extra = dict(w.extra or {}, nidx=n)
+    w.notes = "keys: 2,048 seeded distinct rows of each stream (listed_rows), in a random order"
+    return w
+
+
 def permutation(seed: int, n: int) -> np.ndarray:
     """A seeded permutation of n pool pages (int32)."""
     return _rng(seed, 31337).permutation(n).astype(np.int32)
@@ -212,4 +238,5 @@ WORKLOADS = {
     "prefill_100k": lambda seed=4: chunked_prefill(seed, 2048, 100000),
     "prefill_208k": lambda seed=4: chunked_prefill(seed, 1024, 208000),
     "full_model": full_model,
+    "sparse_decode": sparse_decode,
 }

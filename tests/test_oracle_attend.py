@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 from scipy.special import logsumexp, softmax
 
-from oracle.attend import attend_stream
+from oracle.attend import attend_sparse, attend_stream
 from paged_mla_kv_gb300 import synth as Y
 
 
@@ -162,3 +162,50 @@ def test_rejects_rows_without_keys():
     q, lat, rope = rand_case(10, 1, 2, 1)
     with pytest.raises(ValueError):
         attend_stream(q, lat, rope, 1.0)
+
+
+# ---------------------------------------------------------------- listed rows (sparse)
+
+
+def test_sparse_single_listed_row_is_that_row():
+    q, lat, rope = rand_case(11, 300, 1, 4)
+    out, lse = attend_sparse(q[0], lat, rope, [123], 0.3)
+    for h in range(4):
+        assert np.array_equal(out[h], wide(lat[123]))
+
+
+def test_sparse_zero_query_is_the_mean_of_the_listed_rows():
+    q, lat, rope = rand_case(12, 500, 1, 2)
+    q[:] = 0
+    idx = [7, 400, 3, 250, 7]                              # 7 is listed twice: counted twice
+    out, lse = attend_sparse(q[0], lat, rope, idx, 0.5)
+    want = np.mean([wide(lat[i]) for i in idx], axis=0)
+    assert np.allclose(out[0], want, rtol=0, atol=1e-13)
+    assert lse[0] == pytest.approx(math.log(len(idx)), abs=1e-12)
+
+
+def test_sparse_every_row_listed_twice_moves_only_lse_by_log2():
+    q, lat, rope = rand_case(13, 90, 1, 3)
+    idx = np.random.default_rng(1).choice(90, 40, replace=False)
+    o1, l1 = attend_sparse(q[0], lat, rope, idx, 0.2)
+    o2, l2 = attend_sparse(q[0], lat, rope, np.concatenate([idx, idx]), 0.2)
+    assert np.allclose(o1, o2, rtol=0, atol=1e-12)
+    assert np.allclose(l2 - l1, math.log(2.0), rtol=0, atol=1e-12)
+
+
+def test_sparse_list_order_does_not_matter_and_unlisted_rows_do_not_count():
+    q, lat, rope = rand_case(14, 200, 1, 3)
+    g = np.random.default_rng(2)
+    idx = g.choice(200, 64, replace=False)
+    o1, l1 = attend_sparse(q[0], lat, rope, idx, 0.25)
+    o2, l2 = attend_sparse(q[0], lat, rope, g.permutation(idx), 0.25)
+    assert np.allclose(o1, o2, rtol=0, atol=1e-12) and np.allclose(l1, l2, rtol=0, atol=1e-12)
+    # poisoning a row that is not listed changes nothing
+    lat2 = lat.copy()
+    lat2[np.setdiff1d(np.arange(200), idx)[0]] = 0x7FC0
+    o3, l3 = attend_sparse(q[0], lat2, rope, idx, 0.25)
+    assert np.array_equal(o1, o3) and np.array_equal(l1, l3)
+    # and against scipy on the listed scores
+    s = np.array([0.25 * (wide(q[0, 1, :512]) @ wide(lat[i]) + wide(q[0, 1, 512:]) @ wide(rope[i])) for i in idx])
+    assert l1[1] == pytest.approx(float(logsumexp(s)), abs=1e-12)
+    assert np.allclose(o1[1], softmax(s) @ np.array([wide(lat[i]) for i in idx]), rtol=0, atol=1e-12)
