@@ -29,7 +29,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOADS = ["decode_batch", "tiny_decode", "long_window", "prefill_100k", "prefill_208k", "full_model",
-             "sparse_decode"]
+             "sparse_decode", "topk_prefill"]
+TOPK = {"topk_prefill"}
 METRIC = "paged MLA decode KV GB/s + tokens/s vs HBM roofline; prefill TFLOP/s"
 L2_BYTES = 129 * 1024 * 1024
 
@@ -242,9 +243,54 @@ class OracleSample:
                     sample=f"first {self.k} of {w.H} heads of all {w.S} streams, {what}, cache 0 ({t:.1f} s)")
 
 
+class TopkOracleSample:
+    """The top-k oracle, as it stands, on a bounded sample of rows spread over the chunk; the rate
+    is in GB/s of logits scanned (4 bytes a key in play)."""
+
+    def __init__(self, w, seconds: float):
+        from oracle import topk as OT
+        from paged_mla_kv_gb300 import synth as Y
+        self.OT, self.Y, self.w = OT, Y, w
+        t0, _ = self.run(2)
+        self.n = int(max(1, min(w.rows, 2 * seconds / max(t0, 1e-3))))
+
+    def rows(self, n):
+        return np.unique(np.linspace(0, self.w.rows - 1, n).round().astype(int))
+
+    def run(self, n):
+        w = self.w
+        rows = self.rows(n)
+        x = self.Y.topk_logits(w.seed, rows, w.n)
+        t0 = time.perf_counter()
+        self.OT.topk_rows(x, w.k, w.lens[rows])
+        return time.perf_counter() - t0, 4.0 * float(np.sum(w.lens[rows]))
+
+    def measure(self):
+        t, work = self.run(self.n)
+        return dict(value=work / t / 1e9, unit="GB/s", cores=1, kind="oracle",
+                    sample=f"{len(self.rows(self.n))} of {self.w.rows} rows spread over the chunk ({t:.1f} s, "
+                           f"one numpy sort a row)")
+
+
 def reference_arm(args, rank, world):
     """The oracle timed as the reference arm (host cores, the same bounded sample each step)."""
     if rank != 0:
+        return
+    if args.workload in TOPK:
+        from paged_mla_kv_gb300 import synth as Y
+        w = Y.TOPK_WORKLOADS[args.workload]()
+        o = TopkOracleSample(w, min(20.0, max(1.0, 150.0 / max(1, args.steps + args.warmup))))
+        for _ in range(args.warmup):
+            o.run(o.n)
+        vals = [o.measure() for _ in range(args.steps)]
+        v = statistics.median(x["value"] for x in vals)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": w.name, "rows": w.rows, "n": w.n, "k": w.k},
+                "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": vals[0]["sample"], "value": v},
+                "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
         return
     w = make_workload(args.workload)
     per_step = min(20.0, max(1.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -260,6 +306,89 @@ def reference_arm(args, rank, world):
             "cpu_baseline": {"kind": "oracle", "cores": vals[0]["cores"], "sample": vals[0]["sample"], "value": v},
             "e2e": {"value": v, "unit": vals[0]["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def topk_main(args, rank, world, pg, peaks, peak_src):
+    """Blocked top-k over a prefill chunk's indexer logits: one step = one tf_topk_blocked call
+    (a first-level launch and a merge launch) over the resident 2,048 x 100,000 fp32 matrix."""
+    import torch
+    from paged_mla_kv_gb300 import binding as B
+    from paged_mla_kv_gb300 import synth as Y
+    w = Y.TOPK_WORKLOADS[args.workload]()
+    x = torch.from_numpy(Y.topk_logits(w.seed, range(w.rows), w.n)).cuda()
+    lens = torch.from_numpy(w.lens).cuda()
+    ws = torch.empty(max(B.tf_topk_workspace_bytes(w.rows, w.n, w.k), 16), dtype=torch.uint8, device="cuda")
+    idx = torch.empty((w.rows, w.k), dtype=torch.int32, device="cuda")
+    val = torch.empty((w.rows, w.k), dtype=torch.float32, device="cuda")
+    read = 4 * int(np.sum(w.lens))
+    algo = read + 8 * w.rows * w.k            # logits in play read once, columns and values written
+
+    def step(src=x, oi=idx, ov=val):
+        B.tf_topk_blocked(src, w.k, oi, ov, lens=lens, ws=ws)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if pg is not None:
+            pg.barrier()
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    n0 = B.tf_launch_count()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    barrier()
+    launches = B.tf_launch_count() - n0
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, pg, "cuda")
+    clocks = sampler.stop() if sampler else None
+    value = whole_job_rate(algo, world, ms) / 1e9
+    peak = peaks.get("hbm_gbs", 6800.0)
+    achieved = algo / (ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": None, "peak_kind": f"{peak_src} HBM copy",
+            "kernel": "topk_level_kernel (both levels of one call)", "avg_launch_ms": ms}
+
+    e2e = None
+    if not args.no_e2e:
+        hx = x.cpu().pin_memory()
+        hi = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
+        hv = torch.empty(val.shape, dtype=val.dtype).pin_memory()
+        dx = torch.empty_like(x)
+        for _ in range(max(2, args.warmup)):
+            dx.copy_(hx, non_blocking=True)
+            step(dx)
+            hi.copy_(idx, non_blocking=True)
+            hv.copy_(val, non_blocking=True)
+        barrier()
+        k_ = max(2, min(args.steps, 20))
+        e0.record()
+        for _ in range(k_):
+            dx.copy_(hx, non_blocking=True)
+            step(dx)
+            hi.copy_(idx, non_blocking=True)
+            hv.copy_(val, non_blocking=True)
+        e1.record()
+        barrier()
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / k_, pg, "cuda")
+        e2e = {"value": world * algo / 1e9 / (e_ms / 1e3), "unit": "GB/s", "h2d_bytes_per_step": x.numel() * 4,
+               "d2h_bytes_per_step": idx.numel() * 4 + val.numel() * 4, "ms_per_step": e_ms}
+    cpu = TopkOracleSample(w, args.cpu_seconds).measure() if rank == 0 and not args.no_cpu_baseline else None
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": w.name, "rows": w.rows, "n": w.n, "k": w.k, "lens_sum": int(np.sum(w.lens)),
+                           "l2": "inputs larger than L2", "parallelism": f"replicas x{world}"},
+                "gpu_launches": launches, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks}
+        print(json.dumps(line), flush=True)
 
 
 def main():
@@ -280,6 +409,11 @@ def main():
     from paged_mla_kv_gb300.harness import Resident
     BUILD.build()
     peaks, peak_src = load_peaks()
+    if args.workload in TOPK:
+        topk_main(args, rank, world, pg, peaks, peak_src)
+        if pg is not None:
+            pg.destroy_process_group()
+        return
     w = make_workload(args.workload)
     prefill = w.R > 2
     units = step_units(w)

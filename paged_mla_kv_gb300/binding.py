@@ -74,6 +74,8 @@ _SIGS = {
     "tf_last_error": (ctypes.c_int, [_P, ctypes.POINTER(_I64)]),
     "tf_diag_wait_timeout": (ctypes.c_int, [_P, _I64, _P]),
     "tf_launch_count": (_I64, []),
+    "tf_topk_workspace_bytes": (_SZ, [_I64, _I64, _I32]),
+    "tf_topk_blocked": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
     "tf_profile_enable": (ctypes.c_int, [_P, _I32]),
     "tf_profile_read": (ctypes.c_int, [_P, _I32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I64)]),
 }
@@ -288,6 +290,20 @@ def tf_state_copy_rows(pool: KVPool, cache: int, src_pages, dst_pages, at: int, 
 
 def tf_diag_wait_timeout(pool: KVPool, limit_cycles: int, stream=None) -> None:
     _check(lib().tf_diag_wait_timeout(pool.handle, int(limit_cycles), _stream(stream)), "tf_diag_wait_timeout")
+
+
+def tf_topk_workspace_bytes(rows: int, n: int, k: int) -> int:
+    return int(lib().tf_topk_workspace_bytes(int(rows), int(n), int(k)))
+
+
+def tf_topk_blocked(logits, k: int, idx, val, lens=None, n: int | None = None, ws=None, stream=None) -> None:
+    """logits: fp32 CUDA tensor [rows][ld] (row stride ld, a multiple of 4); n: columns in play
+    (default ld); lens: int32 CUDA tensor [rows] or None; idx: int32 [rows][k]; val: fp32 [rows][k]."""
+    rows, ld = int(logits.shape[0]), int(logits.stride(0)) if logits.dim() == 2 else 0
+    n = int(logits.shape[1]) if n is None else int(n)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().tf_topk_blocked(_ptr(logits), rows, n, ld, _ptr(lens), int(k), _ptr(idx), _ptr(val), _ptr(ws),
+                                 ws_bytes, _stream(stream)), "tf_topk_blocked")
 
 
 def tf_launch_count() -> int:

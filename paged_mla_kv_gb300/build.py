@@ -17,7 +17,7 @@ OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libtf_paged_mla.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["pool.cpp", "copy_kernels.cu", "attend.cu", "attend_noalloc.cu"]
+SOURCES = ["pool.cpp", "copy_kernels.cu", "attend.cu", "attend_noalloc.cu", "topk.cu"]
 HEADERS = ["tf_internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -33,7 +33,7 @@ def _stale() -> bool:
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, "tf_paged_mla.h"), __file__]
+    deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, h) for h in ("tf_paged_mla.h", "tf_topk.h")] + [__file__]
     return any(os.path.getmtime(d) > t for d in deps)
 
 

@@ -231,6 +231,41 @@ def permutation(seed: int, n: int) -> np.ndarray:
     return _rng(seed, 31337).permutation(n).astype(np.int32)
 
 
+@dataclass
+class TopkWorkload:
+    """Rows of indexer logits for the blocked top-k: row t has lens[t] keys in play."""
+    name: str
+    seed: int
+    rows: int
+    n: int
+    k: int
+    lens: np.ndarray
+    grid: float
+    notes: str = ""
+
+
+def topk_logits(seed: int, row_ids, n: int, grid: float = 1.0 / 64) -> np.ndarray:
+    """float32 [len(row_ids)][n]: standard normal scores rounded to multiples of `grid`, so equal
+    scores are common (the indexer's scores come out of low-precision products); row r depends
+    only on (seed, r)."""
+    out = np.empty((len(row_ids), n), dtype=np.float32)
+    for i, r in enumerate(row_ids):
+        x = _rng(seed, 7919, int(r)).standard_normal(n, dtype=np.float32)
+        out[i] = np.round(x / grid) * grid if grid else x
+    return out
+
+
+def topk_prefill(seed: int = 7, T: int = 2048, L: int = 100000, k: int = 512) -> TopkWorkload:
+    """A 2,048-row chunk over a 100,000-key prefix (the chunked-prefill note, section 1); row t
+    sees L - T + 1 + t keys (causal); the top-512 of each row (section 2.3)."""
+    lens = (L - T + 1 + np.arange(T)).astype(np.int32)
+    return TopkWorkload("topk_prefill", seed, T, L, k, lens, 1.0 / 64,
+                        "scores N(0,1) rounded to 1/64; causal row lengths")
+
+
+TOPK_WORKLOADS = {"topk_prefill": topk_prefill}
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "decode_batch": decode_batch,
