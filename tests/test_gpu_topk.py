@@ -4,7 +4,9 @@ Columns and values must match the oracle bit for bit: the order (IEEE total orde
 column) makes the top-k unique.  Shapes span one block, a ragged second block, one and several
 merge levels, k up to its maximum, ragged row lengths (empty, shorter than k, exactly k), a row
 stride wider than the row, and the values that stress the order: heavy ties, all-equal rows,
-NaN, signed zeros and infinities.
+NaN, signed zeros and infinities.  The integer rows put tens, hundreds or thousands of keys on
+the k-th value of a block, so ties are settled by counting, by a radix pass over columns, and
+by the path that re-reads the block when the keys near the k-th do not fit shared memory.
 """
 import numpy as np
 import pytest
@@ -32,6 +34,8 @@ def values(kind: str, rows: int, n: int, seed: int) -> np.ndarray:
         return Y.topk_logits(seed, range(rows), n)
     if kind == "few":
         return g.integers(0, 4, (rows, n)).astype(np.float32)
+    if kind.startswith("int"):   # int<m>: integers below m, ~16384/m equal keys a block per value
+        return g.integers(0, int(kind[3:]), (rows, n)).astype(np.float32)
     if kind == "const":
         return np.full((rows, n), 0.5, np.float32)
     if kind == "special":
@@ -77,6 +81,9 @@ CASES = [
     (2, 300000, 512, "grid"),
     (2, 600000, 2048, "grid"),
     (3, 40000, 512, "few"),
+    (3, 40000, 512, "int32"),
+    (3, 40000, 512, "int256"),
+    (2, 40000, 2048, "int1000"),
     (2, 40000, 300, "const"),
     (4, 40000, 64, "special"),
     (2, 70000, 2048, "special"),
