@@ -74,14 +74,19 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> floa
 # captures summarised in profiles/ (mla_attend_<workload>.md).  Keyed by the first 16 hex
 # digits of the SHA-256 of the attention kernel's source the capture was taken on: once
 # the kernel changes, the counters no longer describe it and "traffic" is reported null.
+# DRAM bytes (read + written) of one launch of the dominant kernel, from one ncu capture, keyed
+# by the SHA-256 prefix of the kernel's source: a changed kernel reports null until re-captured.
 NCU_TRAFFIC = {
-    "dcf182b05d132441": {"decode_batch": 373_832_192 + 3_505_664, "prefill_100k": 1_795_208_000 + 133_645_824},
+    "a960f847979c8a16": {"decode_batch": 374_185_728 + 3_581_184,
+                         "prefill_100k": 1_947_665_000},   # prefill: ncu's DRAM rate x duration
+    # top-k: both launches of one call (first level 811.1 + 8.6 MB, merge 58.8 + 0.2 MB)
+    "4e5c0b41cdefdfb7": {"topk_prefill": 811_079_680 + 8_606_208 + 58_786_560 + 240_640},
 }
 
 
-def ncu_traffic(workload: str):
+def ncu_traffic(workload: str, source: str = "attend.cu"):
     import hashlib
-    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "paged_mla_kv_gb300", "csrc", "attend.cu")
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "paged_mla_kv_gb300", "csrc", source)
     try:
         key = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     except OSError:
@@ -353,7 +358,7 @@ def topk_main(args, rank, world, pg, peaks, peak_src):
     peak = peaks.get("hbm_gbs", 6800.0)
     achieved = algo / (ms / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "traffic": None, "peak_kind": f"{peak_src} HBM copy",
+            "traffic": ncu_traffic(args.workload, "topk.cu"), "peak_kind": f"{peak_src} HBM copy",
             "kernel": "topk_level_kernel (both levels of one call)", "avg_launch_ms": ms}
 
     e2e = None
