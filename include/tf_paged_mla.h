@@ -63,12 +63,31 @@ extern "C" {
 #define TF_POOL_POISON 1u      /* fill pages with bf16 NaN (0x7FC0) when they are taken */
 #define TF_POOL_BATCH_INVARIANT 2u  /* attention on this pool: a stream's bits do not depend
                                        on the other streams of a batch (see tf_paged_mla_attend) */
+#define TF_POOL_FP8 4u              /* FP8 latent rows (see "FP8 pages" below) */
+
+/* ---- FP8 pages (issue #1313, step 1.3, item 3: FP8 rows on pages, each 512-row page keeping
+ * its rows' FP32 scales after its rows; windows keep the same blocks) ----
+ * With TF_POOL_FP8 a page of one cache is
+ *   latent codes  512 rows x 512 bytes, OCP FP8 E4M3 (bias 7, largest finite 448)   262,144 B
+ *   scales        512 fp32, one a row                                                  2,048 B
+ *   rope          512 rows x 64 bf16, as on BF16 pages                                65,536 B
+ * = 329,728 bytes (644 a row and cache instead of 1,152).  Row r's latent value i is
+ * code_r[i] * scale_r.  tf_paged_append takes the same bf16 rows as on a BF16 pool and
+ * quantizes each latent row: amax = max_i |x_i|, scale = amax / 448 (fp32 division), code_i =
+ * E4M3(x_i / scale) rounded to nearest even with saturation to +-448 (fp32 division); a row of
+ * zeros stores scale 0 and codes 0.  Inputs must be finite.  tf_paged_mla_attend computes the
+ * same attention over the dequantized rows (the per-stream rows are expanded to bf16 in the
+ * workspace, then attended; the workspace size includes them).  tf_state_copy_rows copies codes,
+ * scales and rope of rows [0, at).  Poison fills taken pages with 0xFF bytes (NaN in all three
+ * blocks).  tf_paged_mla_attend_sparse and tf_paged_mla_attend_static return TF_E_UNSUPPORTED
+ * on an FP8 pool. */
 
 typedef struct tf_kvpool tf_kvpool;
 
 /* A pool of num_pages pages for each of num_caches caches.  One page of one cache
  * is page_rows x latent_dim bf16 (the latent block) followed by page_rows x
- * rope_dim bf16 (the rope block): 589,824 bytes at 512/512/64.  Cache c's page p
+ * rope_dim bf16 (the rope block): 589,824 bytes at 512/512/64 (329,728 with
+ * TF_POOL_FP8, see "FP8 pages").  Cache c's page p
  * starts at dev_base + (c * num_pages + p) * page_bytes.  A page id names the same
  * page in every cache (a token's rows in all caches live under one id). */
 typedef struct {
@@ -77,7 +96,7 @@ typedef struct {
     int32_t page_rows;   /* must be 512 */
     int32_t latent_dim;  /* must be 512 */
     int32_t rope_dim;    /* must be 64 */
-    uint32_t flags;      /* TF_POOL_POISON | TF_POOL_BATCH_INVARIANT, or 0 */
+    uint32_t flags;      /* TF_POOL_POISON | TF_POOL_BATCH_INVARIANT | TF_POOL_FP8, or 0 */
     uint64_t seed;       /* 0: free pages are handed out in id order; else in a seeded permutation */
 } tf_kvpool_desc;
 

@@ -28,6 +28,8 @@ def _load():
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_double, ctypes.c_int32, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]
+        lib.oracle_mla_attend_f64.restype = ctypes.c_int
+        lib.oracle_mla_attend_f64.argtypes = lib.oracle_mla_attend.argtypes
         _lib = lib
     return _lib
 
@@ -40,12 +42,14 @@ def attend_stream(q: np.ndarray, lat: np.ndarray, rope: np.ndarray, scale: float
                   items=None, threads: int | None = None):
     """Attention of one stream.
 
-    q: bf16 bits [R][H][576]; lat: [len][512]; rope: [len][64] (contiguous rows).
+    q: bf16 bits [R][H][576]; lat: [len][512] bf16 bits, or float64 values (the dequantized
+    rows of FP8 pages, oracle.fp8); rope: [len][64] bf16 bits (contiguous rows).
     items: iterable of r*H + h (default: all).  Returns (out [n][512], lse [n]) in float64.
     """
     lib = _load()
     q = np.ascontiguousarray(q, np.uint16)
-    lat = np.ascontiguousarray(lat, np.uint16)
+    f64 = np.asarray(lat).dtype == np.float64   # dequantized FP8 rows: the latent as doubles
+    lat = np.ascontiguousarray(lat, np.float64 if f64 else np.uint16)
     rope = np.ascontiguousarray(rope, np.uint16)
     R, H, dk = q.shape
     assert dk == 576 and lat.shape[1] == 512 and rope.shape[1] == 64 and lat.shape[0] == rope.shape[0]
@@ -57,7 +61,8 @@ def attend_stream(q: np.ndarray, lat: np.ndarray, rope: np.ndarray, scale: float
     lse = np.zeros(len(items), np.float64)
     if len(items) == 0:
         return out, lse
-    rc = lib.oracle_mla_attend(n, R, H, q.ctypes.data, lat.ctypes.data, rope.ctypes.data,
+    fn = lib.oracle_mla_attend_f64 if f64 else lib.oracle_mla_attend
+    rc = fn(n, R, H, q.ctypes.data, lat.ctypes.data, rope.ctypes.data,
                                float(scale), len(items), items.ctypes.data,
                                out.ctypes.data, lse.ctypes.data,
                                threads if threads is not None else default_threads())
@@ -82,16 +87,21 @@ def attend_sparse(q: np.ndarray, lat: np.ndarray, rope: np.ndarray, idx, scale: 
     return attend_stream(np.asarray(q)[None], np.asarray(lat)[idx], np.asarray(rope)[idx], scale, threads=threads)
 
 
-def attend_workload(w, cache: int = 0, items_per_stream=None, threads: int | None = None):
+def attend_workload(w, cache: int = 0, items_per_stream=None, threads: int | None = None, fp8: bool = False):
     """Oracle outputs for every stream of a synth.Workload.
 
-    items_per_stream: None (all r*H+h) or a list of per-stream item arrays.
+    items_per_stream: None (all r*H+h) or a list of per-stream item arrays.  fp8: attend over
+    the rows quantized as an FP8 pool stores them.
     Returns a list of (items, out, lse) per stream.
     """
     qall = w.q(cache)
     res = []
     for s in range(w.S):
         lat, rope = w.stream_rows(cache, s)
+        if fp8:   # the rows as an FP8 pool holds them (issue #1313, step 1.3, item 3)
+            from . import fp8 as F
+            x = (np.ascontiguousarray(lat, np.uint16).astype(np.uint32) << 16).view(np.float32)
+            lat = F.dequantize_rows(*F.quantize_rows(x))
         items = None if items_per_stream is None else items_per_stream[s]
         if items is None:
             items = np.arange(w.R * w.H, dtype=np.int32)

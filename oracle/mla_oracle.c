@@ -48,10 +48,37 @@ static double widen(uint16_t b)
  * out: [n_items][512] doubles; lse: [n_items] doubles.
  * Returns 0, or -1 on a bad argument (a row with no visible key).
  */
+static int attend_core(int64_t len, int32_t R, int32_t H,
+                       const uint16_t *q, const uint16_t *lat, const double *latd, const uint16_t *rope,
+                       double scale, int32_t n_items, const int32_t *items,
+                       double *out, double *lse, int32_t n_threads);
+
 int oracle_mla_attend(int64_t len, int32_t R, int32_t H,
                       const uint16_t *q, const uint16_t *lat, const uint16_t *rope,
                       double scale, int32_t n_items, const int32_t *items,
                       double *out, double *lse, int32_t n_threads)
+{
+    return attend_core(len, R, H, q, lat, NULL, rope, scale, n_items, items, out, lse, n_threads);
+}
+
+/*
+ * The same definition with the latent given as doubles [len][512] (the dequantized
+ * values of FP8 rows: issue #1313, step 1.3, item 3); q and rope as above.
+ */
+int oracle_mla_attend_f64(int64_t len, int32_t R, int32_t H,
+                          const uint16_t *q, const double *latd, const uint16_t *rope,
+                          double scale, int32_t n_items, const int32_t *items,
+                          double *out, double *lse, int32_t n_threads)
+{
+    return attend_core(len, R, H, q, NULL, latd, rope, scale, n_items, items, out, lse, n_threads);
+}
+
+#define LAT_AT(j, d) (latd ? latd[(j) * LAT + (d)] : widen(lat[(j) * LAT + (d)]))
+
+static int attend_core(int64_t len, int32_t R, int32_t H,
+                       const uint16_t *q, const uint16_t *lat, const double *latd, const uint16_t *rope,
+                       double scale, int32_t n_items, const int32_t *items,
+                       double *out, double *lse, int32_t n_threads)
 {
     if (len < R || R < 1 || H < 1)
         return -1;
@@ -71,7 +98,7 @@ int oracle_mla_attend(int64_t len, int32_t R, int32_t H,
         for (int64_t j = 0; j < nk; ++j) {
             double dot = 0.0;
             for (int d = 0; d < LAT; ++d)
-                dot += qd[d] * widen(lat[j * LAT + d]);
+                dot += qd[d] * LAT_AT(j, d);
             for (int e = 0; e < ROPE; ++e)
                 dot += qd[LAT + e] * widen(rope[j * ROPE + e]);
             s[j] = scale * dot;
@@ -87,7 +114,7 @@ int oracle_mla_attend(int64_t len, int32_t R, int32_t H,
         for (int64_t j = 0; j < nk; ++j) {
             double w = s[j] / sum;
             for (int d = 0; d < LAT; ++d)
-                acc[d] += w * widen(lat[j * LAT + d]);
+                acc[d] += w * LAT_AT(j, d);
         }
         for (int d = 0; d < LAT; ++d)
             out[(int64_t)it * LAT + d] = acc[d];

@@ -20,6 +20,9 @@ TF_OK, TF_E_ARG, TF_E_RANGE, TF_E_NOMEM, TF_E_CUDA, TF_E_TIMEOUT, TF_E_UNSUPPORT
     0, -1, -2, -3, -4, -5, -6, -7
 TF_POOL_POISON = 1
 TF_POOL_BATCH_INVARIANT = 2
+TF_POOL_FP8 = 4
+PAGE_BYTES_BF16 = 589824
+PAGE_BYTES_FP8 = 329728    # 512 x 512 E4M3 codes, 512 fp32 scales, 512 x 64 bf16 rope
 ERR_NAMES = {0: "TF_OK", -1: "TF_E_ARG", -2: "TF_E_RANGE", -3: "TF_E_NOMEM", -4: "TF_E_CUDA",
              -5: "TF_E_TIMEOUT", -6: "TF_E_UNSUPPORTED", -7: "TF_E_DEVICE"}
 PROF_APPEND, PROF_ATTEND, PROF_COMBINE, PROF_COPY, PROF_POISON = range(5)
@@ -121,8 +124,9 @@ def _i64(a):
 
 
 def make_desc(num_caches: int, num_pages: int, poison: bool = False, seed: int = 0,
-              invariant: bool = False) -> tf_kvpool_desc:
-    flags = (TF_POOL_POISON if poison else 0) | (TF_POOL_BATCH_INVARIANT if invariant else 0)
+              invariant: bool = False, fp8: bool = False) -> tf_kvpool_desc:
+    flags = ((TF_POOL_POISON if poison else 0) | (TF_POOL_BATCH_INVARIANT if invariant else 0) |
+             (TF_POOL_FP8 if fp8 else 0))
     return tf_kvpool_desc(num_caches, num_pages, 512, 512, 64, flags, seed)
 
 
@@ -146,8 +150,10 @@ class KVPool:
     """A pool over caller device memory (a torch uint8 tensor kept alive here)."""
 
     def __init__(self, num_caches: int, num_pages: int, poison: bool = False, seed: int = 0, device=None,
-                 memory=None, invariant: bool = False):
-        self.desc = make_desc(num_caches, num_pages, poison, seed, invariant)
+                 memory=None, invariant: bool = False, fp8: bool = False):
+        self.desc = make_desc(num_caches, num_pages, poison, seed, invariant, fp8)
+        self.fp8 = fp8
+        self.page_bytes = PAGE_BYTES_FP8 if fp8 else PAGE_BYTES_BF16
         self.bytes = tf_kvpool_bytes(self.desc)
         if self.bytes == 0:
             raise TFError(TF_E_ARG, "tf_kvpool_bytes")
@@ -200,11 +206,14 @@ class KVPool:
         return int(lib().tf_kvpool_page_ptr(self.handle, cache, page) or 0)
 
     def view(self):
-        """The pool's device bytes as a uint16 tensor [caches][pages][294912]."""
+        """The pool's device bytes as a uint16 tensor [caches][pages][294912] (BF16 pages)."""
+        return self.bytes_view().view(__import__("torch").int16)
+
+    def bytes_view(self):
+        """The pool's device bytes as a uint8 tensor [caches][pages][page bytes]."""
         off = self.base - self.memory.data_ptr()
-        n = self.num_caches * self.num_pages * 589824
-        return self.memory[off:off + n].view(self.num_caches, self.num_pages, 589824).view(
-            __import__("torch").int16)
+        n = self.num_caches * self.num_pages * self.page_bytes
+        return self.memory[off:off + n].view(self.num_caches, self.num_pages, self.page_bytes)
 
     def last_error(self):
         d = ctypes.c_int64(0)

@@ -17,7 +17,7 @@ OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libtf_paged_mla.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["pool.cpp", "copy_kernels.cu", "attend.cu", "attend_noalloc.cu", "topk.cu"]
+SOURCES = ["pool.cpp", "copy_kernels.cu", "attend.cu", "attend_noalloc.cu", "topk.cu", "fp8.cu"]
 HEADERS = ["tf_internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -124,19 +124,22 @@ int launch_state_copy(tf_kvpool *pool, int cache, const int32_t *d_src, const in
 constexpr int kPoisonIds = 2048;
 struct PoisonParams {
     char *base;
+    size_t page_bytes;   // a multiple of 256
+    uint32_t pattern;    // the fill word: bf16 NaN pairs, or all ones on FP8 pages
     int32_t num_pages, num_caches, n;
     int32_t ids[kPoisonIds];
 };
 
-// grid (ids, caches, 16 slices of a page): fill with the bf16 NaN pattern 0x7FC0.
+// grid (ids, caches, 16 slices of a page): fill with the pattern (bf16 NaN 0x7FC0 pairs on BF16
+// pages; 0xFF bytes on FP8 pages, NaN as codes, scales and rope alike).
 __global__ void __launch_bounds__(256) poison_kernel(const __grid_constant__ PoisonParams p) {
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
     const int id = p.ids[blockIdx.x];
     const int cache = blockIdx.y;
-    uint4 *pg = reinterpret_cast<uint4 *>(p.base + ((size_t)cache * p.num_pages + id) * kPageBytes);
-    const int per_slice = (int)(kPageBytes / 16 / 16);
-    const uint4 nan4 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
+    uint4 *pg = reinterpret_cast<uint4 *>(p.base + ((size_t)cache * p.num_pages + id) * p.page_bytes);
+    const int per_slice = (int)(p.page_bytes / 16 / 16);
+    const uint4 nan4 = make_uint4(p.pattern, p.pattern, p.pattern, p.pattern);
     uint4 *q = pg + (size_t)blockIdx.z * per_slice;
     for (int k = threadIdx.x; k < per_slice; k += blockDim.x) q[k] = nan4;
 }
@@ -146,6 +149,8 @@ int launch_poison(tf_kvpool *pool, const int32_t *h_ids, int n, cudaStream_t st)
     for (int b = 0; b < n; b += kPoisonIds) {
         PoisonParams p;
         p.base = pool->base;
+        p.page_bytes = page_bytes(pool->desc);
+        p.pattern = is_fp8(pool->desc) ? 0xFFFFFFFFu : 0x7FC07FC0u;
         p.num_pages = pool->desc.num_pages;
         p.num_caches = pool->desc.num_caches;
         p.n = std::min(kPoisonIds, n - b);

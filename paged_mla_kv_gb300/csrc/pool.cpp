@@ -43,13 +43,13 @@ using namespace tf;
 
 static bool desc_ok(const tf_kvpool_desc *d) {
     return d && d->num_caches >= 1 && d->num_pages >= 1 && d->page_rows == kPageRows && d->latent_dim == kLat &&
-           d->rope_dim == kRope && (d->flags & ~(TF_POOL_POISON | TF_POOL_BATCH_INVARIANT)) == 0 &&
+           d->rope_dim == kRope && (d->flags & ~(TF_POOL_POISON | TF_POOL_BATCH_INVARIANT | TF_POOL_FP8)) == 0 &&
            (uint64_t)d->num_caches * (uint64_t)d->num_pages < (1ull << 31);
 }
 
 extern "C" size_t tf_kvpool_bytes(const tf_kvpool_desc *d) {
     if (!desc_ok(d)) return 0;
-    return (size_t)d->num_caches * (size_t)d->num_pages * kPageBytes + kCtrlBytes;
+    return (size_t)d->num_caches * (size_t)d->num_pages * page_bytes(*d) + kCtrlBytes;
 }
 
 // splitmix64: a published 64-bit mixer, used only to shuffle the free list.
@@ -158,7 +158,7 @@ extern "C" int32_t tf_kvpool_refcount(const tf_kvpool *p, int32_t id) {
 
 extern "C" void *tf_kvpool_page_ptr(const tf_kvpool *p, int32_t cache, int32_t page) {
     if (!p || cache < 0 || cache >= p->desc.num_caches || page < 0 || page >= p->desc.num_pages) return nullptr;
-    return p->base + ((size_t)cache * p->desc.num_pages + page) * kPageBytes;
+    return p->base + ((size_t)cache * p->desc.num_pages + page) * page_bytes(p->desc);
 }
 
 // ---- plan (issue #1313, "Why" bullet 3 and "Proposal" step 1.1) ----
@@ -205,6 +205,8 @@ extern "C" int tf_paged_append(tf_kvpool *p, int32_t cache, const int32_t *d_pt,
     for (int s = 0; s < S; ++s)
         if (h_pos[s] < 0 || h_pos[s] + n > (int64_t)max_pages * kPageRows) return TF_E_RANGE;
     if (n == 0) return TF_OK;
+    if (is_fp8(p->desc))
+        return launch_append_fp8(p, cache, d_pt, max_pages, h_pos, S, n, d_latent, d_rope, (cudaStream_t)stream);
     return launch_append(p, cache, d_pt, max_pages, h_pos, S, n, d_latent, d_rope, (cudaStream_t)stream);
 }
 
@@ -215,7 +217,9 @@ extern "C" size_t tf_paged_mla_workspace_bytes(const tf_kvpool *p, int32_t S, in
     for (int s = 0; s < S; ++s)
         if (h_len[s] < R) return 0;
     const bool invariant = p && (p->desc.flags & TF_POOL_BATCH_INVARIANT);
-    return attend_workspace_bytes(invariant, S, R, H, h_len);
+    const size_t part = attend_workspace_bytes(invariant, S, R, H, h_len);
+    if (p && is_fp8(p->desc)) return (part + 1023) / 1024 * 1024 + fp8_shadow_bytes(S, h_len);
+    return part;
 }
 
 extern "C" int tf_paged_mla_attend(tf_kvpool *p, int32_t cache, const int32_t *d_pt, int32_t max_pages,
@@ -233,9 +237,13 @@ extern "C" int tf_paged_mla_attend(tf_kvpool *p, int32_t cache, const int32_t *d
         if (h_len[s] < R || h_len[s] > (int64_t)max_pages * kPageRows) return TF_E_RANGE;
     if ((reinterpret_cast<uintptr_t>(d_q) & 15u) != 0 || (reinterpret_cast<uintptr_t>(d_out) & 15u) != 0)
         return TF_E_ARG;
-    size_t need = attend_workspace_bytes((p->desc.flags & TF_POOL_BATCH_INVARIANT) != 0, S, R, H, h_len);
+    const size_t part = attend_workspace_bytes((p->desc.flags & TF_POOL_BATCH_INVARIANT) != 0, S, R, H, h_len);
+    const size_t need = is_fp8(p->desc) ? (part + 1023) / 1024 * 1024 + fp8_shadow_bytes(S, h_len) : part;
     if (need > 0 && (!d_ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(d_ws) & 255u) != 0))
         return d_ws && ws_bytes < need ? TF_E_NOMEM : TF_E_ARG;
+    if (is_fp8(p->desc))
+        return launch_attend_fp8(p, cache, d_pt, max_pages, h_len, S, R, H, d_q, scale, d_out, d_lse, d_ws, ws_bytes,
+                                 part, (cudaStream_t)stream);
     return launch_attend(p, cache, d_pt, max_pages, h_len, S, R, H, d_q, scale, d_out, d_lse, d_ws, ws_bytes,
                          (cudaStream_t)stream);
 }
@@ -243,6 +251,7 @@ extern "C" int tf_paged_mla_attend(tf_kvpool *p, int32_t cache, const int32_t *d
 // ---- kept-state copy ----
 // ---- attention over listed rows ----
 static int sparse_checks(const tf_kvpool *p, int32_t S, int32_t H, int32_t max_idx, const int32_t *h_nidx) {
+    if (p && is_fp8(p->desc)) return TF_E_UNSUPPORTED;
     if (S < 1 || S > TF_MAX_STREAMS || H < 1 || H > TF_MAX_HEADS || max_idx < 1 || !h_nidx) return TF_E_ARG;
     for (int s = 0; s < S; ++s)
         if (h_nidx[s] < 1 || h_nidx[s] > max_idx) return TF_E_RANGE;
@@ -289,6 +298,7 @@ extern "C" int tf_state_copy_rows(tf_kvpool *p, int32_t cache, const int32_t *d_
     if (at > (int64_t)p->desc.num_pages * kPageRows) return TF_E_RANGE;
     if (at == 0) return TF_OK;
     if (!d_src || !d_dst) return TF_E_ARG;
+    if (is_fp8(p->desc)) return launch_state_copy_fp8(p, cache, d_src, d_dst, at, (cudaStream_t)stream);
     return launch_state_copy(p, cache, d_src, d_dst, at, (cudaStream_t)stream);
 }
 

@@ -22,6 +22,15 @@ constexpr size_t kLatBlockBytes = size_t(kPageRows) * kLat * 2;   // 524,288
 constexpr size_t kRopeBlockBytes = size_t(kPageRows) * kRope * 2; // 65,536
 constexpr size_t kPageBytes = kLatBlockBytes + kRopeBlockBytes;   // 589,824
 constexpr size_t kCtrlBytes = 256;
+// FP8 pages: E4M3 codes, then one fp32 scale a row, then the bf16 rope block.
+constexpr size_t kF8LatBlockBytes = size_t(kPageRows) * kLat;         // 262,144
+constexpr size_t kF8ScaleOff = kF8LatBlockBytes;
+constexpr size_t kF8RopeOff = kF8ScaleOff + size_t(kPageRows) * 4;     // 264,192
+constexpr size_t kF8PageBytes = kF8RopeOff + kRopeBlockBytes;          // 329,728
+static_assert(kF8PageBytes % 1024 == 0, "FP8 pages keep 1 KiB alignment");
+
+inline bool is_fp8(const tf_kvpool_desc &d) { return (d.flags & TF_POOL_FP8) != 0; }
+inline size_t page_bytes(const tf_kvpool_desc &d) { return is_fp8(d) ? kF8PageBytes : kPageBytes; }
 
 // Device error word, in the pool's control block after the last page.
 struct DevErr {
@@ -56,6 +65,9 @@ struct tf_kvpool {
     bool prof = false;
     std::vector<tf::ProfRec> recs;
     std::vector<cudaEvent_t> spare_events;
+    // FP8 pools: a BF16 view over the workspace that attention expands the rows into.
+    tf_kvpool *shadow = nullptr;
+    ~tf_kvpool() { delete shadow; }
 };
 
 namespace tf {
@@ -103,6 +115,15 @@ int launch_append(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
 int launch_state_copy(tf_kvpool *pool, int cache, const int32_t *d_src, const int32_t *d_dst, int64_t at,
                       cudaStream_t st);
 int launch_poison(tf_kvpool *pool, const int32_t *h_ids, int n, cudaStream_t st);
+// FP8 pages (fp8.cu).
+int launch_append_fp8(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages, const int64_t *h_pos,
+                      int S, int n, const void *d_lat, const void *d_rope, cudaStream_t st);
+int launch_state_copy_fp8(tf_kvpool *pool, int cache, const int32_t *d_src, const int32_t *d_dst, int64_t at,
+                          cudaStream_t st);
+size_t fp8_shadow_bytes(int S, const int64_t *h_len);
+int launch_attend_fp8(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages, const int64_t *h_len, int S,
+                      int R, int H, const void *d_q, float scale, void *d_out, float *d_lse, void *d_ws,
+                      size_t ws_bytes, size_t attend_ws, cudaStream_t st);
 int launch_diag_wait(tf_kvpool *pool, long long limit, cudaStream_t st);
 size_t attend_workspace_bytes(bool invariant, int S, int R, int H, const int64_t *h_len);
 // d_idx / max_idx / h_nidx: a sparse call (the keys are the listed rows, R = 1), or null.

@@ -22,14 +22,15 @@ def bf16_tensor(bits: np.ndarray, device="cuda") -> torch.Tensor:
 class Resident:
     def __init__(self, w: Y.Workload, poison: bool = True, pool_seed: int | None = None, windowed: bool = False,
                  caches=None, chunk_rows: int = 65536, device="cuda", extra_pages: int = 0,
-                 invariant: bool = False):
+                 invariant: bool = False, fp8: bool = False):
         self.w = w
         self.windowed = windowed
         self.device = device
         self.max_pages = w.max_pages
         npages = (w.S * self.max_pages if windowed else w.pool_pages) + extra_pages
         seed = (w.seed * 1000003 + 7) if pool_seed is None else pool_seed
-        self.pool = B.KVPool(w.num_caches, npages, poison=poison, seed=seed, device=device, invariant=invariant)
+        self.pool = B.KVPool(w.num_caches, npages, poison=poison, seed=seed, device=device, invariant=invariant,
+                             fp8=fp8)
         self.caches = list(range(w.num_caches)) if caches is None else list(caches)
         pt = np.full((w.S, self.max_pages), -1, np.int32)
         if windowed:

@@ -12,9 +12,9 @@ REL_L2 = 1e-2
 LSE_ABS = 2e-3
 
 
-def compare(w, out, lse, items_per_stream=None, cache=0, threads=None):
+def compare(w, out, lse, items_per_stream=None, cache=0, threads=None, fp8=False):
     """Compare device outputs [S][R][H][512] / [S][R][H] against the fp64 oracle."""
-    ref = OA.attend_workload(w, cache=cache, items_per_stream=items_per_stream, threads=threads)
+    ref = OA.attend_workload(w, cache=cache, items_per_stream=items_per_stream, threads=threads, fp8=fp8)
     o = out.float().cpu().numpy().reshape(w.S, w.R * w.H, 512)
     lz = lse.float().cpu().numpy().reshape(w.S, w.R * w.H)
     worst = dict(max_abs=0.0, rel_l2=0.0, lse=0.0)

@@ -214,3 +214,28 @@ def test_workspace_is_bounded_by_the_cta_ranges(L):
     slot = 64 * 512 * 4
     assert w1 <= 2 * 240 * slot + 2 * 240 * 64 * 2 * 4 + 255
     assert w1 <= 64 << 20                       # fits the static scratch of the allocation-free call
+
+
+def test_fp8_pool_sizes_and_workspace(L):
+    """FP8 pages: 329,728 bytes a page (codes, scales, rope); attention's workspace adds the rows
+    expanded to BF16 pages, a table and 1 KiB of alignment room; no device memory is touched."""
+    desc = B.make_desc(3, 10, fp8=True)
+    n = B.tf_kvpool_bytes(desc)
+    assert n == 3 * 10 * B.PAGE_BYTES_FP8 + 256
+    h = ctypes.c_void_p()
+    assert L.tf_kvpool_create(ctypes.byref(desc), ctypes.c_void_p(1 << 40), n, ctypes.byref(h)) == B.TF_OK
+    base = L.tf_kvpool_page_ptr(h, 0, 0)
+    assert L.tf_kvpool_page_ptr(h, 1, 2) - base == (10 + 2) * B.PAGE_BYTES_FP8
+    lens = np.array([1000, 513, 7], np.int64)
+    lp = lens.ctypes.data_as(ctypes.c_void_p)
+    plain = B.tf_paged_mla_workspace_bytes(None, 3, 1, 16, lens)
+    fp8 = L.tf_paged_mla_workspace_bytes(h, 3, 1, 16, lp)
+    pages = 2 + 2 + 1
+    assert fp8 == (plain + 1023) // 1024 * 1024 + 1024 + 1024 + pages * B.PAGE_BYTES_BF16
+    # listed-row attention is refused on FP8 pages before anything else
+    assert L.tf_paged_mla_sparse_workspace_bytes(h, 3, 16, np.array([4, 4, 4], np.int32).ctypes.data_as(
+        ctypes.c_void_p)) == 0
+    L.tf_kvpool_destroy(h)
+    bad = B.make_desc(1, 4)
+    bad.flags = 8
+    assert B.tf_kvpool_bytes(bad) == 0
