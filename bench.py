@@ -29,7 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOADS = ["decode_batch", "tiny_decode", "long_window", "prefill_100k", "prefill_208k", "full_model",
-             "sparse_decode", "topk_prefill"]
+             "sparse_decode", "fp8_decode", "topk_prefill"]
 TOPK = {"topk_prefill"}
 METRIC = "paged MLA decode KV GB/s + tokens/s vs HBM roofline; prefill TFLOP/s"
 L2_BYTES = 129 * 1024 * 1024
@@ -121,10 +121,12 @@ def step_units(w):
         flops = 2 * (Y.DK + 512) * H * sum(n)
         return dict(bytes=kv + q + out + app, attend_bytes=kv + q + out, flops=flops, attend_flops=flops,
                     tokens=S, kv=kv)
-    kv = int(np.sum(w.lens)) * Y.ROW_BYTES
+    # an FP8 row is 512 code bytes, a 4-byte scale and the 128-byte bf16 rope
+    row = 644 if w.extra.get("fp8") else Y.ROW_BYTES
+    kv = int(np.sum(w.lens)) * row
     q = S * R * H * Y.DK * 2
     out = S * R * H * (512 * 2 + 4)
-    app = 2 * S * R * Y.ROW_BYTES
+    app = S * R * (Y.ROW_BYTES + row)
     attend_bytes = kv + q + out
     at = int(w.extra.get("at", 0))
     copy = 2 * at * Y.ROW_BYTES * C
@@ -199,6 +201,12 @@ class OracleSample:
         self.prefill = w.R > 2
         self.q = w.q(0)
         self.rows = [w.stream_rows(0, s) for s in range(w.S)]
+        self.row_bytes = 1152
+        if w.extra.get("fp8"):   # the oracle attends over the rows as FP8 pages hold them
+            from oracle import fp8 as F
+            from paged_mla_kv_gb300 import synth as Y
+            self.rows = [(F.dequantize_rows(*F.quantize_rows(Y.bf16_bits_to_f32(a))), b) for a, b in self.rows]
+            self.row_bytes = 644
         self.lists = None
         if "nidx" in w.extra:
             from paged_mla_kv_gb300 import synth as Y
@@ -232,7 +240,7 @@ class OracleSample:
         else:
             for s in range(w.S):
                 self.OA.attend_stream(self.q[s], self.rows[s][0], self.rows[s][1], w.scale, items, self.threads)
-                work += int(w.lens[s]) * 1152 * k / w.H
+                work += int(w.lens[s]) * self.row_bytes * k / w.H
         return time.perf_counter() - t0, work
 
     def measure(self):
@@ -422,7 +430,7 @@ def main():
     w = make_workload(args.workload)
     prefill = w.R > 2
     units = step_units(w)
-    res = Resident(w, poison=True)
+    res = Resident(w, poison=True, fp8=bool(w.extra.get("fp8")))
     qs = [res.q(c) for c in range(w.num_caches)]
     cur = [res.current_rows(c) for c in range(w.num_caches)]
     out = torch.empty((w.S, w.R, w.H, 512), dtype=torch.bfloat16, device="cuda")
@@ -533,7 +541,8 @@ def main():
         peak = peaks.get("hbm_gbs", 6800.0)
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": ncu_traffic(args.workload), "peak_kind": f"{peak_src} HBM copy",
-                "kernel": "mla_attend_kernel",
+                "kernel": ("dequant_kernel + mla_attend_kernel (FP8 rows expanded, then attended)"
+                           if w.extra.get("fp8") else "mla_attend_kernel"),
                 "avg_launch_ms": avg_att}
 
     # end to end through the C-ABI with host buffers: queries and new rows in, outputs out

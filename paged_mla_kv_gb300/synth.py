@@ -226,6 +226,15 @@ def sparse_decode(seed: int = 6, S: int = 64, H: int = 64, lo: int = 4096, hi: i
     return w
 
 
+def fp8_decode(seed: int = 2) -> Workload:
+    """The decode batch (same lengths, sharing and rows) held on FP8 pages."""
+    w = decode_batch(seed)
+    w.name = "fp8_decode"
+    w.extra = dict(w.extra or {}, fp8=True)
+    w.notes = "decode_batch's rows, stored as E4M3 codes with one fp32 scale a row"
+    return w
+
+
 def permutation(seed: int, n: int) -> np.ndarray:
     """A seeded permutation of n pool pages (int32)."""
     return _rng(seed, 31337).permutation(n).astype(np.int32)
@@ -274,4 +283,5 @@ WORKLOADS = {
     "prefill_208k": lambda seed=4: chunked_prefill(seed, 1024, 208000),
     "full_model": full_model,
     "sparse_decode": sparse_decode,
+    "fp8_decode": fp8_decode,
 }
