@@ -116,7 +116,9 @@ struct DequantParams {
 
 // grid (maxp, S): logical page j of stream s, rows [0, min(512, len - 512 j)), expanded to a
 // BF16 page: latent value = bf16(code * scale), rope copied.
-__global__ void __launch_bounds__(256) dequant_kernel(const __grid_constant__ DequantParams p) {
+constexpr int kDequantThreads = 512;
+
+__global__ void __launch_bounds__(kDequantThreads) dequant_kernel(const __grid_constant__ DequantParams p) {
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
     const int j = blockIdx.x, s = blockIdx.y;
@@ -134,26 +136,39 @@ __global__ void __launch_bounds__(256) dequant_kernel(const __grid_constant__ De
     char *dst = p.shadow + (size_t)dpage * kPageBytes;
     const float *scales = reinterpret_cast<const float *>(src + kF8ScaleOff);
     const int nc = rows * (kLat / 16);  // 16 codes a unit
-    for (int k = threadIdx.x; k < nc; k += blockDim.x) {
-        const int r = k >> 5;
-        const uint4 c = __ldg(reinterpret_cast<const uint4 *>(src) + k);
-        const float sc = __ldg(scales + r);
-        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-        uint32_t o[8];
+    constexpr int U = 4;                // units a thread has in flight
+    for (int k0 = threadIdx.x; k0 < nc; k0 += U * kDequantThreads) {
+        uint4 c[U];
+        float sc[U];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const __half2_raw hr =
-                    __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((cw[q] >> (16 * h)) & 0xFFFFu), __NV_E4M3);
-                const float2 f = __half22float2(__half2(hr));
-                const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * sc, f.y * sc);
-                o[2 * q + h] = *reinterpret_cast<const uint32_t *>(&b);
+        for (int u = 0; u < U; ++u) {
+            const int k = k0 + u * kDequantThreads;
+            if (k < nc) {
+                c[u] = __ldg(reinterpret_cast<const uint4 *>(src) + k);
+                sc[u] = __ldg(scales + (k >> 5));
             }
         }
-        uint4 *d = reinterpret_cast<uint4 *>(dst) + 2 * k;
-        d[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int k = k0 + u * kDequantThreads;
+            if (k >= nc) break;
+            const uint32_t cw[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+                        (__nv_fp8x2_storage_t)((cw[q] >> (16 * h)) & 0xFFFFu), __NV_E4M3);
+                    const float2 f = __half22float2(__half2(hr));
+                    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * sc[u], f.y * sc[u]);
+                    o[2 * q + h] = *reinterpret_cast<const uint32_t *>(&b);
+                }
+            }
+            uint4 *d = reinterpret_cast<uint4 *>(dst) + 2 * k;
+            d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
     }
     const int nr = rows * (kRope * 2 / 16);
     for (int k = threadIdx.x; k < nr; k += blockDim.x)
@@ -269,7 +284,8 @@ int launch_attend_fp8(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_p
     }
     if (prepare_launch(pool, st) != TF_OK) return TF_E_CUDA;
     ProfScope prof(pool, kProfAttend, st);  // the expansion and the attention together
-    const cudaError_t e = launch_pdl(dequant_kernel, dim3((unsigned)sp.maxp, (unsigned)S), dim3(256), 0, st, p);
+    const cudaError_t e =
+        launch_pdl(dequant_kernel, dim3((unsigned)sp.maxp, (unsigned)S), dim3(kDequantThreads), 0, st, p);
     launch_counter()++;
     if (e != cudaSuccess) return TF_E_CUDA;
     return launch_attend(sh, 0, spt, sp.maxp, h_len, S, R, H, d_q, scale, d_out, d_lse, d_ws, attend_ws, st);

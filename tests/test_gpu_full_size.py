@@ -1,4 +1,4 @@
-"""Parity at the five workloads' full sizes, in the launch configuration bench.py times.
+"""Parity at the workloads' full sizes, in the launch configuration bench.py times.
 
 Attention is compared with the fp64 oracle on every (stream, row, head) the oracle
 finishes in seconds (all of them for the decode batch and the long window), on a
@@ -100,3 +100,26 @@ def test_full_model_step():
     B.tf_paged_mla_attend(res.pool, 5, pt2, res.max_pages, res.lens, q, w.scale, o2, None, res.workspace())
     torch.cuda.synchronize()
     assert np.array_equal(bits(o1), bits(o2))
+
+
+def test_fp8_decode_all_heads():
+    """The decode batch on FP8 pages, as bench.py runs it: a quantizing append, then the
+    expansion and the attention, against the oracle over the dequantized rows."""
+    w = Y.WORKLOADS["fp8_decode"]()
+    res = Resident(w, fp8=True)
+    out, lse = run_step(res)
+    no_device_error(res.pool)
+    compare(w, out, lse, fp8=True)
+
+
+def test_sparse_decode_full_size():
+    """64 streams, 64 heads, 2,048 listed rows each, in the benchmark's launch configuration."""
+    from tests.test_gpu_sparse import check, run_sparse
+    w = Y.WORKLOADS["sparse_decode"]()
+    lists = Y.listed_rows(w.seed, w.lens, int(w.extra["nidx"]))
+    res = Resident(w)
+    lat, rope = res.current_rows(0)
+    res.append_current(0, lat, rope)
+    out, lse = run_sparse(res, w, lists)
+    no_device_error(res.pool)
+    check(w, out, lse, lists)
