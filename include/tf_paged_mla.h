@@ -76,11 +76,13 @@ extern "C" {
  * quantizes each latent row: amax = max_i |x_i|, scale = amax / 448 (fp32 division), code_i =
  * E4M3(x_i / scale) rounded to nearest even with saturation to +-448 (fp32 division); a row of
  * zeros stores scale 0 and codes 0.  Inputs must be finite.  tf_paged_mla_attend computes the
- * same attention over the dequantized rows (the per-stream rows are expanded to bf16 in the
- * workspace, then attended; the workspace size includes them).  tf_state_copy_rows copies codes,
- * scales and rope of rows [0, at).  Poison fills taken pages with 0xFF bytes (NaN in all three
- * blocks).  tf_paged_mla_attend_sparse and tf_paged_mla_attend_static return TF_E_UNSUPPORTED
- * on an FP8 pool. */
+ * same attention over the dequantized rows, each value taken as bf16(code * scale): the kernel
+ * reads the codes and expands each key tile in shared memory (the workspace is as on a BF16
+ * pool); on a TF_POOL_BATCH_INVARIANT pool the rows are first expanded to bf16 pages in the
+ * workspace, whose size then includes them.  tf_state_copy_rows copies codes, scales and rope
+ * of rows [0, at).  Poison fills taken pages with 0xFF bytes (NaN in all three blocks).
+ * tf_paged_mla_attend_sparse returns TF_E_UNSUPPORTED on an FP8 pool, and so does
+ * tf_paged_mla_attend_static on a batch-invariant FP8 pool. */
 
 typedef struct tf_kvpool tf_kvpool;
 

@@ -30,6 +30,8 @@
 // (one TMEM lane quadrant each); warps 4-5 softmax (quadrants 0-1 = the 64 rows of
 // S); warp 6 the TMA producer; warp 7 TMEM allocation and the single-thread MMA issuer.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -63,6 +65,16 @@ constexpr int TMEM_COLS = 512;
 constexpr int TMEM_O = 0;                       // O^T M-tile j at 64 j (j < 4)
 constexpr int TMEM_S = 256;                     // S buffers at 256 and 320
 constexpr int THREADS = 352;
+// FP8 pages: four more warps (11-14) expand each tile's E4M3 codes into the BF16 boxes in place.
+// The codes land (TMA, 8 boxes of 64 rows x 64 bytes) in the upper half of the latent boxes'
+// room, [F8_STAGING, F8_STAGING + 32 KB) = BF16 boxes 4-7, and box b is written to BF16 box b
+// in order, two boxes a round, so each write covers only codes already read (the last round,
+// boxes 6-7, reads all its rows first).
+constexpr int THREADS_F8 = THREADS + 128;
+constexpr int F8_THREADS = THREADS_F8 - THREADS;   // two threads a tile row
+constexpr int F8_BOX_BYTES = BK * 64;            // [64 rows][64 codes]
+constexpr int F8_STAGING = 4 * BOX_BYTES;        // 32,768
+static_assert(F8_STAGING + 8 * F8_BOX_BYTES == 8 * BOX_BYTES, "the codes fill BF16 boxes 4-7 exactly");
 // A key tile lands in two parts: part 0 the rope box (free once QK^T has read it) and
 // latent boxes 0-1 (the first pair PV releases), part 1 latent boxes 2-7.  QK^T starts
 // on part 0 while the rest of the tile is still loading; the previous tile's latent
@@ -76,6 +88,8 @@ constexpr int MAX_CTAS = 240;                   // CTAs a launch (one a SM); siz
 constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(64, BK, false, false);
 
 struct Ctrl {
+    float scales[NSTAGE][BK];          // FP8: the tile's row scales (a bulk copy; 16-byte aligned)
+    uint64_t f8_full[NSTAGE];          // FP8: codes and scales landed
     uint64_t part_full[NSTAGE][2];     // part 0: rope + latent boxes 0-1 landed; part 1: latent boxes 2-7
     uint64_t lat_empty[NSTAGE][4];     // latent box pair (2j, 2j+1) free: PV M-tile j done
     uint64_t rope_empty[NSTAGE];       // rope box free: QK^T done
@@ -133,6 +147,7 @@ struct Params {
     float *ws_o;          // [slots][64][512]
     float *ws_ml;         // [slots][64][2]
     DevErr *err;
+    const char *pool_base;  // FP8: the pool (row scales are read from each page)
     int64_t total;        // RANGES: numbered key tiles; UNITS: units
     float scale_log2;
     int32_t cache, max_pages, num_pages, S, R, H, ncols, groups, windowed;
@@ -268,8 +283,8 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tm, ui
 // rescale group, done with the previous segment's epilogue, posts its p_full, so
 // the accumulator is never overwritten while it is still being read.
 
-template <int MODE>
-__global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_constant__ Params p) {
+template <int MODE, bool FP8 = false>
+__global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kernel(const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctrl &c = *reinterpret_cast<Ctrl *>(smem + SMEM_CTRL);
@@ -294,6 +309,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
             ptx::mbar_init(&c.part_full[i][1], NBOX - kPart0Boxes);
             for (int jm = 0; jm < 4; ++jm) ptx::mbar_init(&c.lat_empty[i][jm], 1);
             ptx::mbar_init(&c.rope_empty[i], 1);
+            if (FP8) ptx::mbar_init(&c.f8_full[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&c.s_full[i], 1);
@@ -449,7 +465,8 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
             const uint64_t pol_kv = ngroups > 2 ? ptx::policy_evict_last() : ptx::policy_evict_first();
             const uint64_t pol_q = ptx::policy_evict_last();
             int armed[NSTAGE][2];   // last global tile each part barrier was armed for (-1: never)
-            for (int i = 0; i < NSTAGE; ++i) armed[i][0] = armed[i][1] = -1;
+            int armed_f8[NSTAGE];   // FP8: the same for the codes' barrier
+            for (int i = 0; i < NSTAGE; ++i) armed[i][0] = armed[i][1] = armed_f8[i] = -1;
             int q_armed = -1;       // last segment whose queries were loaded
             bool stop = false;
             int gt = 0, si = 0;
@@ -481,32 +498,61 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
                         page = raw;
                     }
                     uint8_t *dst = smem + SMEM_KV + st * STAGE_BYTES;
-                    for (int bi = 0; bi < NBOX; ++bi) {
-                        const int b = kBoxOrder[bi];
+                    if constexpr (FP8) {
+                        // the codes overwrite BF16 boxes 4-7 and their expansion every box: the
+                        // whole stage must be free; the rope box lands as on BF16 pages (part 0)
                         if (gt >= NSTAGE) {
-                            uint64_t *e = (b == 8) ? &c.rope_empty[st] : &c.lat_empty[st][b >> 1];
-                            if (!ptx::mbar_wait(e, ph, abort, errp, 1)) {
+                            bool okw = ptx::mbar_wait(&c.rope_empty[st], ph, abort, errp, 1);
+                            for (int jm = 0; okw && jm < 4; ++jm)
+                                okw = ptx::mbar_wait(&c.lat_empty[st][jm], ph, abort, errp, 1);
+                            if (!okw) {
                                 stop = true;
                                 break;
                             }
                         }
-                        uint64_t *full = &c.part_full[st][bi < kPart0Boxes ? 0 : 1];
-                        ptx::mbar_arrive_expect_tx(full, BOX_BYTES);
-                        if (b == 8)
-                            tma_load_4d(dst + 8 * BOX_BYTES, &p.tm_rope, full, 0, row, page, cache, pol_kv);
-                        else
-                            tma_load_4d(dst + b * BOX_BYTES, &p.tm_lat, full, b * 64, row, page, cache, pol_kv);
-                        armed[st][bi < kPart0Boxes ? 0 : 1] = gt;
+                        ptx::mbar_arrive_expect_tx(&c.part_full[st][0], BOX_BYTES);
+                        tma_load_4d(dst + 8 * BOX_BYTES, &p.tm_rope, &c.part_full[st][0], 0, row, page, cache, pol_kv);
+                        armed[st][0] = gt;
+                        ptx::mbar_arrive_expect_tx(&c.f8_full[st], 8 * F8_BOX_BYTES + BK * 4);
+                        for (int b = 0; b < 8; ++b)
+                            tma_load_4d(dst + F8_STAGING + b * F8_BOX_BYTES, &p.tm_lat, &c.f8_full[st], b * 64, row,
+                                        page, cache, pol_kv);
+                        ptx::bulk_g2s(&c.scales[st][0],
+                                      p.pool_base + ((size_t)cache * num_pages + page) * kF8PageBytes + kF8ScaleOff +
+                                          (size_t)row * 4,
+                                      BK * 4, &c.f8_full[st]);
+                        armed_f8[st] = gt;
+                    } else {
+                        for (int bi = 0; bi < NBOX; ++bi) {
+                            const int b = kBoxOrder[bi];
+                            if (gt >= NSTAGE) {
+                                uint64_t *e = (b == 8) ? &c.rope_empty[st] : &c.lat_empty[st][b >> 1];
+                                if (!ptx::mbar_wait(e, ph, abort, errp, 1)) {
+                                    stop = true;
+                                    break;
+                                }
+                            }
+                            uint64_t *full = &c.part_full[st][bi < kPart0Boxes ? 0 : 1];
+                            ptx::mbar_arrive_expect_tx(full, BOX_BYTES);
+                            if (b == 8)
+                                tma_load_4d(dst + 8 * BOX_BYTES, &p.tm_rope, full, 0, row, page, cache, pol_kv);
+                            else
+                                tma_load_4d(dst + b * BOX_BYTES, &p.tm_lat, full, b * 64, row, page, cache, pol_kv);
+                            armed[st][bi < kPart0Boxes ? 0 : 1] = gt;
+                        }
+                        if (stop) break;
                     }
-                    if (stop) break;
                 }
             }
             // no copy may still be writing shared memory when the CTA exits
             if (q_armed >= 0) ptx::mbar_wait(&c.q_full, q_armed & 1, abort, errp, 10, 1ll << 28);
-            for (int i = 0; i < NSTAGE; ++i)
+            for (int i = 0; i < NSTAGE; ++i) {
                 for (int h = 0; h < 2; ++h)
                     if (armed[i][h] >= 0)
                         ptx::mbar_wait(&c.part_full[i][h], (armed[i][h] / NSTAGE) & 1, abort, errp, 11, 1ll << 28);
+                if (armed_f8[i] >= 0)
+                    ptx::mbar_wait(&c.f8_full[i], (armed_f8[i] / NSTAGE) & 1, abort, errp, 18, 1ll << 28);
+            }
         }
     } else if (warp == 9 || warp == 10) {
         // ================= MMA issuers =================
@@ -604,6 +650,76 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attend_kernel(const __grid_con
             ptx::mbar_wait(&c.drain, 0, abort, errp, 6, 1ll << 29);
         }
         __syncwarp();
+    } else if (FP8 && warp >= 11) {
+        // ================= FP8 expansion (warps 11-14): half a tile row a thread =================
+        // Box b's 64 codes of row r become bf16(code * scale_r), written 128B-swizzled into BF16
+        // box b (16-byte chunk j of the row at j ^ (r & 7)); thread (r, hf) does codes 32hf..+31.
+        // Each finished box is one arrival on the part barrier the MMA issuers wait for, after a
+        // proxy fence.
+        const int ft = (int)threadIdx.x - THREADS;
+        const int r = ft >> 1, hf = ft & 1;
+        bool ok = true;
+        int gt = 0;
+        SegIter<MODE> it(p);
+        Seg q;
+        while (ok && it.next(p, q)) {
+            for (int tl = 0; tl < q.nt; ++tl, ++gt) {
+                const int st = gt % NSTAGE;
+                const bool landed = ptx::mbar_wait(&c.f8_full[st], (gt / NSTAGE) & 1, abort, errp, 16);
+                if (ptx::named_bar_or(2, F8_THREADS, !landed || *abort)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *stage = smem + SMEM_KV + st * STAGE_BYTES;
+                const float sc = c.scales[st][r];
+                // two boxes a round: {0,1} (part 0), then {2,3}, {4,5}, {6,7} (part 1)
+#pragma unroll 1
+                for (int b0 = 0; b0 < 8; b0 += 2) {
+                    uint4 cv[2][2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(stage + F8_STAGING + (b0 + u) * F8_BOX_BYTES +
+                                                                           r * 64 + hf * 32);
+                        cv[u][0] = src[0];
+                        cv[u][1] = src[1];
+                    }
+                    uint32_t o[2][16];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const uint32_t w4[4] = {cv[u][k].x, cv[u][k].y, cv[u][k].z, cv[u][k].w};
+#pragma unroll
+                            for (int wi = 0; wi < 4; ++wi)
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+                                        (__nv_fp8x2_storage_t)((w4[wi] >> (16 * h)) & 0xFFFFu), __NV_E4M3);
+                                    const float2 f = __half22float2(__half2(hr));
+                                    o[u][k * 8 + wi * 2 + h] = ptx::pack_bf16x2(f.x * sc, f.y * sc);
+                                }
+                        }
+                    // boxes 6-7 cover their own codes: every row read before any is overwritten
+                    if (b0 == 6) ptx::named_bar(2, F8_THREADS);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        uint8_t *dst = stage + (b0 + u) * BOX_BYTES + r * 128;
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int j = 4 * hf + jj;
+                            *reinterpret_cast<uint4 *>(dst + ((j ^ (r & 7)) << 4)) =
+                                make_uint4(o[u][4 * jj], o[u][4 * jj + 1], o[u][4 * jj + 2], o[u][4 * jj + 3]);
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();
+                    ptx::named_bar(2, F8_THREADS);
+                    if (ft == 0) {
+                        ptx::mbar_arrive(&c.part_full[st][b0 < 2 ? 0 : 1]);
+                        ptx::mbar_arrive(&c.part_full[st][b0 < 2 ? 0 : 1]);
+                    }
+                }
+            }
+        }
     } else if (warp >= 4) {
         // ================= softmax (warps 4-7: TMEM quadrant w holds S rows 16w..16w+15) =================
         // A 16x256b load gives thread t rows r0 = 16w + t/4 and r1 = r0 + 8, keys
@@ -1090,13 +1206,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 static bool encode(CUtensorMap *tm, void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-                   const cuuint32_t *box) {
+                   const cuuint32_t *box, CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = get_encode();
     if (!fn) return false;
     cuuint32_t es[4] = {1, 1, 1, 1};
-    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, dims, strides, box, es,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(tm, type, rank, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -1106,6 +1222,28 @@ static int ensure_pool_maps(tf_kvpool *pool) {
     pool->tm_lat.resize(2);
     pool->tm_rope.resize(2);
     const cuuint64_t P = (cuuint64_t)pool->desc.num_pages, C = (cuuint64_t)pool->desc.num_caches;
+    if (is_fp8(pool->desc)) {
+        // FP8 pages: the codes as bytes, unswizzled 64 x 64 boxes (expanded in shared memory);
+        // the rope block as on BF16 pages, at its FP8-page offset.  No row views (no gathers).
+        {
+            cuuint64_t dims[4] = {(cuuint64_t)kLat, (cuuint64_t)kPageRows, P, C};
+            cuuint64_t strides[3] = {(cuuint64_t)kLat, (cuuint64_t)kF8PageBytes, (cuuint64_t)kF8PageBytes * P};
+            cuuint32_t box[4] = {64, (cuuint32_t)attn::BK, 1, 1};
+            if (!encode(&pool->tm_lat[0], pool->base, 4, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
+                return TF_E_CUDA;
+        }
+        {
+            cuuint64_t dims[4] = {(cuuint64_t)kRope, (cuuint64_t)kPageRows, P, C};
+            cuuint64_t strides[3] = {(cuuint64_t)kRope * 2, (cuuint64_t)kF8PageBytes, (cuuint64_t)kF8PageBytes * P};
+            cuuint32_t box[4] = {64, (cuuint32_t)attn::BK, 1, 1};
+            if (!encode(&pool->tm_rope[0], pool->base + kF8RopeOff, 4, dims, strides, box)) return TF_E_CUDA;
+        }
+        pool->tm_lat[1] = pool->tm_lat[0];
+        pool->tm_rope[1] = pool->tm_rope[0];
+        pool->tmaps_ready = true;
+        return TF_OK;
+    }
     {
         cuuint64_t dims[4] = {(cuuint64_t)kLat, (cuuint64_t)kPageRows, P, C};
         cuuint64_t strides[3] = {(cuuint64_t)kLat * 2, (cuuint64_t)kPageBytes, (cuuint64_t)kPageBytes * P};
@@ -1151,6 +1289,10 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
             cudaFuncSetAttribute(mla_attend_kernel<MODE_SPLITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_TOTAL) != cudaSuccess ||
             cudaFuncSetAttribute(mla_attend_kernel<MODE_SPARSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_TOTAL) != cudaSuccess ||
+            cudaFuncSetAttribute(mla_attend_kernel<MODE_RANGES, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_TOTAL) != cudaSuccess ||
+            cudaFuncSetAttribute(mla_attend_kernel<MODE_UNITS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_TOTAL) != cudaSuccess)
             return TF_E_CUDA;
         attr_set = true;
@@ -1178,6 +1320,7 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     p.out = static_cast<__nv_bfloat16 *>(d_out);
     p.lse = d_lse;
     p.err = pool->err;
+    p.pool_base = pool->base;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     p.cache = cache;
     p.max_pages = max_pages;
@@ -1238,11 +1381,15 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     (void)ws_bytes;
     {
         ProfScope prof(pool, kProfAttend, st);
-        auto *kern = pl.mode == MODE_RANGES   ? mla_attend_kernel<MODE_RANGES>
-                     : pl.mode == MODE_UNITS  ? mla_attend_kernel<MODE_UNITS>
-                     : pl.mode == MODE_SPARSE ? mla_attend_kernel<MODE_SPARSE>
-                                              : mla_attend_kernel<MODE_SPLITS>;
-        const cudaError_t e = launch_pdl(kern, dim3(pl.nctas), dim3(THREADS), SMEM_TOTAL, st, p);
+        const bool f8 = is_fp8(pool->desc);
+        if (f8 && pl.mode != MODE_RANGES && pl.mode != MODE_UNITS) return TF_E_UNSUPPORTED;
+        auto *kern = f8 ? (pl.mode == MODE_RANGES ? mla_attend_kernel<MODE_RANGES, true>
+                                                  : mla_attend_kernel<MODE_UNITS, true>)
+                   : pl.mode == MODE_RANGES ? mla_attend_kernel<MODE_RANGES>
+                   : pl.mode == MODE_UNITS  ? mla_attend_kernel<MODE_UNITS>
+                   : pl.mode == MODE_SPARSE ? mla_attend_kernel<MODE_SPARSE>
+                                            : mla_attend_kernel<MODE_SPLITS>;
+        const cudaError_t e = launch_pdl(kern, dim3(pl.nctas), dim3(f8 ? THREADS_F8 : THREADS), SMEM_TOTAL, st, p);
         launch_counter()++;
         if (e != cudaSuccess) return TF_E_CUDA;
     }

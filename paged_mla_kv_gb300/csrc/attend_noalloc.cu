@@ -36,7 +36,8 @@ extern "C" int tf_paged_mla_attend_static(tf_kvpool *pool, int32_t cache, const 
                                           const int64_t *h_len, int32_t S, int32_t R, int32_t H, const void *d_q,
                                           float scale, void *d_out, float *d_lse, void *cuda_stream) {
     if (!pool || !h_len || S < 1 || S > TF_MAX_STREAMS || R < 1 || H < 1 || H > TF_MAX_HEADS) return TF_E_ARG;
-    if (tf::is_fp8(pool->desc)) return TF_E_UNSUPPORTED;  // the expanded rows need a caller workspace
+    // FP8 pages on a batch-invariant pool are expanded in a caller workspace
+    if (tf::is_fp8(pool->desc) && (pool->desc.flags & TF_POOL_BATCH_INVARIANT)) return TF_E_UNSUPPORTED;
     for (int s = 0; s < S; ++s)
         if (h_len[s] < R) return TF_E_RANGE;
     const size_t need = tf_paged_mla_workspace_bytes(pool, S, R, H, h_len);

@@ -218,7 +218,8 @@ extern "C" size_t tf_paged_mla_workspace_bytes(const tf_kvpool *p, int32_t S, in
         if (h_len[s] < R) return 0;
     const bool invariant = p && (p->desc.flags & TF_POOL_BATCH_INVARIANT);
     const size_t part = attend_workspace_bytes(invariant, S, R, H, h_len);
-    if (p && is_fp8(p->desc)) return (part + 1023) / 1024 * 1024 + fp8_shadow_bytes(S, h_len);
+    // FP8 pages on a batch-invariant pool are expanded to bf16 in the workspace first
+    if (p && is_fp8(p->desc) && invariant) return (part + 1023) / 1024 * 1024 + fp8_shadow_bytes(S, h_len);
     return part;
 }
 
@@ -237,11 +238,13 @@ extern "C" int tf_paged_mla_attend(tf_kvpool *p, int32_t cache, const int32_t *d
         if (h_len[s] < R || h_len[s] > (int64_t)max_pages * kPageRows) return TF_E_RANGE;
     if ((reinterpret_cast<uintptr_t>(d_q) & 15u) != 0 || (reinterpret_cast<uintptr_t>(d_out) & 15u) != 0)
         return TF_E_ARG;
-    const size_t part = attend_workspace_bytes((p->desc.flags & TF_POOL_BATCH_INVARIANT) != 0, S, R, H, h_len);
-    const size_t need = is_fp8(p->desc) ? (part + 1023) / 1024 * 1024 + fp8_shadow_bytes(S, h_len) : part;
+    const bool invariant = (p->desc.flags & TF_POOL_BATCH_INVARIANT) != 0;
+    const size_t part = attend_workspace_bytes(invariant, S, R, H, h_len);
+    const bool expand = is_fp8(p->desc) && invariant;   // else FP8 codes are expanded in the kernel
+    const size_t need = expand ? (part + 1023) / 1024 * 1024 + fp8_shadow_bytes(S, h_len) : part;
     if (need > 0 && (!d_ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(d_ws) & 255u) != 0))
         return d_ws && ws_bytes < need ? TF_E_NOMEM : TF_E_ARG;
-    if (is_fp8(p->desc))
+    if (expand)
         return launch_attend_fp8(p, cache, d_pt, max_pages, h_len, S, R, H, d_q, scale, d_out, d_lse, d_ws, ws_bytes,
                                  part, (cudaStream_t)stream);
     return launch_attend(p, cache, d_pt, max_pages, h_len, S, R, H, d_q, scale, d_out, d_lse, d_ws, ws_bytes,

@@ -140,8 +140,9 @@ def test_poison_fills_whole_fp8_pages():
 
 
 def test_unsupported_calls_and_small_workspace():
+    # a batch-invariant FP8 pool: attention expands the rows into the workspace first
     w = Y.custom("f8err", 67, lens=[900, 40], R=1, H=16)
-    res = Resident(w, fp8=True)
+    res = Resident(w, fp8=True, invariant=True)
     q = res.q()
     out = torch.empty((w.S, 1, w.H, 512), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((w.S, 1, w.H), dtype=torch.float32, device="cuda")
@@ -154,6 +155,14 @@ def test_unsupported_calls_and_small_workspace():
     with pytest.raises(B.TFError) as e:
         B.tf_paged_mla_attend_static(res.pool, 0, res.pt, res.max_pages, res.lens, q, w.scale, out, lse)
     assert e.value.code == -6
+    # on a default FP8 pool the codes are expanded in the kernel: no extra workspace, and the
+    # call that needs no workspace works
+    res2 = Resident(w, fp8=True)
+    assert B.tf_paged_mla_workspace_bytes(res2.pool, w.S, 1, w.H, res2.lens) == \
+        B.tf_paged_mla_workspace_bytes(None, w.S, 1, w.H, res2.lens)
+    B.tf_paged_mla_attend_static(res2.pool, 0, res2.pt, res2.max_pages, res2.lens, res2.q(), w.scale, out, lse)
+    torch.cuda.synchronize()
+    compare(w, out, lse, fp8=True)
     idx = torch.zeros((w.S, 4), dtype=torch.int32, device="cuda")
     with pytest.raises(B.TFError) as e:
         B.tf_paged_mla_attend_sparse(res.pool, 0, res.pt, res.max_pages, res.lens, idx, [4, 4], q[:, 0], w.scale,

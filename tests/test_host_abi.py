@@ -217,9 +217,11 @@ def test_workspace_is_bounded_by_the_cta_ranges(L):
 
 
 def test_fp8_pool_sizes_and_workspace(L):
-    """FP8 pages: 329,728 bytes a page (codes, scales, rope); attention's workspace adds the rows
-    expanded to BF16 pages, a table and 1 KiB of alignment room; no device memory is touched."""
-    desc = B.make_desc(3, 10, fp8=True)
+    """FP8 pages: 329,728 bytes a page (codes, scales, rope).  On a batch-invariant pool
+    attention's workspace adds the rows expanded to BF16 pages, a table and 1 KiB of alignment
+    room; on a default pool the kernel expands the codes itself and needs only the partials.
+    No device memory is touched."""
+    desc = B.make_desc(3, 10, fp8=True, invariant=True)
     n = B.tf_kvpool_bytes(desc)
     assert n == 3 * 10 * B.PAGE_BYTES_FP8 + 256
     h = ctypes.c_void_p()
@@ -228,13 +230,22 @@ def test_fp8_pool_sizes_and_workspace(L):
     assert L.tf_kvpool_page_ptr(h, 1, 2) - base == (10 + 2) * B.PAGE_BYTES_FP8
     lens = np.array([1000, 513, 7], np.int64)
     lp = lens.ctypes.data_as(ctypes.c_void_p)
-    plain = B.tf_paged_mla_workspace_bytes(None, 3, 1, 16, lens)
+    dinv = B.make_desc(3, 10, invariant=True)   # the same partials on a BF16 invariant pool
+    hb = ctypes.c_void_p()
+    assert L.tf_kvpool_create(ctypes.byref(dinv), ctypes.c_void_p(1 << 40), B.tf_kvpool_bytes(dinv),
+                              ctypes.byref(hb)) == B.TF_OK
+    plain = L.tf_paged_mla_workspace_bytes(hb, 3, 1, 16, lp)
+    L.tf_kvpool_destroy(hb)
     fp8 = L.tf_paged_mla_workspace_bytes(h, 3, 1, 16, lp)
     pages = 2 + 2 + 1
     assert fp8 == (plain + 1023) // 1024 * 1024 + 1024 + 1024 + pages * B.PAGE_BYTES_BF16
     # listed-row attention is refused on FP8 pages before anything else
     assert L.tf_paged_mla_sparse_workspace_bytes(h, 3, 16, np.array([4, 4, 4], np.int32).ctypes.data_as(
         ctypes.c_void_p)) == 0
+    L.tf_kvpool_destroy(h)
+    d2 = B.make_desc(3, 10, fp8=True)
+    assert L.tf_kvpool_create(ctypes.byref(d2), ctypes.c_void_p(1 << 40), n, ctypes.byref(h)) == B.TF_OK
+    assert L.tf_paged_mla_workspace_bytes(h, 3, 1, 16, lp) == L.tf_paged_mla_workspace_bytes(None, 3, 1, 16, lp)
     L.tf_kvpool_destroy(h)
     bad = B.make_desc(1, 4)
     bad.flags = 8
