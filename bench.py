@@ -77,8 +77,9 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> floa
 # DRAM bytes (read + written) of one launch of the dominant kernel, from one ncu capture, keyed
 # by the SHA-256 prefix of the kernel's source: a changed kernel reports null until re-captured.
 NCU_TRAFFIC = {
-    "a960f847979c8a16": {"decode_batch": 374_185_728 + 3_581_184,
-                         "prefill_100k": 1_947_665_000},   # prefill: ncu's DRAM rate x duration
+    "ffe7dc2342538a25": {"decode_batch": 373_990_912 + 3_765_504,
+                         "fp8_decode": 207_363_840 + 3_905_536,
+                         "prefill_100k": 1_933_900_000},   # prefill: ncu's DRAM rate x duration
     # top-k: both launches of one call (first level 811.1 + 8.6 MB, merge 58.8 + 0.2 MB)
     "4e5c0b41cdefdfb7": {"topk_prefill": 811_079_680 + 8_606_208 + 58_786_560 + 240_640},
 }
@@ -541,7 +542,7 @@ def main():
         peak = peaks.get("hbm_gbs", 6800.0)
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": ncu_traffic(args.workload), "peak_kind": f"{peak_src} HBM copy",
-                "kernel": ("dequant_kernel + mla_attend_kernel (FP8 rows expanded, then attended)"
+                "kernel": ("mla_attend_kernel<RANGES, FP8> (codes expanded in shared memory)"
                            if w.extra.get("fp8") else "mla_attend_kernel"),
                 "avg_launch_ms": avg_att}
 
