@@ -169,3 +169,31 @@ def test_unsupported_calls_and_small_workspace():
                                      out[:, 0], lse[:, 0])
     assert e.value.code == -6
     no_device_error(res.pool)
+
+
+@pytest.mark.parametrize("R,H", [(1, 64), (2, 64), (64, 64)])
+def test_fp8_attention_is_bf16_attention_over_the_expanded_rows(R, H):
+    """The kernel reads FP8 codes and expands them to bf16(code * scale) in shared memory, then
+    runs the BF16 pipeline: so it must equal, bit for bit, the BF16 attention over a pool that
+    holds those bf16 values.  R = 64 at 64 heads deals whole units (the prefill plan), the
+    others ranges of key tiles."""
+    lens = [700, 3000, 65]
+    share = [(-1, 0), (0, 1), (-1, 0)]   # the owner's first page is full (700 rows)
+    w8 = Y.custom(f"f8eq_{R}", 68 + R, lens=lens, R=R, H=H, share=share)
+    wb = Y.custom(f"f8eq_{R}", 68 + R, lens=lens, R=R, H=H, share=share)
+    orig = wb.page_rows
+
+    def expanded(c, s, p):
+        lat, rope = orig(c, s, p)
+        codes, scales = F.quantize_rows(Y.bf16_bits_to_f32(lat))
+        vals = F.decode_table()[codes].astype(np.float32) * scales[:, None]   # fp32 product, rounded
+        return Y.f32_to_bf16_bits(vals.astype(np.float32)), rope
+
+    wb.page_rows = expanded
+    _, o8, l8 = run(w8)
+    rb = Resident(wb)
+    ob, lb = rb.attend(rb.q())
+    torch.cuda.synchronize()
+    no_device_error(rb.pool)
+    assert np.array_equal(bits(o8), bits(ob))
+    assert np.array_equal(l8.cpu().numpy().view(np.uint32), lb.cpu().numpy().view(np.uint32))
