@@ -29,7 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOADS = ["decode_batch", "tiny_decode", "long_window", "prefill_100k", "prefill_208k", "full_model",
-             "sparse_decode", "fp8_decode", "topk_prefill"]
+             "sparse_decode", "fp8_decode", "sparse_fp8_decode", "topk_prefill"]
 TOPK = {"topk_prefill"}
 METRIC = "paged MLA decode KV GB/s + tokens/s vs HBM roofline; prefill TFLOP/s"
 L2_BYTES = 129 * 1024 * 1024
@@ -112,18 +112,18 @@ def step_units(w):
     """Algorithmic work of one step: bytes, flops, tokens."""
     from paged_mla_kv_gb300 import synth as Y
     S, R, H, C = w.S, w.R, w.H, w.num_caches
+    # an FP8 row is 512 code bytes, a 4-byte scale and the 128-byte bf16 rope
+    row = 644 if w.extra.get("fp8") else Y.ROW_BYTES
     if "nidx" in w.extra:
         # attention over listed rows: each stream reads its listed rows once for all heads
         n = [min(int(w.extra["nidx"]), int(L)) for L in w.lens]
-        kv = sum(n) * Y.ROW_BYTES
+        kv = sum(n) * row
         q = S * H * Y.DK * 2
         out = S * H * (512 * 2 + 4)
-        app = 2 * S * Y.ROW_BYTES
+        app = S * (Y.ROW_BYTES + row)
         flops = 2 * (Y.DK + 512) * H * sum(n)
         return dict(bytes=kv + q + out + app, attend_bytes=kv + q + out, flops=flops, attend_flops=flops,
                     tokens=S, kv=kv)
-    # an FP8 row is 512 code bytes, a 4-byte scale and the 128-byte bf16 rope
-    row = 644 if w.extra.get("fp8") else Y.ROW_BYTES
     kv = int(np.sum(w.lens)) * row
     q = S * R * H * Y.DK * 2
     out = S * R * H * (512 * 2 + 4)
@@ -237,7 +237,7 @@ class OracleSample:
             for s in range(w.S):
                 self.OA.attend_sparse(self.q[s, 0, :k], self.rows[s][0], self.rows[s][1], self.lists[s], w.scale,
                                       self.threads)
-                work += len(self.lists[s]) * 1152 * k / w.H
+                work += len(self.lists[s]) * self.row_bytes * k / w.H
         else:
             for s in range(w.S):
                 self.OA.attend_stream(self.q[s], self.rows[s][0], self.rows[s][1], w.scale, items, self.threads)
@@ -542,7 +542,7 @@ def main():
         peak = peaks.get("hbm_gbs", 6800.0)
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": ncu_traffic(args.workload), "peak_kind": f"{peak_src} HBM copy",
-                "kernel": ("mla_attend_kernel<RANGES, FP8> (codes expanded in shared memory)"
+                "kernel": ("mla_attend_kernel, FP8 instance (codes expanded in shared memory)"
                            if w.extra.get("fp8") else "mla_attend_kernel"),
                 "avg_launch_ms": avg_att}
 

@@ -81,8 +81,8 @@ extern "C" {
  * pool); on a TF_POOL_BATCH_INVARIANT pool the rows are first expanded to bf16 pages in the
  * workspace, whose size then includes them.  tf_state_copy_rows copies codes, scales and rope
  * of rows [0, at).  Poison fills taken pages with 0xFF bytes (NaN in all three blocks).
- * tf_paged_mla_attend_sparse returns TF_E_UNSUPPORTED on an FP8 pool, and so does
- * tf_paged_mla_attend_static on a batch-invariant FP8 pool. */
+ * tf_paged_mla_attend_sparse gathers the listed rows' codes and scales and expands them the
+ * same way.  tf_paged_mla_attend_static returns TF_E_UNSUPPORTED on a batch-invariant FP8 pool. */
 
 typedef struct tf_kvpool tf_kvpool;
 

@@ -37,6 +37,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <mutex>
 #include <numeric>
 
 #include "ptx.cuh"
@@ -309,7 +310,8 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             ptx::mbar_init(&c.part_full[i][1], NBOX - kPart0Boxes);
             for (int jm = 0; jm < 4; ++jm) ptx::mbar_init(&c.lat_empty[i][jm], 1);
             ptx::mbar_init(&c.rope_empty[i], 1);
-            if (FP8) ptx::mbar_init(&c.f8_full[i], 1);
+            // FP8: the codes' copies (and, for listed rows, the producer's scale stores)
+            if (FP8) ptx::mbar_init(&c.f8_full[i], MODE == MODE_SPARSE ? 2 : 1);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&c.s_full[i], 1);
@@ -351,8 +353,8 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             }
             const uint64_t pol_kv = ptx::policy_evict_first();
             const uint64_t pol_q = ptx::policy_evict_last();
-            int armed[NSTAGE][2];
-            for (int i = 0; i < NSTAGE; ++i) armed[i][0] = armed[i][1] = -1;
+            int armed[NSTAGE][2], armed_f8[NSTAGE];
+            for (int i = 0; i < NSTAGE; ++i) armed[i][0] = armed[i][1] = armed_f8[i] = -1;
             int q_armed = -1;
             bool stop = false;
             int gt = 0, si = 0;
@@ -379,6 +381,7 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                     const uint32_t ph = ((gt / NSTAGE) - 1) & 1;
                     const int64_t k0 = q.kb + (int64_t)tl * BK;
                     int ylat[2], yrope[2], badv = 0;
+                    const char *sc_addr[2] = {nullptr, nullptr};
                     bool bad = false;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -399,8 +402,14 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                             }
                         }
                         const int base = cache * num_pages + pg;
-                        ylat[h] = base * (int)(kPageBytes / (kLat * 2)) + (r & 511);
-                        yrope[h] = base * (int)(kPageBytes / (kRope * 2)) + (r & 511);
+                        // rows of the views: 1,024-byte latent rows (576 a page) and 128-byte rope
+                        // rows (4,608 a page) on BF16 pages; 512-byte code rows (644 a page) and
+                        // 128-byte rope rows (2,576 a page) on FP8 pages
+                        constexpr int kLatRowsPerPage = FP8 ? (int)(kF8PageBytes / kLat) : (int)(kPageBytes / (kLat * 2));
+                        constexpr int kRopeRowsPerPage = FP8 ? (int)(kF8PageBytes / (kRope * 2)) : (int)(kPageBytes / (kRope * 2));
+                        ylat[h] = base * kLatRowsPerPage + (r & 511);
+                        yrope[h] = base * kRopeRowsPerPage + (r & 511);
+                        if (FP8) sc_addr[h] = p.pool_base + (size_t)base * kF8PageBytes + kF8ScaleOff + (size_t)(r & 511) * 4;
                     }
                     const unsigned badm = __ballot_sync(0xffffffffu, bad);
                     if (badm) {
@@ -420,6 +429,41 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                     const int ro2 = __shfl_sync(0xffffffffu, yrope[0], 2 * jl + 1),
                               ro3 = __shfl_sync(0xffffffffu, yrope[1], 2 * jl + 1);
                     uint8_t *dst = smem + SMEM_KV + st * STAGE_BYTES;
+                    if constexpr (FP8) {
+                        // the whole stage must be free (the codes and their expansion cover it)
+                        int okw = 1;
+                        if (lane == 0 && gt >= NSTAGE) {
+                            okw = ptx::mbar_wait(&c.rope_empty[st], ph, abort, errp, 1);
+                            for (int jm = 0; okw && jm < 4; ++jm)
+                                okw = ptx::mbar_wait(&c.lat_empty[st][jm], ph, abort, errp, 1);
+                        }
+                        if (!__shfl_sync(0xffffffffu, okw, 0)) {
+                            stop = true;
+                            break;
+                        }
+                        if (lane == 0) {
+                            ptx::mbar_arrive_expect_tx(&c.part_full[st][0], BOX_BYTES);
+                            ptx::mbar_arrive_expect_tx(&c.f8_full[st], 8 * F8_BOX_BYTES);
+                        }
+                        __syncwarp();
+                        if (lane < 16) {
+                            ptx::tma_gather4(dst + 8 * BOX_BYTES + lane * 512, &p.tm_rope_rows, &c.part_full[st][0], 0,
+                                             ro0, ro1, ro2, ro3, pol_kv);
+                            // rows 4j..4j+3 of code box b: 4 x 64 bytes, unswizzled
+                            for (int b = 0; b < 8; ++b)
+                                ptx::tma_gather4(dst + F8_STAGING + b * F8_BOX_BYTES + lane * 256, &p.tm_lat_rows,
+                                                 &c.f8_full[st], b * 64, la0, la1, la2, la3, pol_kv);
+                        }
+                        // the row scales: each lane its two listed rows; a second arrival
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) c.scales[st][2 * lane + h] = __ldg(reinterpret_cast<const float *>(sc_addr[h]));
+                        __threadfence_block();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(&c.f8_full[st]);
+                        armed[st][0] = gt;
+                        armed_f8[st] = gt;
+                        continue;
+                    }
                     for (int bi = 0; bi < NBOX; ++bi) {
                         const int b = kBoxOrder[bi];
                         const int part = bi < kPart0Boxes ? 0 : 1;
@@ -451,10 +495,13 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             // no copy may still be writing shared memory when the CTA exits
             if (lane == 0) {
                 if (q_armed >= 0) ptx::mbar_wait(&c.q_full, q_armed & 1, abort, errp, 10, 1ll << 28);
-                for (int i = 0; i < NSTAGE; ++i)
+                for (int i = 0; i < NSTAGE; ++i) {
                     for (int h = 0; h < 2; ++h)
                         if (armed[i][h] >= 0)
                             ptx::mbar_wait(&c.part_full[i][h], (armed[i][h] / NSTAGE) & 1, abort, errp, 11, 1ll << 28);
+                    if (armed_f8[i] >= 0)
+                        ptx::mbar_wait(&c.f8_full[i], (armed_f8[i] / NSTAGE) & 1, abort, errp, 18, 1ll << 28);
+                }
             }
         } else if (lane == 0) {
             ptx::prefetch_tmap(&p.tm_lat);
@@ -1239,8 +1286,23 @@ static int ensure_pool_maps(tf_kvpool *pool) {
             cuuint32_t box[4] = {64, (cuuint32_t)attn::BK, 1, 1};
             if (!encode(&pool->tm_rope[0], pool->base + kF8RopeOff, 4, dims, strides, box)) return TF_E_CUDA;
         }
-        pool->tm_lat[1] = pool->tm_lat[0];
-        pool->tm_rope[1] = pool->tm_rope[0];
+        // row views for gathers: 512-byte code rows (644 a page: the scales and the rope block
+        // follow, never addressed) and 128-byte rope rows (2,576 a page); one-row boxes
+        const cuuint64_t pages = P * C;
+        {
+            cuuint64_t dims[2] = {(cuuint64_t)kLat, (pages - 1) * (kF8PageBytes / kLat) + kPageRows};
+            cuuint64_t strides[1] = {(cuuint64_t)kLat};
+            cuuint32_t box[2] = {64, 1};
+            if (!encode(&pool->tm_lat[1], pool->base, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
+                return TF_E_CUDA;
+        }
+        {
+            cuuint64_t dims[2] = {(cuuint64_t)kRope, (pages - 1) * (kF8PageBytes / (kRope * 2)) + kPageRows};
+            cuuint64_t strides[1] = {(cuuint64_t)kRope * 2};
+            cuuint32_t box[2] = {64, 1};
+            if (!encode(&pool->tm_rope[1], pool->base + kF8RopeOff, 2, dims, strides, box)) return TF_E_CUDA;
+        }
         pool->tmaps_ready = true;
         return TF_OK;
     }
@@ -1280,9 +1342,11 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
                   cudaStream_t st, const int32_t *d_idx, int max_idx, const int32_t *h_nidx) {
     using namespace attn;
     if (prepare_launch(pool, st) != TF_OK) return TF_E_CUDA;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(mla_attend_kernel<MODE_RANGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // every instance opted in to its shared memory once, whichever host thread comes first
+    static std::once_flag attr_once;
+    static bool attr_ok = false;
+    std::call_once(attr_once, [] {
+        attr_ok = !(cudaFuncSetAttribute(mla_attend_kernel<MODE_RANGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_TOTAL) != cudaSuccess ||
             cudaFuncSetAttribute(mla_attend_kernel<MODE_UNITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_TOTAL) != cudaSuccess ||
@@ -1293,10 +1357,11 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
             cudaFuncSetAttribute(mla_attend_kernel<MODE_RANGES, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_TOTAL) != cudaSuccess ||
             cudaFuncSetAttribute(mla_attend_kernel<MODE_UNITS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_TOTAL) != cudaSuccess)
-            return TF_E_CUDA;
-        attr_set = true;
-    }
+                                 SMEM_TOTAL) != cudaSuccess ||
+            cudaFuncSetAttribute(mla_attend_kernel<MODE_SPARSE, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_TOTAL) != cudaSuccess);
+    });
+    if (!attr_ok) return TF_E_CUDA;
     int rc = ensure_pool_maps(pool);
     if (rc != TF_OK) return rc;
 
@@ -1382,9 +1447,10 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     {
         ProfScope prof(pool, kProfAttend, st);
         const bool f8 = is_fp8(pool->desc);
-        if (f8 && pl.mode != MODE_RANGES && pl.mode != MODE_UNITS) return TF_E_UNSUPPORTED;
-        auto *kern = f8 ? (pl.mode == MODE_RANGES ? mla_attend_kernel<MODE_RANGES, true>
-                                                  : mla_attend_kernel<MODE_UNITS, true>)
+        if (f8 && pl.mode == MODE_SPLITS) return TF_E_UNSUPPORTED;
+        auto *kern = f8 ? (pl.mode == MODE_RANGES  ? mla_attend_kernel<MODE_RANGES, true>
+                           : pl.mode == MODE_UNITS ? mla_attend_kernel<MODE_UNITS, true>
+                                                   : mla_attend_kernel<MODE_SPARSE, true>)
                    : pl.mode == MODE_RANGES ? mla_attend_kernel<MODE_RANGES>
                    : pl.mode == MODE_UNITS  ? mla_attend_kernel<MODE_UNITS>
                    : pl.mode == MODE_SPARSE ? mla_attend_kernel<MODE_SPARSE>

@@ -254,7 +254,6 @@ extern "C" int tf_paged_mla_attend(tf_kvpool *p, int32_t cache, const int32_t *d
 // ---- kept-state copy ----
 // ---- attention over listed rows ----
 static int sparse_checks(const tf_kvpool *p, int32_t S, int32_t H, int32_t max_idx, const int32_t *h_nidx) {
-    if (p && is_fp8(p->desc)) return TF_E_UNSUPPORTED;
     if (S < 1 || S > TF_MAX_STREAMS || H < 1 || H > TF_MAX_HEADS || max_idx < 1 || !h_nidx) return TF_E_ARG;
     for (int s = 0; s < S; ++s)
         if (h_nidx[s] < 1 || h_nidx[s] > max_idx) return TF_E_RANGE;

@@ -235,6 +235,15 @@ def fp8_decode(seed: int = 2) -> Workload:
     return w
 
 
+def sparse_fp8_decode(seed: int = 6) -> Workload:
+    """The listed-row decode (same streams, rows and lists) held on FP8 pages."""
+    w = sparse_decode(seed)
+    w.name = "sparse_fp8_decode"
+    w.extra = dict(w.extra or {}, fp8=True)
+    w.notes += "; rows stored as E4M3 codes with one fp32 scale a row"
+    return w
+
+
 def permutation(seed: int, n: int) -> np.ndarray:
     """A seeded permutation of n pool pages (int32)."""
     return _rng(seed, 31337).permutation(n).astype(np.int32)
@@ -284,4 +293,5 @@ WORKLOADS = {
     "full_model": full_model,
     "sparse_decode": sparse_decode,
     "fp8_decode": fp8_decode,
+    "sparse_fp8_decode": sparse_fp8_decode,
 }

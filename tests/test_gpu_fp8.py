@@ -139,7 +139,7 @@ def test_poison_fills_whole_fp8_pages():
         assert (img[:, int(p)] == 0xFF).all()
 
 
-def test_unsupported_calls_and_small_workspace():
+def test_invariant_pool_workspace_and_static_call():
     # a batch-invariant FP8 pool: attention expands the rows into the workspace first
     w = Y.custom("f8err", 67, lens=[900, 40], R=1, H=16)
     res = Resident(w, fp8=True, invariant=True)
@@ -163,11 +163,6 @@ def test_unsupported_calls_and_small_workspace():
     B.tf_paged_mla_attend_static(res2.pool, 0, res2.pt, res2.max_pages, res2.lens, res2.q(), w.scale, out, lse)
     torch.cuda.synchronize()
     compare(w, out, lse, fp8=True)
-    idx = torch.zeros((w.S, 4), dtype=torch.int32, device="cuda")
-    with pytest.raises(B.TFError) as e:
-        B.tf_paged_mla_attend_sparse(res.pool, 0, res.pt, res.max_pages, res.lens, idx, [4, 4], q[:, 0], w.scale,
-                                     out[:, 0], lse[:, 0])
-    assert e.value.code == -6
     no_device_error(res.pool)
 
 
@@ -197,3 +192,55 @@ def test_fp8_attention_is_bf16_attention_over_the_expanded_rows(R, H):
     no_device_error(rb.pool)
     assert np.array_equal(bits(o8), bits(ob))
     assert np.array_equal(l8.cpu().numpy().view(np.uint32), lb.cpu().numpy().view(np.uint32))
+
+
+def run_sparse8(res, w, lists):
+    nidx = np.array([len(x) for x in lists], np.int32)
+    idx = np.zeros((w.S, int(nidx.max())), np.int32)
+    for s, x in enumerate(lists):
+        idx[s, :len(x)] = x
+    q = res.q()[:, 0]
+    out = torch.empty((w.S, w.H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.S, w.H), dtype=torch.float32, device="cuda")
+    n = B.tf_paged_mla_sparse_workspace_bytes(res.pool, w.S, w.H, nidx)
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device="cuda") if n else None
+    B.tf_paged_mla_attend_sparse(res.pool, 0, res.pt, res.max_pages, res.lens, torch.from_numpy(idx).cuda(), nidx,
+                                 q, w.scale, out, lse, ws)
+    torch.cuda.synchronize()
+    no_device_error(res.pool)
+    return out, lse
+
+
+@pytest.mark.parametrize("H", [16, 64])
+def test_listed_rows_on_fp8_pages(H):
+    """Listed-row attention gathers codes, scales and rope rows of an FP8 pool: against the
+    oracle over the dequantized rows, and bit for bit against the BF16 pool that holds
+    bf16(code * scale)."""
+    from oracle import attend as OA
+    lens = [5000, 700, 64, 3000]
+    w8 = Y.custom(f"f8sp_{H}", 80 + H, lens=lens, R=1, H=H)
+    wb = Y.custom(f"f8sp_{H}", 80 + H, lens=lens, R=1, H=H)
+    orig = wb.page_rows
+
+    def expanded(c, s, p):
+        lat, rope = orig(c, s, p)
+        codes, scales = F.quantize_rows(Y.bf16_bits_to_f32(lat))
+        vals = F.decode_table()[codes].astype(np.float32) * scales[:, None]
+        return Y.f32_to_bf16_bits(vals.astype(np.float32)), rope
+
+    wb.page_rows = expanded
+    lists = Y.listed_rows(90 + H, lens, 300, repeats=True)
+    r8 = Resident(w8, fp8=True)
+    o8, l8 = run_sparse8(r8, w8, lists)
+    rb = Resident(wb)
+    ob, lb = run_sparse8(rb, wb, lists)
+    assert np.array_equal(bits(o8), bits(ob))
+    assert np.array_equal(l8.cpu().numpy().view(np.uint32), lb.cpu().numpy().view(np.uint32))
+    qall = w8.q(0)
+    o = o8.float().cpu().numpy()
+    for s, x in enumerate(lists):
+        lat, rope = w8.stream_rows(0, s)
+        deq = F.dequantize_rows(*F.quantize_rows(Y.bf16_bits_to_f32(lat)))
+        ref, lref = OA.attend_sparse(qall[s, 0], deq, rope, x, w8.scale)
+        assert float(np.max(np.abs(o[s] - ref))) <= 2e-3, s
+        assert float(np.max(np.abs(l8.cpu().numpy()[s] - lref))) <= 2e-3, s
