@@ -77,9 +77,9 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> floa
 # DRAM bytes (read + written) of one launch of the dominant kernel, from one ncu capture, keyed
 # by the SHA-256 prefix of the kernel's source: a changed kernel reports null until re-captured.
 NCU_TRAFFIC = {
-    "ffe7dc2342538a25": {"decode_batch": 373_990_912 + 3_765_504,
-                         "fp8_decode": 207_363_840 + 3_905_536,
-                         "prefill_100k": 1_933_900_000},   # prefill: ncu's DRAM rate x duration
+    "2f59a0afe5387acf": {"decode_batch": 374_411_008 + 3_947_008,
+                         "fp8_decode": 207_393_536 + 3_709_952,
+                         "prefill_100k": 1_937_500_000},   # prefill: ncu's DRAM rate x duration
     # top-k: both launches of one call (first level 811.1 + 8.6 MB, merge 58.8 + 0.2 MB)
     "4e5c0b41cdefdfb7": {"topk_prefill": 811_079_680 + 8_606_208 + 58_786_560 + 240_640},
 }
