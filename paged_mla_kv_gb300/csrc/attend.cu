@@ -7,28 +7,30 @@
 //   out[s,r,h,:] = softmax_j(scale * q[s,r,h,:] . K_j) . C_j,  j <= len[s]-R+r
 // with K_j = (latent C_j, rope Kr_j), 576 wide, and the value the 512-wide latent.
 //
-// Work unit (one CTA): one stream, a group of up to 64 (row, head) columns, and a
-// split of the stream's keys.  Keys stream through 64-row tiles: 9 boxes of
-// [64 keys x 64 columns] bf16 (8 latent + 1 rope), loaded by TMA with 128-byte
-// swizzle from the tile's pool page into a 2-stage ring; the rope box is released
-// after QK^T and each latent box pair as soon as its PV M-tile finishes, so the next
-// tile's loads start early.  The same shared-memory tile feeds both
-// contractions on the 5th-generation tensor cores:
-//   S   = Q . K^T     tcgen05.mma M=128 (Q rows; rows 64-127 unused), N=64 keys, K=576,
-//                     Q K-major, the tile K-major; S accumulates in TMEM (2 buffers)
-//   O^T += V^T . P^T  tcgen05.mma M=128 latent columns x 4, N = group columns, K=64 keys,
-//                     the tile read MN-major as V^T, P (bf16, in shared memory) K-major;
-//                     O^T accumulates in TMEM (4 x 64 columns)
-// Softmax is online in fp32 registers, one thread per (row, head) column, with a
-// lazily moved reference maximum: O is rescaled only when a tile's maximum passes
-// the reference by more than 2^8, by a separate warp group, so the softmax warps
-// never wait for it.  Each split writes fp32 partials (unnormalised O, running
-// maximum, sum); a combine kernel merges them in split-index order.  A stream cut
-// into one split writes bf16 output directly.
+// Work (one persistent CTA an SM): a CTA walks segments, each one column group (up to 64
+// (row, head) columns) of one stream over a run of its key tiles; how the tiles are dealt out
+// (RANGES, UNITS, SPLITS, SPARSE) is described at the Params below.  Keys stream through
+// 64-row tiles: 9 boxes of [64 keys x 64 values] bf16 (8 latent + 1 rope), loaded by TMA with
+// 128-byte swizzle from the tile's pool page into a 2-stage ring, landing in a part of 3 boxes
+// (rope + latent 0-1) and a part of 6; the rope box is released after QK^T and each latent
+// box pair as soon as its PV M-tile finishes, so the next tile's loads start early.  The same
+// shared-memory tile feeds both contractions on the 5th-generation tensor cores:
+//   S   = Q . K^T     tcgen05.mma M=64 (the columns), N=64 keys, K=576, Q and the tile
+//                     K-major; S accumulates in TMEM (2 buffers)
+//   O^T += V^T . P^T  tcgen05.mma M=128 latent values x 4, N = columns rounded up to 16,
+//                     K=64 keys, the tile read MN-major as V^T, P (bf16, in shared memory)
+//                     K-major; O^T accumulates in TMEM (4 x 64 columns)
+// Softmax is online in fp32 registers, each of four warps reading one TMEM lane quadrant
+// (two rows and 16 of their keys a thread), with a lazily moved reference maximum: O^T is
+// rescaled only when a tile's maximum passes the reference by more than 2^8, by a separate
+// warp group.  A segment that is its whole unit writes bf16 output directly; a unit cut into
+// several segments writes fp32 partials (unnormalised O, running maximum, sum) that a
+// combine kernel merges in key order.
 //
-// Warp roles (256 threads): warps 0-3 rescale O^T when asked and run the epilogue
-// (one TMEM lane quadrant each); warps 4-5 softmax (quadrants 0-1 = the 64 rows of
-// S); warp 6 the TMA producer; warp 7 TMEM allocation and the single-thread MMA issuer.
+// Warp roles (352 threads; 480 on FP8 pages): warps 0-3 rescale O^T when asked and run the
+// epilogue (one TMEM lane quadrant each); warps 4-7 softmax; warp 8 the TMA producer; warp 9
+// the TMEM allocation and the QK^T issuer; warp 10 the PV issuer; on FP8 pages warps 11-14
+// expand each tile's codes to bf16 in shared memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
