@@ -82,8 +82,9 @@ NCU_TRAFFIC = {
     "05f8dad3b10daf10": {"decode_batch": 374_411_008 + 3_947_008,
                          "fp8_decode": 207_393_536 + 3_709_952,
                          "prefill_100k": 1_937_500_000},   # prefill: ncu's DRAM rate x duration
-    # top-k: both launches of one call (first level 811.1 + 8.6 MB, merge 58.8 + 0.2 MB)
-    "4e5c0b41cdefdfb7": {"topk_prefill": 811_079_680 + 8_606_208 + 58_786_560 + 240_640},
+    # top-k: both launches of one call (first level 811.1 + 8.6 MB, merge 58.8 + 0.2 MB), taken
+    # on source 4e5c0b41cdefdfb7; 837315f872e36916 differs in its header comment only (same cubin)
+    "837315f872e36916": {"topk_prefill": 811_079_680 + 8_606_208 + 58_786_560 + 240_640},
 }
 
 

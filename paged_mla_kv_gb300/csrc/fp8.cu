@@ -4,8 +4,9 @@
 //
 // append_fp8_kernel quantizes each new latent row (amax / 448 scale, E4M3 round-to-nearest-even
 // with saturation); state_copy_fp8_kernel copies the first `at` rows of a kept state block by
-// block; attention expands every stream's rows to bf16 pages in the caller's workspace
-// (dequant_kernel) and runs the BF16 attention over that view.
+// block.  The attention kernel reads the codes itself (attend.cu); on a batch-invariant pool
+// the rows are first expanded to bf16 pages in the caller's workspace (dequant_kernel) and the
+// BF16 attention runs over that view.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>

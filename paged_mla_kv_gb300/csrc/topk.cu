@@ -4,12 +4,15 @@
 // number), larger first, ties by the smaller column.
 //
 // One CTA a block.  The block's keys live in registers (32 a thread for logits, 16 key/column
-// pairs a thread for candidates), mapped to unsigned integers that compare like the values.
-// A radix select with digits of 11, 11 and 10 bits (histograms in shared memory) finds the
-// k-th key; it stops early at the first digit whose bin is needed whole.  When only part of the
-// keys equal to the k-th are needed, a second radix select over their columns picks the
-// smallest.  The winners are compacted with one shared atomic a warp; the last level sorts
-// them (bitonic, in shared memory) and writes columns and values.
+// pairs a thread for candidates), mapped to unsigned integers that compare like the values
+// (merge blocks rescaled onto the whole range first).  One histogram of the top 11 bits finds
+// the bin of the k-th key; the keys at or above it go to a shared list, where the select goes
+// on with digits of 11 and 10 bits (stopping at the first digit whose bin is needed whole),
+// and the keys equal to the k-th are ranked by counting their smaller columns (a radix pass
+// over columns when there are many).  A block whose list overflows selects over the block
+// again from global memory.  The winners are compacted with one shared atomic a warp; the last
+// level sorts them (a bitonic network: registers, warp shuffles, then shared memory) and writes
+// columns and values.
 #include <cstdint>
 #include <mutex>
 
