@@ -76,10 +76,10 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> floa
 # the kernel changes, the counters no longer describe it and "traffic" is reported null.
 # DRAM bytes (read + written) of one launch of the dominant kernel, from one ncu capture, keyed
 # by the SHA-256 prefix of the kernel's source: a changed kernel reports null until re-captured.
-# The attention counters were taken on source 2f59a0afe5387acf; 05f8dad3b10daf10 differs from it
-# in its header comment only, and compiles to the same device code (equal cubin hashes).
+# The attention counters were taken on source 2f59a0afe5387acf; c5105e5b44b72992 differs from it
+# in comments only, and compiles to the same device code (equal cubin hashes).
 NCU_TRAFFIC = {
-    "05f8dad3b10daf10": {"decode_batch": 374_411_008 + 3_947_008,
+    "c5105e5b44b72992": {"decode_batch": 374_411_008 + 3_947_008,
                          "fp8_decode": 207_393_536 + 3_709_952,
                          "prefill_100k": 1_937_500_000},   # prefill: ncu's DRAM rate x duration
     # top-k: both launches of one call (first level 811.1 + 8.6 MB, merge 58.8 + 0.2 MB), taken

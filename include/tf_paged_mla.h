@@ -8,8 +8,8 @@
  *  - rows sit in 512-row pages taken from one shared pool; a stream maps its
  *    logical pages to pool pages through a page table, and the cache kernels take
  *    that table plus the elements between pages (issue #1142, "GLM declares a
- *    kv_pool.Layout"); a null table keeps contiguous rows, so a window is pages
- *    in order and one address formula serves both (issue #1313, step 1.3);
+ *    kv_pool.Layout"); a null table keeps contiguous rows: a window is its pages taken in
+ *    order, under the same addressing rule (issue #1313, step 1.3);
  *  - taken pages can be filled with NaN so that a read before a write shows
  *    (issue #1142, same section: TF_KV_POISON=1);
  *  - streams share prefix pages by reference the way the radix prompt store keeps
@@ -61,12 +61,12 @@ extern "C" {
 #define TF_MAX_STREAMS 512
 #define TF_MAX_HEADS 128
 #define TF_POOL_POISON 1u      /* fill pages with bf16 NaN (0x7FC0) when they are taken */
-#define TF_POOL_BATCH_INVARIANT 2u  /* attention on this pool: a stream's bits do not depend
-                                       on the other streams of a batch (see tf_paged_mla_attend) */
+#define TF_POOL_BATCH_INVARIANT 2u  /* attention on this pool: a stream's result has the same
+                                       bits whatever else is in the batch (see tf_paged_mla_attend) */
 #define TF_POOL_FP8 4u              /* FP8 latent rows (see "FP8 pages" below) */
 
-/* ---- FP8 pages (issue #1313, step 1.3, item 3: FP8 rows on pages, each 512-row page keeping
- * its rows' FP32 scales after its rows; windows keep the same blocks) ----
+/* ---- FP8 pages (issue #1313, step 1.3, item 3: FP8 latent rows on pages, a page's fp32 row
+ * scales stored behind its rows; windows laid out the same way) ----
  * With TF_POOL_FP8 a page of one cache is
  *   latent codes  512 rows x 512 bytes, OCP FP8 E4M3 (bias 7, largest finite 448)   262,144 B
  *   scales        512 fp32, one a row                                                  2,048 B
@@ -240,9 +240,9 @@ int tf_paged_mla_attend(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int
  *   order them on one stream, or use tf_paged_mla_attend with separate workspaces. */
 #define TF_STATIC_WS_BYTES (64u << 20)
 
-/* ---- attention over listed rows (issue #1313, step 2: a sparse row reads up to 2,048
- * latent rows; issue #1142, section 2: the latent kernels for dense chunks and the sparse
- * gather take the page table; "What stays as it is": the sparse pass gathers the same rows) ----
+/* ---- attention over listed rows (issue #1313, step 2: a sparse decode row touches at most
+ * 2,048 latent rows; issue #1142, section 2: both the dense
+ * latent kernels and the sparse gather are given the page table; "What stays as it is": the sparse path reads the same rows) ----
  * One query row a stream (R = 1).  Stream s's keys are the rows d_idx[s][0 .. h_nidx[s]) of the
  * stream (row numbers as in tf_paged_mla_attend, each < h_len[s]), in list order:
  *   s_j = scale * (q[s][h][0:512] . C_idx[j] + q[s][h][512:576] . Kr_idx[j])

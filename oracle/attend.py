@@ -75,8 +75,8 @@ def attend_sparse(q: np.ndarray, lat: np.ndarray, rope: np.ndarray, idx, scale: 
                   threads: int | None = None):
     """Attention of one query row over listed rows of a stream.
 
-    Issue #1313, step 2: a sparse row reads up to 2,048 listed latent rows; issue #1142,
-    "What stays as it is": the sparse pass gathers the same rows.  The keys are the rows
+    Issue #1313, step 2: a sparse decode row touches at most 2,048 latent rows; issue #1142,
+    "What stays as it is": the sparse path reads the same rows.  The keys are the rows
     idx[0..n) in list order (a row listed twice counts twice), so this is the contiguous
     definition above applied to the gathered rows.
     q: bf16 bits [H][576]; lat: [len][512]; rope: [len][64]; idx: n row numbers in [0, len).

@@ -1,7 +1,7 @@
 """FP8 latent rows: E4M3 codes with one fp32 scale a row -- TEST INFRASTRUCTURE ONLY.
 
-Issue #1313, step 1.3, item 3: FP8 rows on pages, each 512-row page keeping its rows' FP32
-scales after its rows (516 bytes a row and cache for the latent).  The pages fix neither the
+Issue #1313, step 1.3, item 3: FP8 latent rows on pages, a page's fp32 row scales stored
+behind its 512 rows (516 latent bytes a row and cache).  The pages fix neither the
 FP8 format nor how the scale is chosen.  Read here as the OCP E4M3 format (1 sign bit,
 4 exponent bits with bias 7, 3 mantissa bits; subnormals; no infinities; 0x7F / 0xFF are NaN;
 the largest finite value is 448) and a per-row absolute-maximum scale:

@@ -119,7 +119,7 @@ static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 //  - SPLITS (a pool made with TF_POOL_BATCH_INVARIANT).  Each stream's keys are cut
 //    into splits whose bounds depend on that stream's length alone, one CTA a
 //    (split, group) item, and the partials are merged in split order, so a stream's
-//    bits do not depend on the other streams of the batch.
+//    result has the same bits whatever else is in the batch.
 //  - SPARSE (tf_paged_mla_attend_sparse).  RANGES over the tiles of each stream's list
 //    of rows; the key tiles are gathered row by row (TMA gather4) through the table.
 enum { MODE_RANGES = 0, MODE_UNITS = 1, MODE_SPLITS = 2, MODE_SPARSE = 3 };

@@ -1,6 +1,5 @@
-// FP8 pages (issue #1313, step 1.3, item 3: FP8 rows on pages, each 512-row page keeping its
-// rows' FP32 scales after its rows; the windows keep the same blocks, so one address formula
-// serves both).  A page of one cache: 512 x 512 E4M3 codes, 512 fp32 scales, 512 x 64 bf16 rope.
+// FP8 pages (issue #1313, step 1.3, item 3: FP8 latent rows on pages, a page's fp32 row scales
+// stored behind its rows; windows laid out the same way, under the same addressing rule).  A page of one cache: 512 x 512 E4M3 codes, 512 fp32 scales, 512 x 64 bf16 rope.
 //
 // append_fp8_kernel quantizes each new latent row (amax / 448 scale, E4M3 round-to-nearest-even
 // with saturation); state_copy_fp8_kernel copies the first `at` rows of a kept state block by

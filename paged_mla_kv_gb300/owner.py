@@ -6,9 +6,9 @@ ranks (tensor parallel), so a decode step moves queries instead of rows:
   to their owners;
 - each owner runs attention for every head of the rows it owns, over its own pages,
   with the same attention call a single rank would make;
-- each owner sends every rank its heads' outputs back.
-Each head of each row is therefore computed by the same call over the same bytes as on
-one rank, so every rank's outputs equal the unsharded engine's bit for bit.
+- each owner returns to every rank the outputs of that rank's heads.
+Every (row, head) output thus comes from the same call over the same bytes as on one
+rank, so every rank's outputs equal the unsharded engine's bit for bit.
 
 This module is the routing only: who owns what, what moves where, and in which order.
 The attention itself is a callable the caller passes in (on a GPU, the library's
@@ -110,7 +110,7 @@ class OwnerDecode:
                         full[slot[s], :, hs] = msg[j]
         # 2. the owner computes every head of its rows, as a single rank would
         out_owned = attend(self.owned, full) if self.owned else None
-        # 3. every rank gets its heads' outputs back
+        # 3. every rank receives the outputs of its own heads
         out = torch.empty((S, R, hw, 512), dtype=q_local.dtype)
         for i, s in enumerate(self.owned):
             out[s] = out_owned[i, :, self.hs]

@@ -67,7 +67,7 @@ def test_tp2_256k():
     out = P.plan(mk(room_tp2(), 262144, 8))
     assert out.pool_pages == g["pool_pages"] and out.pool_tokens == g["pool_tokens"]
     assert P.windows_served(room_tp2(), 262144, BPT, FIXED) == g["windows_served"]
-    # step 1 holds at least the rows windows would have held in the same room
+    # step 1 never holds fewer rows than windows in the same room
     s1 = P.plan(mk(room_tp2(), 262144, 8, paged=True))
     assert s1.n_windows == g["windows_served"]
     assert s1.pool_tokens >= g["windows_served"] * 262144
