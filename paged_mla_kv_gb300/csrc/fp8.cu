@@ -11,6 +11,7 @@
 #include <cuda_fp8.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "ptx.cuh"
 #include "tf_internal.h"
@@ -248,7 +249,9 @@ int launch_attend_fp8(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_p
     char *shadow = reinterpret_cast<char *>((raw + 1023) & ~uintptr_t(1023));
     if ((size_t)(shadow - ws) + (size_t)sp.pages * kPageBytes > ws_bytes) return TF_E_NOMEM;
 
-    // the BF16 view over the workspace: one cache, its own maps, the pool's error word
+    // the BF16 view over the workspace: one cache, its own maps, the pool's error word; held
+    // until both launches are queued (their parameters are copied at launch)
+    std::lock_guard<std::mutex> guard(pool->shadow_mu);
     tf_kvpool *sh = pool->shadow;
     if (!sh) {
         sh = new (std::nothrow) tf_kvpool();

@@ -65,8 +65,10 @@ struct tf_kvpool {
     bool prof = false;
     std::vector<tf::ProfRec> recs;
     std::vector<cudaEvent_t> spare_events;
-    // FP8 pools: a BF16 view over the workspace that attention expands the rows into.
+    // FP8 pools on batch-invariant plans: a BF16 view over the workspace that attention expands
+    // the rows into, set up and launched under shadow_mu (calls from several host threads)
     tf_kvpool *shadow = nullptr;
+    std::mutex shadow_mu;
     ~tf_kvpool() { delete shadow; }
 };
 
