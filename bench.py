@@ -206,15 +206,18 @@ class OracleSample:
         self.q = w.q(0)
         self.rows = [w.stream_rows(0, s) for s in range(w.S)]
         self.row_bytes = 1152
+        self.lists = None
+        if "nidx" in w.extra:
+            from paged_mla_kv_gb300 import synth as Y
+            self.lists = Y.listed_rows(w.seed, w.lens, int(w.extra["nidx"]))
+            # only the listed rows are read: keep those, and list positions into them
+            self.rows = [(a[x], b[x]) for (a, b), x in zip(self.rows, self.lists)]
+            self.lists = [np.arange(len(x)) for x in self.lists]
         if w.extra.get("fp8"):   # the oracle attends over the rows as FP8 pages hold them
             from oracle import fp8 as F
             from paged_mla_kv_gb300 import synth as Y
             self.rows = [(F.dequantize_rows(*F.quantize_rows(Y.bf16_bits_to_f32(a))), b) for a, b in self.rows]
             self.row_bytes = 644
-        self.lists = None
-        if "nidx" in w.extra:
-            from paged_mla_kv_gb300 import synth as Y
-            self.lists = Y.listed_rows(w.seed, w.lens, int(w.extra["nidx"]))
         k0 = min(w.R if self.prefill else w.H, max(1, self.threads // (w.R if not self.prefill else 1)))
         k0 = max(1, min(k0, self.threads))
         t0, _ = self.run(k0)

@@ -10,7 +10,8 @@ the largest finite value is 448) and a per-row absolute-maximum scale:
 The latent value a code stands for is decode(code) * scale, exactly (in float64).
 
 Where floating point decides a code, this module takes the decision in fp32, as the
-quantizer does.  Encoding and decoding follow the bit fields of the format, not a library.
+quantizer does.  Encoding and decoding follow the bit fields of the format, not a library;
+encode() is the scalar definition and encode_array() the same rule over arrays (pinned to it).
 """
 from __future__ import annotations
 
@@ -68,6 +69,29 @@ def encode(x: float) -> int:
     return sign | ((e + 7) << 3) | m
 
 
+def encode_array(x) -> np.ndarray:
+    """encode() of every value of an array, the same definition written with numpy: the
+    exponent from frexp, the 3-bit mantissa rounded half to even (rint), the subnormal range
+    in steps of 2^-9, saturation to +-448 and NaN -> 0x7F.  uint8 codes."""
+    v = np.asarray(x, dtype=np.float32).astype(np.float64)
+    nan = np.isnan(v)
+    a = np.minimum(np.where(nan, 0.0, np.abs(v)), 2.0 * MAX_FINITE)   # all past 448 saturate
+    sign = np.where(np.signbit(v), 0x80, 0).astype(np.int64)
+    ms = np.rint(a / 2.0 ** -9).astype(np.int64)                 # subnormal: exact ratio
+    sub_code = np.where(ms >= 8, 0x08, ms)
+    fm, fe = np.frexp(a)                                         # a = fm * 2^fe, fm in [0.5, 1)
+    e = fe.astype(np.int64) - 1
+    mm = np.rint((2.0 * fm - 1.0) * 8.0).astype(np.int64)        # exact before rounding
+    carry = mm == 8
+    e = np.where(carry, e + 1, e)
+    mm = np.where(carry, 0, mm)
+    norm_code = ((e + 7) << 3) | mm
+    over = (a >= MAX_FINITE) | (e > 8) | ((e == 8) & (mm == 7))
+    code = np.where(a < 2.0 ** -6, sub_code, np.where(over, 0x7E, norm_code))
+    code = np.where(nan, NAN_CODE, code | sign)
+    return code.astype(np.uint8)
+
+
 def quantize_row(x) -> tuple:
     """(codes uint8[n], scale float32) of one latent row x (float32 values, finite)."""
     x = np.asarray(x, dtype=np.float32)
@@ -76,7 +100,7 @@ def quantize_row(x) -> tuple:
         return np.zeros(x.size, np.uint8), np.float32(0)
     scale = np.float32(amax / np.float32(MAX_FINITE))
     q = (x / scale).astype(np.float32)
-    return np.array([encode(v) for v in q], np.uint8), scale
+    return encode_array(q), scale
 
 
 def dequantize_row(codes, scale) -> np.ndarray:
@@ -99,10 +123,11 @@ def quantize_rows(x) -> tuple:
     """quantize_row over the last axis of a [..., n] array: (codes uint8[..., n], scales float32[...])."""
     x = np.asarray(x, dtype=np.float32)
     flat = x.reshape(-1, x.shape[-1])
-    codes = np.empty(flat.shape, np.uint8)
-    scales = np.empty(flat.shape[0], np.float32)
-    for i, row in enumerate(flat):
-        codes[i], scales[i] = quantize_row(row)
+    amax = np.max(np.abs(flat), axis=1).astype(np.float32) if flat.size else np.zeros(flat.shape[0], np.float32)
+    scales = (amax / np.float32(MAX_FINITE)).astype(np.float32)
+    safe = np.where(scales == 0, np.float32(1), scales).astype(np.float32)
+    q = (flat / safe[:, None]).astype(np.float32)
+    codes = np.where((scales == 0)[:, None], np.uint8(0), encode_array(q))
     return codes.reshape(x.shape), scales.reshape(x.shape[:-1])
 
 

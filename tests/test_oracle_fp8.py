@@ -96,3 +96,20 @@ def test_attention_over_double_latent_is_the_same_definition():
     deq = F.dequantize_rows(codes, scales)
     out, _ = OA.attend_stream(q[:1], deq, rope[:1], w.scale, threads=1)
     assert np.array_equal(out, np.repeat(deq, out.shape[0], axis=0))
+
+
+def test_array_encoder_is_the_scalar_definition():
+    g = np.random.default_rng(21)
+    x = np.concatenate([g.standard_normal(20000) * 50, g.uniform(-2 ** -5, 2 ** -5, 20000),
+                        g.uniform(-600, 600, 5000), [0.0, -0.0, np.nan, np.inf, -np.inf, 448.0, 464.0, 2 ** -10,
+                                                     3 * 2 ** -10, 15 * 2 ** -10, 1 + 1 / 16, 1 + 3 / 16]])
+    x = x.astype(np.float32)
+    x = np.concatenate([x, np.array([F.decode(c) for c in range(256) if c not in (0x7F, 0xFF)], np.float32)])
+    want = np.array([F.encode(v) for v in x], np.uint8)
+    assert np.array_equal(F.encode_array(x), want)
+    rows = (g.standard_normal((5, 512)) * 0.3).astype(np.float32)
+    rows[2] = 0
+    c, s_ = F.quantize_rows(rows)
+    for i in range(5):
+        ci, si = F.quantize_row(rows[i])
+        assert np.array_equal(c[i], ci) and s_[i] == si
