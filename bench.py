@@ -76,12 +76,12 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> floa
 # the kernel changes, the counters no longer describe it and "traffic" is reported null.
 # DRAM bytes (read + written) of one launch of the dominant kernel, from one ncu capture, keyed
 # by the SHA-256 prefix of the kernel's source: a changed kernel reports null until re-captured.
-# The attention counters were taken on source 2f59a0afe5387acf; c5105e5b44b72992 differs from it
-# in comments only, and compiles to the same device code (equal cubin hashes).
+# Attention: DRAM bytes re-captured on source 94c4ab2dc8479ab9 (`--metrics dram__bytes_read.sum,
+# dram__bytes_write.sum,gpu__time_duration.sum`, and the FP8 launch under `--set full`).
 NCU_TRAFFIC = {
-    "c5105e5b44b72992": {"decode_batch": 374_411_008 + 3_947_008,
-                         "fp8_decode": 207_393_536 + 3_709_952,
-                         "prefill_100k": 1_937_500_000},   # prefill: ncu's DRAM rate x duration
+    "94c4ab2dc8479ab9": {"decode_batch": 374_700_544 + 3_504_128,
+                         "fp8_decode": 207_994_112 + 4_065_024,
+                         "prefill_100k": 1_845_974_272 + 135_486_464},
     # top-k: both launches of one call (first level 811.1 + 8.6 MB, merge 58.8 + 0.2 MB), taken
     # on source 4e5c0b41cdefdfb7; 837315f872e36916 differs in its header comment only (same cubin)
     "837315f872e36916": {"topk_prefill": 811_079_680 + 8_606_208 + 58_786_560 + 240_640},

@@ -69,15 +69,21 @@ constexpr int TMEM_O = 0;                       // O^T M-tile j at 64 j (j < 4)
 constexpr int TMEM_S = 256;                     // S buffers at 256 and 320
 constexpr int THREADS = 352;
 // FP8 pages: four more warps (11-14) expand each tile's E4M3 codes into the BF16 boxes in place.
-// The codes land (TMA, 8 boxes of 64 rows x 64 bytes) in the upper half of the latent boxes'
-// room, [F8_STAGING, F8_STAGING + 32 KB) = BF16 boxes 4-7, and box b is written to BF16 box b
-// in order, two boxes a round, so each write covers only codes already read (the last round,
-// boxes 6-7, reads all its rows first).
+// The codes land by TMA, unswizzled, in the upper half of the latent boxes' room,
+// [F8_STAGING, +32 KB) = BF16 boxes 4-7: dense tiles as 8 boxes of 64 rows x 64 bytes (codes
+// 64b.. of row r at 4 KB b + 64 r), gathered tiles as 2 blocks of 64 rows x 256 bytes (codes
+// 256q.. of row r at 16 KB q + 256 r; a quarter of the gathers).  BF16 box b (codes 64b..64b+63)
+// is written in order, two boxes a round, so each write covers only codes already read (the
+// last round, boxes 6-7, reads all its rows first).
 constexpr int THREADS_F8 = THREADS + 128;
 constexpr int F8_THREADS = THREADS_F8 - THREADS;   // two threads a tile row
-constexpr int F8_BOX_BYTES = BK * 64;            // [64 rows][64 codes]
+constexpr int F8_BOX_BYTES = BK * 64;            // dense: [64 rows][64 codes]
+constexpr int F8_BLK = 256;                      // gathered: codes a box row (the unswizzled maximum)
+constexpr int F8_BLK_BYTES = BK * F8_BLK;        // [64 rows][256 codes] = 16 KB
+constexpr int F8_NBLK = kLat / F8_BLK;           // 2
 constexpr int F8_STAGING = 4 * BOX_BYTES;        // 32,768
 static_assert(F8_STAGING + 8 * F8_BOX_BYTES == 8 * BOX_BYTES, "the codes fill BF16 boxes 4-7 exactly");
+static_assert(F8_NBLK * F8_BLK_BYTES == 8 * F8_BOX_BYTES, "both layouts fill the same room");
 // A key tile lands in two parts: part 0 the rope box (free once QK^T has read it) and
 // latent boxes 0-1 (the first pair PV releases), part 1 latent boxes 2-7.  QK^T starts
 // on part 0 while the rest of the tile is still loading; the previous tile's latent
@@ -445,16 +451,17 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                         }
                         if (lane == 0) {
                             ptx::mbar_arrive_expect_tx(&c.part_full[st][0], BOX_BYTES);
-                            ptx::mbar_arrive_expect_tx(&c.f8_full[st], 8 * F8_BOX_BYTES);
+                            ptx::mbar_arrive_expect_tx(&c.f8_full[st], F8_NBLK * F8_BLK_BYTES);
                         }
                         __syncwarp();
                         if (lane < 16) {
                             ptx::tma_gather4(dst + 8 * BOX_BYTES + lane * 512, &p.tm_rope_rows, &c.part_full[st][0], 0,
                                              ro0, ro1, ro2, ro3, pol_kv);
-                            // rows 4j..4j+3 of code box b: 4 x 64 bytes, unswizzled
-                            for (int b = 0; b < 8; ++b)
-                                ptx::tma_gather4(dst + F8_STAGING + b * F8_BOX_BYTES + lane * 256, &p.tm_lat_rows,
-                                                 &c.f8_full[st], b * 64, la0, la1, la2, la3, pol_kv);
+                            // rows 4j..4j+3 of code block q: 4 x 256 bytes, unswizzled
+                            for (int qb = 0; qb < F8_NBLK; ++qb)
+                                ptx::tma_gather4(dst + F8_STAGING + qb * F8_BLK_BYTES + lane * 4 * F8_BLK,
+                                                 &p.tm_lat_rows, &c.f8_full[st], qb * F8_BLK, la0, la1, la2, la3,
+                                                 pol_kv);
                         }
                         // the row scales: each lane its two listed rows; a second arrival
 #pragma unroll
@@ -727,8 +734,10 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                     uint4 cv[2][2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const uint4 *src = reinterpret_cast<const uint4 *>(stage + F8_STAGING + (b0 + u) * F8_BOX_BYTES +
-                                                                           r * 64 + hf * 32);
+                        const int b = b0 + u;   // codes 64b.. of row r, in the dense or the gathered layout
+                        const int off = MODE == MODE_SPARSE ? (b >> 2) * F8_BLK_BYTES + r * F8_BLK + (b & 3) * 64
+                                                            : b * F8_BOX_BYTES + r * 64;
+                        const uint4 *src = reinterpret_cast<const uint4 *>(stage + F8_STAGING + off + hf * 32);
                         cv[u][0] = src[0];
                         cv[u][1] = src[1];
                     }
@@ -1294,7 +1303,7 @@ static int ensure_pool_maps(tf_kvpool *pool) {
         {
             cuuint64_t dims[2] = {(cuuint64_t)kLat, (pages - 1) * (kF8PageBytes / kLat) + kPageRows};
             cuuint64_t strides[1] = {(cuuint64_t)kLat};
-            cuuint32_t box[2] = {64, 1};
+            cuuint32_t box[2] = {(cuuint32_t)attn::F8_BLK, 1};
             if (!encode(&pool->tm_lat[1], pool->base, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8,
                         CU_TENSOR_MAP_SWIZZLE_NONE))
                 return TF_E_CUDA;
