@@ -12,7 +12,7 @@ Follows issue #1313 ("Why", third bullet; "Proposal, in two steps", step 1.1):
   (integer division, at least one window); the streams then hold
   max(n windows, one window plus a page for each other stream).
 
-Readings where the text is silent (also listed in the design doc):
+Readings where the text is silent:
 * "180 MiB fixed" is charged once for each of the lanes - 1 other streams;
 * every quantity is in bytes; `/` is integer division;
 * the plan refuses (None) when the room cannot hold the streams' pages and
