@@ -70,18 +70,17 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> floa
     return world * units_per_rank / (slowest_ms / 1e3)
 
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one mla_attend_kernel launch, from the ncu
-# captures summarised in profiles/ (mla_attend_<workload>.md).  Keyed by the first 16 hex
-# digits of the SHA-256 of the attention kernel's source the capture was taken on: once
-# the kernel changes, the counters no longer describe it and "traffic" is reported null.
-# DRAM bytes (read + written) of one launch of the dominant kernel, from one ncu capture, keyed
-# by the SHA-256 prefix of the kernel's source: a changed kernel reports null until re-captured.
-# Attention: DRAM bytes re-captured on source 94c4ab2dc8479ab9 (`--metrics dram__bytes_read.sum,
-# dram__bytes_write.sum,gpu__time_duration.sum`, and the FP8 launch under `--set full`).
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the dominant
+# kernel, from the ncu captures summarised in profiles/, keyed by the first 16 hex digits of
+# the SHA-256 of the kernel's source the capture was taken on: once the kernel changes, the
+# counters no longer describe it and "traffic" is reported null until it is re-captured.
+# Attention on source 94c4ab2dc8479ab9 (`--metrics dram__bytes_read.sum,dram__bytes_write.sum,
+# gpu__time_duration.sum`; the FP8 decode launch under `--set full`).
 NCU_TRAFFIC = {
     "94c4ab2dc8479ab9": {"decode_batch": 374_700_544 + 3_504_128,
                          "fp8_decode": 207_994_112 + 4_065_024,
-                         "prefill_100k": 1_845_974_272 + 135_486_464},
+                         "prefill_100k": 1_845_974_272 + 135_486_464,
+                         "sparse_fp8_decode": 103_608_832 + 3_570_432},
     # top-k: both launches of one call (first level 811.1 + 8.6 MB, merge 58.8 + 0.2 MB), taken
     # on source 4e5c0b41cdefdfb7; 837315f872e36916 differs in its header comment only (same cubin)
     "837315f872e36916": {"topk_prefill": 811_079_680 + 8_606_208 + 58_786_560 + 240_640},
