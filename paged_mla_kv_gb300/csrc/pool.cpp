@@ -203,7 +203,7 @@ extern "C" int tf_paged_append(tf_kvpool *p, int32_t cache, const int32_t *d_pt,
     if (cache < 0 || cache >= p->desc.num_caches) return TF_E_RANGE;
     if (!d_pt && (int64_t)S * max_pages > p->desc.num_pages) return TF_E_RANGE;
     for (int s = 0; s < S; ++s)
-        if (h_pos[s] < 0 || h_pos[s] + n > (int64_t)max_pages * kPageRows) return TF_E_RANGE;
+        if (h_pos[s] < 0 || h_pos[s] > (int64_t)max_pages * kPageRows - n) return TF_E_RANGE;
     if (n == 0) return TF_OK;
     if (is_fp8(p->desc))
         return launch_append_fp8(p, cache, d_pt, max_pages, h_pos, S, n, d_latent, d_rope, (cudaStream_t)stream);

@@ -195,6 +195,9 @@ def test_bad_arguments_are_refused_before_launch(L):
                          fake, None) == B.TF_E_RANGE
     assert _args_refused(L, h, L.tf_paged_append, 5, fake, 16, pos.ctypes.data_as(ctypes.c_void_p), 1, 1, fake,
                          fake, None) == B.TF_E_RANGE
+    huge = np.array([(1 << 63) - 1], np.int64)     # a position whose sum with n would overflow
+    assert _args_refused(L, h, L.tf_paged_append, 0, fake, 16, huge.ctypes.data_as(ctypes.c_void_p), 1, 2, fake,
+                         fake, None) == B.TF_E_RANGE
     # state copy: at past the pool, cache out of range
     assert _args_refused(L, h, L.tf_state_copy_rows, 0, fake, fake, 8 * 512 + 1, None) == B.TF_E_RANGE
     assert _args_refused(L, h, L.tf_state_copy_rows, 2, fake, fake, 10, None) == B.TF_E_RANGE
