@@ -53,8 +53,8 @@ size_t tf_topk_workspace_bytes(int64_t rows, int64_t n, int32_t k);
  * level; the levels are ordered on `stream`.
  *
  * Errors: TF_E_ARG for a null pointer, rows < 0, n < 0, ld < n, an unaligned d_logits or ld,
- * or k outside [1, TF_TOPK_MAX_K]; TF_E_UNSUPPORTED for n > INT32_MAX or more than INT32_MAX
- * blocks in a level; TF_E_NOMEM if ws_bytes is too small; TF_E_CUDA if a launch
+ * or k outside [1, TF_TOPK_MAX_K]; TF_E_UNSUPPORTED for n > INT32_MAX, rows > INT32_MAX or more
+ * than INT32_MAX blocks in a level; TF_E_NOMEM if ws_bytes is too small; TF_E_CUDA if a launch
  * fails.  rows == 0 (with valid sizes) launches nothing and may pass NULL pointers. */
 int tf_topk_blocked(const float *d_logits, int64_t rows, int64_t n, int64_t ld, const int32_t *d_len, int32_t k,
                     int32_t *d_idx, float *d_val, void *d_ws, size_t ws_bytes, void *stream);

@@ -690,7 +690,7 @@ extern "C" int tf_topk_blocked(const float *d_logits, int64_t rows, int64_t n, i
     if (rows == 0) return TF_OK;
     if (!d_logits || !d_idx || !d_val) return TF_E_ARG;
     if ((reinterpret_cast<uintptr_t>(d_logits) & 15u) || (ld & 3)) return TF_E_ARG;
-    if (n > INT32_MAX) return TF_E_UNSUPPORTED;
+    if (n > INT32_MAX || rows > INT32_MAX) return TF_E_UNSUPPORTED;
     const size_t need = tf_topk_workspace_bytes(rows, n, k);
     if (need && (!d_ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(d_ws) & 15u))) return TF_E_NOMEM;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

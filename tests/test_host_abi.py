@@ -250,3 +250,36 @@ def test_fp8_pool_sizes_and_workspace(L):
     bad = B.make_desc(1, 4)
     bad.flags = 8
     assert B.tf_kvpool_bytes(bad) == 0
+
+
+def test_topk_bad_arguments_are_refused_before_launch(L):
+    fake = ctypes.c_void_p(1 << 41)
+    T = L.tf_topk_blocked
+
+    def refused(*a):
+        before = L.tf_launch_count()
+        rc = T(*a)
+        assert L.tf_launch_count() == before
+        return rc
+
+    for k in (0, 2049):
+        assert refused(fake, 2, 64, 64, None, k, fake, fake, None, 0, None) == B.TF_E_ARG
+    assert refused(fake, -1, 64, 64, None, 8, fake, fake, None, 0, None) == B.TF_E_ARG        # rows < 0
+    assert refused(fake, 2, 64, 63, None, 8, fake, fake, None, 0, None) == B.TF_E_ARG         # ld < n
+    assert refused(fake, 2, 60, 62, None, 8, fake, fake, None, 0, None) == B.TF_E_ARG         # ld % 4
+    assert refused(ctypes.c_void_p((1 << 41) + 4), 2, 64, 64, None, 8, fake, fake, None, 0,
+                   None) == B.TF_E_ARG                                                          # unaligned
+    assert refused(None, 2, 64, 64, None, 8, fake, fake, None, 0, None) == B.TF_E_ARG         # null logits
+    assert refused(fake, 2, 64, 64, None, 8, fake, None, None, 0, None) == B.TF_E_ARG         # null values
+    # sizes the launch cannot number
+    assert refused(fake, 1 << 31, 64, 64, None, 8, fake, fake, fake, 1 << 62, None) == B.TF_E_UNSUPPORTED
+    assert refused(fake, 2, 1 << 31, 1 << 31, None, 8, fake, fake, fake, 1 << 62, None) == B.TF_E_UNSUPPORTED
+    # two levels need a workspace of the stated size
+    need = L.tf_topk_workspace_bytes(2, 40000, 8)
+    assert need == 2 * 3 * 8 * 8            # a row's 3 first-level blocks keep 8 (key, column) pairs each
+    # 17 blocks of 512 candidates need two merge blocks, then a last level: both lower levels are held
+    assert L.tf_topk_workspace_bytes(1, 17 * 16384, 512) == (17 + 2) * 512 * 8
+    assert refused(fake, 2, 40000, 40000, None, 8, fake, fake, None, 0, None) == B.TF_E_NOMEM
+    assert refused(fake, 2, 40000, 40000, None, 8, fake, fake, fake, need - 1, None) == B.TF_E_NOMEM
+    assert L.tf_topk_workspace_bytes(2, 16384, 8) == 0     # one block a row: a single level
+    assert refused(None, 0, 64, 64, None, 8, None, None, None, 0, None) == B.TF_OK            # no rows
