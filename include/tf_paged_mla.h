@@ -207,7 +207,8 @@ int tf_paged_append(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int32_t
  * 256-byte aligned, used for the split partials (fp32); it may be NULL only when
  * that size is 0.  Rows past h_len[s] are never read into the result (they may
  * hold NaN).  Limits: 1 <= S <= TF_MAX_STREAMS, 1 <= H <= TF_MAX_HEADS, scale a
- * finite number > 0 (TF_E_ARG otherwise). */
+ * finite number > 0 (TF_E_ARG otherwise); h_len[s] <= INT32_MAX (TF_E_UNSUPPORTED
+ * otherwise, and a workspace size of 0). */
 size_t tf_paged_mla_workspace_bytes(const tf_kvpool *pool, int32_t S, int32_t R, int32_t H,
                                     const int64_t *h_len);   /* pool may be NULL: default plan */
 
@@ -252,8 +253,8 @@ int tf_paged_mla_attend(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int
  * Each row is fetched through d_pt (or the contiguous windows of a NULL table) with TMA gathers.
  * A listed row outside [0, h_len[s]) or a table entry outside the pool is recorded as
  * TF_E_DEVICE and the call's output is undefined.  Limits: 1 <= h_nidx[s] <= max_idx, S and H as
- * for tf_paged_mla_attend; the pool must have fewer than 2^31 / 4,608 pages over all caches
- * (TF_E_UNSUPPORTED).  The keys are dealt out as in the default plan of tf_paged_mla_attend
+ * for tf_paged_mla_attend; h_len[s] <= INT32_MAX and the pool must have fewer than 2^31 / 4,608
+ * pages over all caches (TF_E_UNSUPPORTED otherwise).  The keys are dealt out as in the default plan of tf_paged_mla_attend
  * (whatever the pool's flags); d_ws holds the partials as there. */
 size_t tf_paged_mla_sparse_workspace_bytes(const tf_kvpool *pool, int32_t S, int32_t H, const int32_t *h_nidx);
 

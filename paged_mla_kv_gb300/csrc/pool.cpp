@@ -211,11 +211,15 @@ extern "C" int tf_paged_append(tf_kvpool *p, int32_t cache, const int32_t *d_pt,
 }
 
 // ---- attention ----
+// The launch numbers a stream's rows and key tiles in int32 (and listed rows are int32), so a
+// stream may hold at most INT32_MAX rows.  Only a table that repeats page ids can describe more.
+static constexpr int64_t kMaxStreamRows = INT32_MAX;
+
 extern "C" size_t tf_paged_mla_workspace_bytes(const tf_kvpool *p, int32_t S, int32_t R, int32_t H,
                                                const int64_t *h_len) {
     if (S < 1 || S > TF_MAX_STREAMS || R < 1 || H < 1 || H > TF_MAX_HEADS || !h_len) return 0;
     for (int s = 0; s < S; ++s)
-        if (h_len[s] < R) return 0;
+        if (h_len[s] < R || h_len[s] > kMaxStreamRows) return 0;
     const bool invariant = p && (p->desc.flags & TF_POOL_BATCH_INVARIANT);
     const size_t part = attend_workspace_bytes(invariant, S, R, H, h_len);
     // FP8 pages on a batch-invariant pool are expanded to bf16 in the workspace first
@@ -236,6 +240,8 @@ extern "C" int tf_paged_mla_attend(tf_kvpool *p, int32_t cache, const int32_t *d
     if ((int64_t)S * R * H > (int64_t)1 << 30) return TF_E_UNSUPPORTED;
     for (int s = 0; s < S; ++s)
         if (h_len[s] < R || h_len[s] > (int64_t)max_pages * kPageRows) return TF_E_RANGE;
+    for (int s = 0; s < S; ++s)
+        if (h_len[s] > kMaxStreamRows) return TF_E_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(d_q) & 15u) != 0 || (reinterpret_cast<uintptr_t>(d_out) & 15u) != 0)
         return TF_E_ARG;
     const bool invariant = (p->desc.flags & TF_POOL_BATCH_INVARIANT) != 0;
@@ -282,6 +288,8 @@ extern "C" int tf_paged_mla_attend_sparse(tf_kvpool *p, int32_t cache, const int
     if (!d_pt && (int64_t)S * max_pages > p->desc.num_pages) return TF_E_RANGE;
     for (int s = 0; s < S; ++s)
         if (h_len[s] < 1 || h_len[s] > (int64_t)max_pages * kPageRows) return TF_E_RANGE;
+    for (int s = 0; s < S; ++s)
+        if (h_len[s] > kMaxStreamRows) return TF_E_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(d_q) & 15u) != 0 || (reinterpret_cast<uintptr_t>(d_out) & 15u) != 0)
         return TF_E_ARG;
     int64_t n[TF_MAX_STREAMS];

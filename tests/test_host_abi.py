@@ -189,6 +189,17 @@ def test_bad_arguments_are_refused_before_launch(L):
     assert _args_refused(L, h, A, 0, fake, 16, lp, 2, 1, 16, fake, 0.1, fake, None, None, 0, None) == B.TF_E_ARG
     assert _args_refused(L, h, A, 0, fake, 16, lp, 2, 1, 16, fake, 0.1, fake, None, fake, need - 1,
                          None) == B.TF_E_NOMEM
+    # a stream longer than INT32_MAX rows (only a table that repeats page ids can hold one)
+    long_ = np.array([(1 << 31) + 7, 5000], np.int64)
+    wide = (1 << 31) // 512 + 1
+    lq = long_.ctypes.data_as(ctypes.c_void_p)
+    assert _args_refused(L, h, A, 0, fake, wide, lq, 2, 1, 16, fake, 0.1, fake, None, fake, 1 << 40,
+                         None) == B.TF_E_UNSUPPORTED
+    assert L.tf_paged_mla_workspace_bytes(h, 2, 1, 16, lq) == 0
+    nidx = np.array([8, 8], np.int32)
+    assert _args_refused(L, h, L.tf_paged_mla_attend_sparse, 0, fake, wide, lq, fake, 8,
+                         nidx.ctypes.data_as(ctypes.c_void_p), 2, 16, fake, 0.1, fake, None, fake, 1 << 40,
+                         None) == B.TF_E_UNSUPPORTED
     # append: position past the table
     pos = np.array([16 * 512 - 1], np.int64)
     assert _args_refused(L, h, L.tf_paged_append, 0, fake, 16, pos.ctypes.data_as(ctypes.c_void_p), 1, 2, fake,
