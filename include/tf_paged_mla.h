@@ -93,8 +93,8 @@ typedef struct tf_kvpool tf_kvpool;
  * starts at dev_base + (c * num_pages + p) * page_bytes.  A page id names the same
  * page in every cache (a token's rows in all caches live under one id). */
 typedef struct {
-    int32_t num_caches;  /* >= 1 (12 for 11 MLA layers plus the MTP layer) */
-    int32_t num_pages;   /* >= 1 */
+    int32_t num_caches;  /* 1 .. 65,535 (12 for 11 MLA layers plus the MTP layer) */
+    int32_t num_pages;   /* >= 1; num_caches * num_pages < 2^31 */
     int32_t page_rows;   /* must be 512 */
     int32_t latent_dim;  /* must be 512 */
     int32_t rope_dim;    /* must be 64 */

@@ -39,6 +39,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <memory>
 #include <mutex>
 #include <numeric>
 
@@ -1248,18 +1249,18 @@ size_t attend_workspace_bytes(bool invariant, int S, int R, int H, const int64_t
     return o + ((ml + 255) & ~size_t(255));
 }
 
+// The driver's tensor-map encoder, looked up once: a function-local static is initialised
+// exactly once even when several host threads make their first call together.
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *f = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
     return fn;
 }
 
@@ -1377,8 +1378,8 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     if (rc != TF_OK) return rc;
 
     // Params is large (tensor maps + the per-stream plan); keep one per host thread.
-    thread_local Params *pp = nullptr;
-    if (!pp) pp = new Params();
+    thread_local std::unique_ptr<Params> pp;
+    if (!pp) pp.reset(new Params());
     Params &p = *pp;
     p.tm_lat = pool->tm_lat[0];
     p.tm_rope = pool->tm_rope[0];

@@ -42,7 +42,9 @@ ProfScope::~ProfScope() {
 using namespace tf;
 
 static bool desc_ok(const tf_kvpool_desc *d) {
-    return d && d->num_caches >= 1 && d->num_pages >= 1 && d->page_rows == kPageRows && d->latent_dim == kLat &&
+    // the poison and state-copy launches put the caches on the grid's y dimension (at most 65,535)
+    return d && d->num_caches >= 1 && d->num_caches <= 65535 && d->num_pages >= 1 && d->page_rows == kPageRows &&
+           d->latent_dim == kLat &&
            d->rope_dim == kRope && (d->flags & ~(TF_POOL_POISON | TF_POOL_BATCH_INVARIANT | TF_POOL_FP8)) == 0 &&
            (uint64_t)d->num_caches * (uint64_t)d->num_pages < (1ull << 31);
 }

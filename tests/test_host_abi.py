@@ -66,6 +66,9 @@ def test_pool_bytes_and_descriptor_checks(L):
     bad = B.make_desc(1, 16)
     bad.page_rows = 256
     assert B.tf_kvpool_bytes(bad) == 0
+    assert B.tf_kvpool_bytes(B.make_desc(65535, 1)) == 65535 * 589824 + 256
+    assert B.tf_kvpool_bytes(B.make_desc(65536, 1)) == 0      # caches are a launch's grid.y
+    assert B.tf_kvpool_bytes(B.make_desc(2, 1 << 30)) == 0    # 2^31 pages over all caches
     h = ctypes.c_void_p()
     good = B.make_desc(1, 16)
     n = B.tf_kvpool_bytes(good)
