@@ -87,6 +87,36 @@ def test_matches_scipy_softmax_for_the_last_row(seed):
             assert lse[r * H + h] == pytest.approx(logsumexp(s), rel=1e-12)
 
 
+def test_matches_a_40_digit_evaluation_of_the_definition():
+    """Every output of a tiny causal case (two rows, two heads, 19 keys) against the definition
+    evaluated in 40-digit arithmetic with mpmath, no numpy on that side: scores as the two dot
+    products, max-shifted exponentials, their sum, the weighted latent mean and the log-sum-exp.
+    The fp64 oracle must agree to 1e-12 of the output's size, far inside any kernel tolerance."""
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 40
+    n, R, H = 19, 2, 2
+    q, lat, rope = rand_case(11, n, R, H, std=1.0, qstd=1.0)
+    scale = 1 / math.sqrt(576)
+    out, lse = attend_stream(q, lat, rope, scale)
+    C = [[mp.mpf(float(v)) for v in row] for row in wide(lat)]
+    Kr = [[mp.mpf(float(v)) for v in row] for row in wide(rope)]
+    sc = mp.mpf(scale)                       # the same double the oracle is given
+    for r in range(R):
+        p_ = n - R + r                        # the row's position: it sees keys 0 .. p_
+        for h in range(H):
+            qq = [mp.mpf(float(v)) for v in wide(q[r, h])]
+            s = [sc * (mp.fsum(qq[d] * C[j][d] for d in range(512)) +
+                       mp.fsum(qq[512 + e] * Kr[j][e] for e in range(64))) for j in range(p_ + 1)]
+            m = max(s)
+            ex = [mp.exp(x - m) for x in s]
+            Z = mp.fsum(ex)
+            want = [float(mp.fsum(ex[j] * C[j][d] for j in range(p_ + 1)) / Z) for d in range(512)]
+            got = out[r * H + h]
+            size = max(1.0, max(abs(w) for w in want))
+            assert max(abs(w - g) for w, g in zip(want, got)) <= 1e-12 * size, (r, h)
+            assert abs(float(m + mp.log(Z)) - lse[r * H + h]) <= 1e-12 * max(1.0, abs(float(m))), (r, h)
+
+
 def test_items_select_row_and_head():
     n, R, H = 40, 2, 3
     q, lat, rope = rand_case(6, n, R, H)
