@@ -99,6 +99,20 @@ def ncu_traffic(workload: str, source: str = "attend.cu"):
     return NCU_TRAFFIC.get(key, {}).get(workload)
 
 
+def read_kernel_times(pool) -> dict:
+    """(total ms, launches) of each launch kind the library recorded while the pool's profiling
+    was on (CUDA events around each launch, on its stream); reading clears the records."""
+    from paged_mla_kv_gb300 import binding as B
+    kinds = {"append": B.PROF_APPEND, "attend": B.PROF_ATTEND, "combine": B.PROF_COMBINE,
+             "state_copy": B.PROF_COPY, "poison": B.PROF_POISON}
+    return {name: pool.profile_read(kind) for name, kind in kinds.items()}
+
+
+def kernels_per_step(times: dict, steps: int) -> dict:
+    """Device ms and launches a step of every launch kind that ran."""
+    return {name: {"ms": t / steps, "launches": n / steps} for name, (t, n) in times.items() if n}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -509,17 +523,20 @@ def main():
         barrier()
         total_ms = sum(a.elapsed_time(b) for a, b in ev)
     launches = B.tf_launch_count() - n0
-    # the attention kernel's own duration: CUDA events around each of its launches, on
-    # its stream, in a second pass of the same steps (the events cost ~15 us a step and
-    # serialise the launches, so they stay out of the timed region above)
+    # each kernel's own duration (the attention's for the roofline; every kind for
+    # "kernels_per_step"): CUDA events around each launch, on its stream, in a second pass of
+    # the same steps (the events cost ~15 us a step and serialise the launches, so they stay
+    # out of the timed region above, and the kinds' times may add up to more than a step)
     res.pool.profile(True)
-    res.pool.profile_read(B.PROF_ATTEND)
-    for i in range(min(args.steps, 200)):
+    read_kernel_times(res.pool)
+    nprof = min(args.steps, 200)
+    for i in range(nprof):
         if flush is not None:
             flush.zero_()
         step()
     barrier()
-    att_ms, att_n = res.pool.profile_read(B.PROF_ATTEND)
+    times = read_kernel_times(res.pool)
+    att_ms, att_n = times["attend"]
     res.pool.profile(False)
     clocks = sampler.stop() if sampler else None
     rc, detail = res.pool.last_error()
@@ -647,7 +664,7 @@ def main():
                            "l2": "flushed between steps" if flush is not None else "inputs larger than L2",
                            "parallelism": f"replicas x{world}", "tokens_per_step": units["tokens"]},
                 "tokens_per_s": tokens_s, "gpu_launches": launches, "roofline": roof, "cpu_baseline": cpu,
-                "e2e": e2e, "clocks": clocks}
+                "e2e": e2e, "clocks": clocks, "kernels_per_step": kernels_per_step(times, nprof)}
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()

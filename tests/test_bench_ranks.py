@@ -49,3 +49,22 @@ def test_two_gloo_ranks_agree_on_the_slowest_time():
 def test_single_rank_needs_no_group():
     assert bench.max_over_ranks(4.25) == 4.25
     assert bench.whole_job_rate(10.0, 1, 2.0) == pytest.approx(5000.0)
+
+
+def test_kernel_times_read_every_kind_and_scale_per_step():
+    """The bench's per-kind kernel times: every launch kind is read (and cleared) from the pool's
+    records, and only kinds that ran appear, per step.  The pool sits over host bytes it never
+    touches; with nothing recorded no CUDA call is made."""
+    from paged_mla_kv_gb300 import binding as B
+    from paged_mla_kv_gb300 import build as BUILD
+    BUILD.build()
+    mem = torch.empty(B.tf_kvpool_bytes(B.make_desc(1, 4)) + 1024, dtype=torch.uint8)
+    pool = B.KVPool(1, 4, memory=mem)
+    pool.profile(True)
+    t = bench.read_kernel_times(pool)
+    assert set(t) == {"append", "attend", "combine", "state_copy", "poison"}
+    assert all(v == (0.0, 0) for v in t.values())
+    assert bench.kernels_per_step(t, 10) == {}
+    got = bench.kernels_per_step({"attend": (5.0, 20), "append": (1.0, 10), "combine": (0.0, 0)}, 10)
+    assert got == {"attend": {"ms": 0.5, "launches": 2.0}, "append": {"ms": 0.1, "launches": 1.0}}
+    pool.close()
