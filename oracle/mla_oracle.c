@@ -46,7 +46,7 @@ static double widen(uint16_t b)
  * One stream.  q: [R][H][576] bf16 bits; lat: [len][512]; rope: [len][64]
  * (contiguous logical rows).  items: n_items indices r*H + h to evaluate.
  * out: [n_items][512] doubles; lse: [n_items] doubles.
- * Returns 0, or -1 on a bad argument (a row with no visible key).
+ * Returns 0, or -1 on a bad argument (a row with no visible key, an item outside [0, R*H)).
  */
 static int attend_core(int64_t len, int32_t R, int32_t H,
                        const uint16_t *q, const uint16_t *lat, const double *latd, const uint16_t *rope,
@@ -85,8 +85,8 @@ static int attend_core(int64_t len, int32_t R, int32_t H,
     int bad = 0;
 #pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads > 0 ? n_threads : 1) reduction(| : bad)
     for (int32_t it = 0; it < n_items; ++it) {
+        if (items[it] < 0 || (int64_t)items[it] >= (int64_t)R * H) { bad = 1; continue; }
         int32_t r = items[it] / H, h = items[it] % H;
-        if (r < 0 || r >= R) { bad = 1; continue; }
         int64_t p = len - R + r;               /* this row's position: keys 0..p are visible */
         int64_t nk = p + 1;
         double qd[DK];

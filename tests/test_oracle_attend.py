@@ -194,6 +194,13 @@ def test_rejects_rows_without_keys():
         attend_stream(q, lat, rope, 1.0)
 
 
+def test_rejects_items_outside_the_rows_and_heads():
+    q, lat, rope = rand_case(10, 8, 2, 3)
+    for bad in (-1, 6):                       # r*H + h must lie in [0, R*H)
+        with pytest.raises(ValueError):
+            attend_stream(q, lat, rope, 1.0, items=[0, bad])
+
+
 # ---------------------------------------------------------------- listed rows (sparse)
 
 
