@@ -3,8 +3,9 @@
  *
  * The problem, as the TensorFold pages state it:
  *  - each token's cache row is 512 bf16 latent values plus a 64-value bf16 rope
- *    key (issue #1142, "What happens now": 12 caches x (1,024 + 64) bytes; the
- *    spec reading stores the rope key as 64 bf16, i.e. 1,152 B a row);
+ *    key (issue #1142, "What happens now": 12 caches x (1,024 + 64) bytes; 64 bytes
+ *    cannot hold 64 bf16 values, so the rope key is stored as 64 bf16 and a row of
+ *    one cache is 1,152 B);
  *  - rows sit in 512-row pages taken from one shared pool; a stream maps its
  *    logical pages to pool pages through a page table, and the cache kernels take
  *    that table plus the elements between pages (issue #1142, "GLM declares a
@@ -110,23 +111,28 @@ size_t tf_kvpool_bytes(const tf_kvpool_desc *desc);
 /* Make a pool over caller memory dev_base (>= tf_kvpool_bytes, 1024-byte aligned).
  * All pages start free with refcount 0.  Touches no device memory: the device
  * error word is zeroed, asynchronously, on the stream of the pool's first launch.
- * On success *out owns host state only; the device memory stays the caller's. */
+ * On success *out owns host state only; the device memory stays the caller's.
+ * TF_E_ARG for a null pointer, an invalid descriptor or an unaligned dev_base;
+ * TF_E_NOMEM if dev_bytes < tf_kvpool_bytes(desc). */
 int tf_kvpool_create(const tf_kvpool_desc *desc, void *dev_base, size_t dev_bytes, tf_kvpool **out);
 
-/* Free the host state.  The device memory is untouched. */
+/* Free the host state.  The device memory is untouched.  TF_E_ARG for NULL. */
 int tf_kvpool_destroy(tf_kvpool *pool);
 
 /* Take n free pages (refcount 1) into h_ids_out[n].  With TF_POOL_POISON the taken
  * pages of every cache are NaN-filled on cuda_stream before the call returns
- * (asynchronously).  TF_E_NOMEM, and nothing taken, if fewer than n are free. */
+ * (asynchronously).  TF_E_NOMEM, and nothing taken, if fewer than n are free;
+ * TF_E_ARG for n < 0 or a null h_ids_out with n > 0. */
 int tf_kvpool_take(tf_kvpool *pool, int32_t n, int32_t *h_ids_out, void *cuda_stream);
 
 /* Add one reference to each of n taken pages: a kept state or a second stream
- * holding a prefix page (PR #1732: kept states hold prefix pages by reference). */
+ * holding a prefix page (PR #1732: kept states hold prefix pages by reference).
+ * TF_E_RANGE, and nothing changed, if any id is not taken; TF_E_ARG as for take. */
 int tf_kvpool_ref(tf_kvpool *pool, const int32_t *h_ids, int32_t n);
 
 /* Drop one reference from each of n pages; a page whose count reaches 0 is free
- * again.  TF_E_RANGE, and nothing changed, if any id is not taken. */
+ * again.  TF_E_RANGE, and nothing changed, if any id is not taken (an id listed
+ * k times must hold k references); TF_E_ARG as for take. */
 int tf_kvpool_release(tf_kvpool *pool, const int32_t *h_ids, int32_t n);
 
 /* Free pages now, and one page's reference count (-1 for a bad id). */
@@ -143,7 +149,9 @@ void *tf_kvpool_page_ptr(const tf_kvpool *pool, int32_t cache, int32_t page);
  * holds, n = min(lanes, 1 + (room - window) / (window + fixed)), at least one,
  * the streams holding max(n windows, one window + lanes - 1 pages); then each
  * other stream's fixed bytes; then the prompt cache up to its budget; then the
- * remaining room as more pages.  TF_E_NOMEM if the room cannot hold the streams. */
+ * remaining room as more pages.  TF_E_NOMEM if the room cannot hold the streams;
+ * TF_E_ARG for a null pointer, a negative byte count, budget or lookahead, or a
+ * context, lanes, page_rows or bytes_per_token below 1. */
 typedef struct {
     int64_t room_bytes;
     int64_t context_tokens;
@@ -175,8 +183,13 @@ int tf_kvpool_plan(const tf_plan_in *in, tf_plan_out *out);
  * d_pt: int32 [S][max_pages] device table, or NULL for contiguous windows
  * (stream s's logical page j is pool page s * max_pages + j).
  * h_pos: host int64 [S]; every pos + n must be <= max_pages * 512.
+ * d_latent and d_rope must be 16-byte aligned.
  * A table entry outside [0, num_pages) is recorded as TF_E_DEVICE and that row
- * is skipped.  Bit-exact: the bytes are copied, never converted. */
+ * is skipped.  Bit-exact: the bytes are copied, never converted (FP8 pools quantize).
+ * Errors: TF_E_ARG for a null pool or h_pos, S outside [1, TF_MAX_STREAMS], n < 0,
+ * max_pages < 1, null or unaligned row buffers with n > 0; TF_E_RANGE for a cache
+ * outside the pool, a position outside the table, or a NULL table wider than the
+ * pool (S * max_pages > num_pages).  n == 0 launches nothing. */
 int tf_paged_append(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int32_t max_pages,
                     const int64_t *h_pos, int32_t S, int32_t n,
                     const void *d_latent, const void *d_rope, void *cuda_stream);
@@ -207,8 +220,11 @@ int tf_paged_append(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int32_t
  * 256-byte aligned, used for the split partials (fp32); it may be NULL only when
  * that size is 0.  Rows past h_len[s] are never read into the result (they may
  * hold NaN).  Limits: 1 <= S <= TF_MAX_STREAMS, 1 <= H <= TF_MAX_HEADS, scale a
- * finite number > 0 (TF_E_ARG otherwise); h_len[s] <= INT32_MAX (TF_E_UNSUPPORTED
- * otherwise, and a workspace size of 0). */
+ * finite number > 0, d_q and d_out 16-byte aligned (TF_E_ARG otherwise); h_len[s] <=
+ * INT32_MAX (TF_E_UNSUPPORTED otherwise, and a workspace size of 0).  TF_E_RANGE for a
+ * cache outside the pool, a length below R or past the table, or a NULL table wider than
+ * the pool; TF_E_NOMEM for a workspace smaller than needed (TF_E_ARG if it is NULL or
+ * not 256-byte aligned). */
 size_t tf_paged_mla_workspace_bytes(const tf_kvpool *pool, int32_t S, int32_t R, int32_t H,
                                     const int64_t *h_len);   /* pool may be NULL: default plan */
 
@@ -252,8 +268,8 @@ int tf_paged_mla_attend(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int
  * not read.  d_q: bf16 [S][H][576]; d_out: bf16 [S][H][512]; d_lse: fp32 [S][H] or NULL.
  * Each row is fetched through d_pt (or the contiguous windows of a NULL table) with TMA gathers.
  * A listed row outside [0, h_len[s]) or a table entry outside the pool is recorded as
- * TF_E_DEVICE and the call's output is undefined.  Limits: 1 <= h_nidx[s] <= max_idx, S and H as
- * for tf_paged_mla_attend; h_len[s] <= INT32_MAX and the pool must have fewer than 2^31 / 4,608
+ * TF_E_DEVICE and the call's output is undefined.  Limits: 1 <= h_nidx[s] <= max_idx (TF_E_RANGE
+ * otherwise), S, H, scale, alignment, lengths and workspace as for tf_paged_mla_attend; h_len[s] <= INT32_MAX and the pool must have fewer than 2^31 / 4,608
  * pages over all caches (TF_E_UNSUPPORTED otherwise).  The keys are dealt out as in the default plan of tf_paged_mla_attend
  * (whatever the pool's flags); d_ws holds the partials as there. */
 size_t tf_paged_mla_sparse_workspace_bytes(const tf_kvpool *pool, int32_t S, int32_t H, const int32_t *h_nidx);
@@ -272,7 +288,9 @@ int tf_paged_mla_attend_static(tf_kvpool *pool, int32_t cache, const int32_t *d_
  * Copies rows [0, at) of cache `cache` (every cache when cache < 0) from the
  * pages d_src_pages[0 .. ceil(at/512)) to the pages d_dst_pages[same], row for
  * row.  Rows at and past `at` of the last page are neither read nor written.
- * Page ids outside the pool are recorded as TF_E_DEVICE and skipped.  Bit-exact. */
+ * Page ids outside the pool are recorded as TF_E_DEVICE and skipped.  Bit-exact.
+ * TF_E_ARG for a null pool, at < 0, or null tables with at > 0; TF_E_RANGE for a
+ * cache >= num_caches or at > num_pages * 512.  at == 0 launches nothing. */
 int tf_state_copy_rows(tf_kvpool *pool, int32_t cache, const int32_t *d_src_pages,
                        const int32_t *d_dst_pages, int64_t at, void *cuda_stream);
 
