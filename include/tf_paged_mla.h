@@ -52,7 +52,7 @@ extern "C" {
 #define TF_E_NOMEM (-3)        /* the pool has too few free pages, or a buffer is too small */
 #define TF_E_CUDA (-4)         /* a CUDA runtime or driver call failed */
 #define TF_E_TIMEOUT (-5)      /* a kernel's bounded wait ran out (device error word) */
-#define TF_E_UNSUPPORTED (-6)  /* a shape this build does not handle */
+#define TF_E_UNSUPPORTED (-6)  /* a shape this library does not handle */
 #define TF_E_DEVICE (-7)       /* a kernel met a bad page id (device error word) */
 
 #define TF_PAGE_ROWS 512
