@@ -297,3 +297,56 @@ def test_topk_bad_arguments_are_refused_before_launch(L):
     assert refused(fake, 2, 40000, 40000, None, 8, fake, fake, fake, need - 1, None) == B.TF_E_NOMEM
     assert L.tf_topk_workspace_bytes(2, 16384, 8) == 0     # one block a row: a single level
     assert refused(None, 0, 64, 64, None, 8, None, None, None, 0, None) == B.TF_OK            # no rows
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include "tf_paged_mla.h"
+#include "tf_topk.h"
+
+int main(void)
+{
+    /* the plan of a TP=2 pair at a 1M window with 8 lanes (the pages' worked example) */
+    const int64_t GiB = (int64_t)1 << 30, MiB = (int64_t)1 << 20;
+    tf_plan_in in = {0};
+    tf_plan_out out = {0};
+    in.room_bytes = (int64_t)(2.33 * (double)GiB + 0.5) + (int64_t)1048576 * 13056 + 180 * MiB;
+    in.context_tokens = 1048576;
+    in.lanes = 8;
+    in.page_rows = TF_PAGE_ROWS;
+    in.lookahead = 1;
+    in.engine_paged = 0;
+    in.bytes_per_token = 13056;
+    in.fixed_bytes = 180 * MiB;
+    in.cache_budget_bytes = 16 * GiB;
+    if (tf_kvpool_plan(&in, &out) != TF_OK) return 1;
+    tf_kvpool_desc d = {12, 1344, TF_PAGE_ROWS, TF_LATENT_DIM, TF_ROPE_DIM, 0u, 0u};
+    tf_kvpool_desc f = d;
+    f.flags = TF_POOL_FP8;
+    tf_kvpool *pool = NULL;
+    int rc = tf_kvpool_create(&d, (void *)0, 0, &pool);   /* a null base is refused */
+    printf("%lld %lld %zu %zu %zu %d %d\n", (long long)out.pool_pages, (long long)out.pool_tokens,
+           tf_kvpool_bytes(&d), tf_kvpool_bytes(&f), tf_topk_workspace_bytes(2, 40000, 8), rc, pool == NULL);
+    return 0;
+}
+"""
+
+
+def test_headers_compile_as_c_and_the_library_links_from_c(L, tmp_path):
+    """The C ABI as a C caller sees it: both headers compile as strict C99 with every warning an
+    error, and a C program linked to the library gets the same answers as the binding."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(B.LIB_PATH)
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), "-L", libdir, "-ltf_paged_mla", "-Wl,-rpath," + libdir],
+                   check=True, capture_output=True, text=True)
+    got = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    want = [2056, 1052672, 12 * 1344 * 589824 + 256, 12 * 1344 * 329728 + 256, 2 * 3 * 8 * 8, B.TF_E_ARG, 1]
+    assert [int(x) for x in got] == want
