@@ -207,11 +207,13 @@ class ClockSampler:
 class OracleSample:
     """The oracle, as it stands, timed on a bounded sample of the workload.
 
-    Decode: the first k heads of every stream (all query rows); a stream's rows
-    count once for all its heads, scaled by k / H, so the rate is in KV GB/s.
-    Prefill: n query rows spread over the chunk, all heads; the rate is in
-    TFLOP/s of the causal (row, key) pairs computed.  k or n is calibrated once
-    so that a sample takes about `seconds` on all host cores."""
+    The workload is cut into items, one (stream, query row, head) each, and the sample is the
+    k cheapest items (a stream's items in head order; ties in stream, row, head order).  The
+    rate is the sample's work over its time: in KV GB/s for decode (a stream's key rows count
+    once for all its heads and rows, so an item carries 1/(R*H) of them; for listed rows the
+    listed rows), in TFLOP/s of causal (row, key) pairs for a prefill chunk.  k is calibrated
+    once so that a sample takes about `seconds` on the host cores; the smallest sample is one
+    item, so a step can be made as short as the run's number of steps needs."""
 
     def __init__(self, w, seconds: float):
         from oracle import attend as OA
@@ -233,49 +235,55 @@ class OracleSample:
             from paged_mla_kv_gb300 import synth as Y
             self.rows = [(F.dequantize_rows(*F.quantize_rows(Y.bf16_bits_to_f32(a))), b) for a, b in self.rows]
             self.row_bytes = 644
-        k0 = min(w.R if self.prefill else w.H, max(1, self.threads // (w.R if not self.prefill else 1)))
-        k0 = max(1, min(k0, self.threads))
-        t0, _ = self.run(k0)
-        lim = w.R if self.prefill else w.H
-        self.k = int(max(1, min(lim, k0 * seconds / max(t0, 1e-3))))
-
-    def items(self, k):
-        w = self.w
-        if self.prefill:
-            rows = np.unique(np.linspace(0, w.R - 1, k).round().astype(int))
-            return rows, np.array([r * w.H + h for r in rows for h in range(w.H)], np.int32)
-        return None, np.array([r * w.H + h for r in range(w.R) for h in range(k)], np.int32)
+        # items (work, stream, row, head), cheapest first
+        its = []
+        for s in range(w.S):
+            L = int(w.lens[s])
+            for r in range(w.R):
+                keys = len(self.lists[s]) if self.lists is not None else L - w.R + r + 1
+                if self.prefill:
+                    work = 2.0 * 1088 * keys
+                else:
+                    nrows = len(self.lists[s]) if self.lists is not None else L
+                    work = nrows * self.row_bytes / (w.R * w.H)
+                for h in range(w.H):
+                    its.append((work, keys, s, r, h))
+        its.sort(key=lambda x: (x[1], x[2], x[4], x[3]))
+        self.its = [(wk, s, r, h) for wk, _, s, r, h in its]
+        # calibrate on the cheapest items: the rate, then the longest prefix of items whose work
+        # fits `seconds` at that rate (items differ in cost by the stream's length)
+        k0 = min(len(self.its), max(1, self.threads))
+        t0, w0 = self.run(k0)
+        budget = w0 / max(t0, 1e-4) * seconds
+        cum = np.cumsum([x[0] for x in self.its])
+        self.k = int(max(1, min(len(self.its), np.searchsorted(cum, budget, side="right"))))
 
     def run(self, k):
         w = self.w
-        rows, items = self.items(k)
+        chosen = self.its[:k]
+        by_stream = {}
+        for wk, s, r, h in chosen:
+            by_stream.setdefault(s, []).append(r * w.H + h)
         t0 = time.perf_counter()
-        work = 0.0
-        if self.prefill:
-            self.OA.attend_stream(self.q[0], self.rows[0][0], self.rows[0][1], w.scale, items, self.threads)
-            work = sum(2 * 1088 * (int(w.lens[0]) - w.R + int(r) + 1) for r in rows) * w.H
-        elif self.lists is not None:
-            for s in range(w.S):
-                self.OA.attend_sparse(self.q[s, 0, :k], self.rows[s][0], self.rows[s][1], self.lists[s], w.scale,
-                                      self.threads)
-                work += len(self.lists[s]) * self.row_bytes * k / w.H
-        else:
-            for s in range(w.S):
-                self.OA.attend_stream(self.q[s], self.rows[s][0], self.rows[s][1], w.scale, items, self.threads)
-                work += int(w.lens[s]) * self.row_bytes * k / w.H
-        return time.perf_counter() - t0, work
+        for s, items in by_stream.items():
+            if self.lists is not None:   # R = 1; a stream's items are its first heads
+                self.OA.attend_sparse(self.q[s, 0, :len(items)], self.rows[s][0], self.rows[s][1], self.lists[s],
+                                      w.scale, self.threads)
+            else:
+                self.OA.attend_stream(self.q[s], self.rows[s][0], self.rows[s][1], w.scale,
+                                      np.array(items, np.int32), self.threads)
+        return time.perf_counter() - t0, sum(x[0] for x in chosen)
 
     def measure(self):
         t, work = self.run(self.k)
         w = self.w
+        streams = len({s for _, s, _, _ in self.its[:self.k]})
+        cores = min(self.threads, max(1, self.k))
+        what = (f"the {self.k} cheapest of {len(self.its)} (stream, row, head) items ({streams} of {w.S} streams"
+                f"{', listed rows' if self.lists is not None else ''}), cache 0 ({t:.2f} s)")
         if self.prefill:
-            rows, _ = self.items(self.k)
-            return dict(value=work / t / 1e12, unit="TFLOP/s", cores=self.threads, kind="oracle",
-                        sample=f"{len(rows)} of {w.R} query rows spread over the chunk, all {w.H} heads, "
-                               f"cache 0 ({t:.1f} s)")
-        what = "listed rows" if self.lists is not None else f"all {w.R} rows"
-        return dict(value=work / t / 1e9, unit="GB/s", cores=self.threads, kind="oracle",
-                    sample=f"first {self.k} of {w.H} heads of all {w.S} streams, {what}, cache 0 ({t:.1f} s)")
+            return dict(value=work / t / 1e12, unit="TFLOP/s", cores=cores, kind="oracle", sample=what)
+        return dict(value=work / t / 1e9, unit="GB/s", cores=cores, kind="oracle", sample=what)
 
 
 class TopkOracleSample:
@@ -314,30 +322,42 @@ def reference_arm(args, rank, world):
     if args.workload in TOPK:
         from paged_mla_kv_gb300 import synth as Y
         w = Y.TOPK_WORKLOADS[args.workload]()
-        o = TopkOracleSample(w, min(20.0, max(1.0, 150.0 / max(1, args.steps + args.warmup))))
+        o = TopkOracleSample(w, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
         for _ in range(args.warmup):
             o.run(o.n)
         vals = [o.measure() for _ in range(args.steps)]
         v = statistics.median(x["value"] for x in vals)
+        scanned = 4.0 * float(np.sum(w.lens))   # the logits in play, the sample's unit of work
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": {"workload": w.name, "rows": w.rows, "n": w.n, "k": w.k},
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": scanned / (v * 1e9) * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic",
+                "config": {"workload": w.name, "rows": w.rows, "n": w.n, "k": w.k, "lens_sum": int(np.sum(w.lens)),
+                           "parallelism": "one host core"},
                 "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": vals[0]["sample"], "value": v},
                 "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
     w = make_workload(args.workload)
-    per_step = min(20.0, max(1.0, 150.0 / max(1, args.steps + args.warmup)))
+    per_step = min(20.0, 150.0 / max(1, args.steps + args.warmup))   # ~150 s for the whole run
     o = OracleSample(w, per_step)
     for _ in range(args.warmup):
         o.run(o.k)
     vals = [o.measure() for _ in range(args.steps)]
     v = statistics.median(x["value"] for x in vals)
+    units = step_units(w)
+    # ms_per_step: the whole workload's step at the sample's rate (flops of a prefill chunk; the
+    # key rows of every cache for decode)
+    if vals[0]["unit"] == "TFLOP/s":
+        ms = units["flops"] / (v * 1e12) * 1e3
+    else:
+        ms = w.num_caches * units["kv"] / (v * 1e9) * 1e3
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": vals[0]["unit"], "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "S": w.S, "R": w.R, "H": w.H, "caches": w.num_caches},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "S": w.S, "R": w.R, "H": w.H, "caches": w.num_caches,
+                       "lens_sum": int(np.sum(w.lens)), "kv_bytes": units["kv"], "tokens_per_step": units["tokens"],
+                       "parallelism": f"host cores x{vals[0]['cores']}"},
             "cpu_baseline": {"kind": "oracle", "cores": vals[0]["cores"], "sample": vals[0]["sample"], "value": v},
             "e2e": {"value": v, "unit": vals[0]["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
