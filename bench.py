@@ -315,6 +315,9 @@ class TopkOracleSample:
                            f"one numpy sort a row)")
 
 
+REFERENCE_SECONDS = 150.0   # the reference arm's whole run, warm-up included, on the host cores
+
+
 def reference_arm(args, rank, world):
     """The oracle timed as the reference arm (host cores, the same bounded sample each step)."""
     if rank != 0:
@@ -322,7 +325,7 @@ def reference_arm(args, rank, world):
     if args.workload in TOPK:
         from paged_mla_kv_gb300 import synth as Y
         w = Y.TOPK_WORKLOADS[args.workload]()
-        o = TopkOracleSample(w, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+        o = TopkOracleSample(w, min(20.0, REFERENCE_SECONDS / max(1, args.steps + args.warmup)))
         for _ in range(args.warmup):
             o.run(o.n)
         vals = [o.measure() for _ in range(args.steps)]
@@ -339,7 +342,7 @@ def reference_arm(args, rank, world):
         print(json.dumps(line), flush=True)
         return
     w = make_workload(args.workload)
-    per_step = min(20.0, 150.0 / max(1, args.steps + args.warmup))   # ~150 s for the whole run
+    per_step = min(20.0, REFERENCE_SECONDS / max(1, args.steps + args.warmup))
     o = OracleSample(w, per_step)
     for _ in range(args.warmup):
         o.run(o.k)

@@ -68,3 +68,25 @@ def test_kernel_times_read_every_kind_and_scale_per_step():
     got = bench.kernels_per_step({"attend": (5.0, 20), "append": (1.0, 10), "combine": (0.0, 0)}, 10)
     assert got == {"attend": {"ms": 0.5, "launches": 2.0}, "append": {"ms": 0.1, "launches": 1.0}}
     pool.close()
+
+
+@pytest.mark.parametrize("workload", ["tiny_decode", "topk_prefill"])
+def test_reference_arm_line(workload, capsys, monkeypatch):
+    """The reference arm on the host: one JSON line with the contract's keys, the oracle as its
+    baseline and no host-device bytes (the run's time budget cut to a few seconds here)."""
+    import argparse
+    import json
+    monkeypatch.setattr(bench, "REFERENCE_SECONDS", 3.0)
+    args = argparse.Namespace(workload=workload, steps=3, warmup=3, gpus=1, impl="reference",
+                              no_cpu_baseline=False, no_e2e=False, cpu_seconds=1.0)
+    bench.reference_arm(args, 0, 1)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["config"]["workload"] == workload
+    assert line["value"] > 0 and line["ms_per_step"] > 0 and line["unit"] == "GB/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    bench.reference_arm(args, 1, 2)            # other ranks print nothing
+    assert capsys.readouterr().out == ""
