@@ -3,6 +3,7 @@ slowest rank's time, and the whole-job rate counts the units of all replicas."""
 import os
 import socket
 
+import numpy as np
 import pytest
 import torch
 import torch.distributed as dist
@@ -90,3 +91,29 @@ def test_reference_arm_line(workload, capsys, monkeypatch):
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     bench.reference_arm(args, 1, 2)            # other ranks print nothing
     assert capsys.readouterr().out == ""
+
+
+def test_algorithmic_work_matches_the_stated_formulas():
+    """The roofline's numerator: the bytes and flops a step is credited with, recomputed here from
+    the per-unit figures (a key row read once a stream for all heads; q, out and lse once; a
+    (row, head, key) triple is 2 x (576 + 512) flops)."""
+    from paged_mla_kv_gb300 import synth as Y
+    w = Y.WORKLOADS["decode_batch"]()
+    u = bench.step_units(w)
+    S, R, H = w.S, w.R, w.H
+    assert u["attend_bytes"] == int(np.sum(w.lens)) * 1152 + S * R * H * (576 * 2 + 512 * 2 + 4)
+    assert u["kv"] == int(np.sum(w.lens)) * 1152 and u["tokens"] == S * R
+    f = Y.WORKLOADS["fp8_decode"]()
+    assert bench.step_units(f)["attend_bytes"] == int(np.sum(f.lens)) * 644 + S * R * H * (576 * 2 + 512 * 2 + 4)
+    p = Y.WORKLOADS["prefill_100k"]()
+    T, L = 2048, 100000
+    pairs = sum(L + t + 1 for t in range(T))              # row t sees L + t + 1 keys
+    assert bench.step_units(p)["attend_flops"] == 2176 * 64 * pairs
+    assert abs(2176 * 64 * pairs / 1e12 - 28.81) < 0.01    # the chunk's 28.81 TFLOP
+    sp = Y.WORKLOADS["sparse_decode"]()
+    assert bench.step_units(sp)["attend_bytes"] == 64 * 2048 * 1152 + 64 * 64 * (576 * 2 + 512 * 2 + 4)
+    fm = Y.WORKLOADS["full_model"]()
+    uf = bench.step_units(fm)
+    one = 16 * 40960 * 1152 + 16 * 64 * (576 * 2 + 512 * 2 + 4)
+    assert uf["attend_bytes"] == one
+    assert uf["bytes"] == 12 * (one + 16 * 2 * 1152) + 2 * 32768 * 1152 * 12   # appends and the state copy
