@@ -158,6 +158,12 @@ def step_units(w):
                 attend_flops=flops // C, tokens=S * R if R <= 2 else S * R, kv=kv)
 
 
+def topk_bytes(w) -> int:
+    """Algorithmic bytes of one blocked top-k call: the logits in play read once (4 bytes a key),
+    each row's k columns and values written once (8 bytes a pair)."""
+    return 4 * int(np.sum(w.lens)) + 8 * w.rows * w.k
+
+
 class ClockSampler:
     def __init__(self, index: int):
         self.index, self.rows, self.proc, self.th = index, [], None, None
@@ -378,8 +384,7 @@ def topk_main(args, rank, world, pg, peaks, peak_src):
     ws = torch.empty(max(B.tf_topk_workspace_bytes(w.rows, w.n, w.k), 16), dtype=torch.uint8, device="cuda")
     idx = torch.empty((w.rows, w.k), dtype=torch.int32, device="cuda")
     val = torch.empty((w.rows, w.k), dtype=torch.float32, device="cuda")
-    read = 4 * int(np.sum(w.lens))
-    algo = read + 8 * w.rows * w.k            # logits in play read once, columns and values written
+    algo = topk_bytes(w)
 
     def step(src=x, oi=idx, ov=val):
         B.tf_topk_blocked(src, w.k, oi, ov, lens=lens, ws=ws)

@@ -117,3 +117,7 @@ def test_algorithmic_work_matches_the_stated_formulas():
     one = 16 * 40960 * 1152 + 16 * 64 * (576 * 2 + 512 * 2 + 4)
     assert uf["attend_bytes"] == one
     assert uf["bytes"] == 12 * (one + 16 * 2 * 1152) + 2 * 32768 * 1152 * 12   # appends and the state copy
+    tk = Y.TOPK_WORKLOADS["topk_prefill"]()
+    keys = sum(100000 - 2048 + 1 + t for t in range(2048))
+    assert bench.topk_bytes(tk) == 4 * keys + 2048 * 512 * 8
+    assert abs(bench.topk_bytes(tk) / 1e6 - 819.2) < 0.1  # 810.8 MB of logits in play + 8.4 MB written
