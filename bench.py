@@ -143,6 +143,8 @@ def step_units(w):
         return dict(bytes=kv + q + out + app, attend_bytes=kv + q + out, flops=flops, attend_flops=flops,
                     tokens=S, kv=kv)
     kv = int(np.sum(w.lens)) * row
+    # the same rows with each shared prefix page counted once (what the pool holds)
+    unique_kv = sum(int(w.lens[s]) - w.shared_pages(s) * Y.PAGE_ROWS for s in range(S)) * row
     q = S * R * H * Y.DK * 2
     out = S * R * H * (512 * 2 + 4)
     app = S * R * (Y.ROW_BYTES + row)
@@ -155,7 +157,7 @@ def step_units(w):
         pairs += sum(L - R + r + 1 for r in range(R)) if R <= 4096 else 0
     flops = 2 * (Y.DK + 512) * H * pairs * C
     return dict(bytes=C * (attend_bytes + app) + copy, attend_bytes=attend_bytes, flops=flops,
-                attend_flops=flops // C, tokens=S * R if R <= 2 else S * R, kv=kv)
+                attend_flops=flops // C, tokens=S * R if R <= 2 else S * R, kv=kv, unique_kv=unique_kv)
 
 
 def topk_bytes(w) -> int:
@@ -689,6 +691,7 @@ def main():
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": w.name, "S": w.S, "R": w.R, "H": w.H, "caches": w.num_caches,
                            "lens_sum": int(np.sum(w.lens)), "kv_bytes": units["kv"],
+                           "unique_kv_bytes": units.get("unique_kv", units["kv"]),
                            "l2": "flushed between steps" if flush is not None else "inputs larger than L2",
                            "parallelism": f"replicas x{world}", "tokens_per_step": units["tokens"]},
                 "tokens_per_s": tokens_s, "gpu_launches": launches, "roofline": roof, "cpu_baseline": cpu,

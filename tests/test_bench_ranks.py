@@ -103,6 +103,8 @@ def test_algorithmic_work_matches_the_stated_formulas():
     S, R, H = w.S, w.R, w.H
     assert u["attend_bytes"] == int(np.sum(w.lens)) * 1152 + S * R * H * (576 * 2 + 512 * 2 + 4)
     assert u["kv"] == int(np.sum(w.lens)) * 1152 and u["tokens"] == S * R
+    shared = sum(w.share[s][1] for s in range(S)) * 512 * 1152          # streams 1-3's prefix pages
+    assert u["unique_kv"] == u["kv"] - shared and shared > 0
     f = Y.WORKLOADS["fp8_decode"]()
     assert bench.step_units(f)["attend_bytes"] == int(np.sum(f.lens)) * 644 + S * R * H * (576 * 2 + 512 * 2 + 4)
     p = Y.WORKLOADS["prefill_100k"]()
