@@ -75,10 +75,10 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> floa
 # the SHA-256 of the kernel's source the capture was taken on: once the kernel changes, the
 # counters no longer describe it and "traffic" is reported null until it is re-captured.
 # Attention captured on source 94c4ab2dc8479ab9 (`--metrics dram__bytes_read.sum,dram__bytes_write.sum,
-# gpu__time_duration.sum`; the FP8 decode launch under `--set full`); 8d4e84ac7fed2680 differs from
+# gpu__time_duration.sum`; the FP8 decode launch under `--set full`); 3212b017dcca9adb differs from
 # it in host code only (the cubins built without line info hash the same).
 NCU_TRAFFIC = {
-    "8d4e84ac7fed2680": {"decode_batch": 374_700_544 + 3_504_128,
+    "3212b017dcca9adb": {"decode_batch": 374_700_544 + 3_504_128,
                          "fp8_decode": 207_994_112 + 4_065_024,
                          "prefill_100k": 1_845_974_272 + 135_486_464,
                          "sparse_fp8_decode": 103_608_832 + 3_570_432},

@@ -309,6 +309,29 @@ int tf_last_error(tf_kvpool *pool, int64_t *detail);
  * library's own failure path without faulting or hanging the GPU. */
 int tf_diag_wait_timeout(tf_kvpool *pool, int64_t limit_cycles, void *cuda_stream);
 
+/* The work plan tf_paged_mla_attend would use for these lengths, for inspection: host
+ * arithmetic only, nothing launched.  sms: the SMs to plan for (<= 0: the current device's,
+ * or TF_PLAN_MAX_RANGES without one); invariant != 0: a TF_POOL_BATCH_INVARIANT pool.
+ *   info->mode     0 key-tile ranges (decode, MTP rows), 1 whole (stream, column group) units
+ *                  round robin (prefill chunks), 2 per-stream splits (batch-invariant pools)
+ *   info->ctas     CTAs launched
+ *   info->nranges  mode 0: ranges (each taken by info->groups CTAs side by side); else 0
+ *   info->groups   column groups a stream: ceil(R * H / 64)
+ *   info->work     mode 0: 64-key tiles of the batch; mode 1: units; mode 2: (split, group) items
+ *   info->slots    fp32 partial slots in the workspace (0: no combine pass)
+ * range_bounds (may be NULL): with mode 0, the nranges + 1 tile numbers that bound the ranges,
+ * tiles numbered stream by stream (at most TF_PLAN_MAX_RANGES + 1 entries).
+ * split_keys (may be NULL): with mode 2, the keys of one split of each stream [S].
+ * TF_E_ARG for a null h_len or info, or S, R, H outside the attention's limits; TF_E_RANGE for a
+ * length below R or above INT32_MAX. */
+#define TF_PLAN_MAX_RANGES 240
+typedef struct {
+    int32_t mode, ctas, nranges, groups;
+    int64_t work, slots;
+} tf_attend_plan;
+int tf_paged_mla_plan_info(int32_t S, int32_t R, int32_t H, const int64_t *h_len, int32_t sms, int32_t invariant,
+                           tf_attend_plan *info, int64_t *range_bounds, int64_t *split_keys);
+
 /* Kernels this library has launched since the process started. */
 int64_t tf_launch_count(void);
 

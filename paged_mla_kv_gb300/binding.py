@@ -47,6 +47,14 @@ class tf_plan_in(ctypes.Structure):
                 ("cache_budget_bytes", ctypes.c_int64)]
 
 
+class tf_attend_plan(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("ctas", ctypes.c_int32), ("nranges", ctypes.c_int32),
+                ("groups", ctypes.c_int32), ("work", ctypes.c_int64), ("slots", ctypes.c_int64)]
+
+
+TF_PLAN_MAX_RANGES = 240
+
+
 class tf_plan_out(ctypes.Structure):
     _fields_ = [("n_windows", ctypes.c_int32), ("window_pages", ctypes.c_int64), ("stream_pages", ctypes.c_int64),
                 ("cache_bytes", ctypes.c_int64), ("other_pages", ctypes.c_int64), ("pool_pages", ctypes.c_int64),
@@ -77,6 +85,7 @@ _SIGS = {
     "tf_last_error": (ctypes.c_int, [_P, ctypes.POINTER(_I64)]),
     "tf_diag_wait_timeout": (ctypes.c_int, [_P, _I64, _P]),
     "tf_launch_count": (_I64, []),
+    "tf_paged_mla_plan_info": (ctypes.c_int, [_I32, _I32, _I32, _P, _I32, _I32, _P, _P, _P]),
     "tf_topk_workspace_bytes": (_SZ, [_I64, _I64, _I32]),
     "tf_topk_blocked": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
     "tf_profile_enable": (ctypes.c_int, [_P, _I32]),
@@ -313,6 +322,23 @@ def tf_topk_blocked(logits, k: int, idx, val, lens=None, n: int | None = None, w
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib().tf_topk_blocked(_ptr(logits), rows, n, ld, _ptr(lens), int(k), _ptr(idx), _ptr(val), _ptr(ws),
                                  ws_bytes, _stream(stream)), "tf_topk_blocked")
+
+
+def tf_paged_mla_plan_info(S: int, R: int, H: int, lens, sms: int = 0, invariant: bool = False) -> dict:
+    """The attention's work plan for these lengths (host arithmetic, nothing launched): mode,
+    ctas, nranges, groups, work, slots, and the range bounds (mode 0) or each stream's split
+    keys (mode 2) as int64 arrays."""
+    a, p = _i64(lens)
+    info = tf_attend_plan()
+    bounds = np.zeros(TF_PLAN_MAX_RANGES + 1, np.int64)
+    splits = np.zeros(max(S, 1), np.int64)
+    _check(lib().tf_paged_mla_plan_info(S, R, H, p, sms, 1 if invariant else 0, ctypes.byref(info),
+                                        bounds.ctypes.data_as(ctypes.c_void_p),
+                                        splits.ctypes.data_as(ctypes.c_void_p)), "tf_paged_mla_plan_info")
+    out = {f: int(getattr(info, f)) for f, _ in tf_attend_plan._fields_}
+    out["bounds"] = bounds[:out["nranges"] + 1] if out["mode"] == 0 else None
+    out["split_keys"] = splits[:S] if out["mode"] == 2 else None
+    return out
 
 
 def tf_launch_count() -> int:

@@ -1249,6 +1249,28 @@ size_t attend_workspace_bytes(bool invariant, int S, int R, int H, const int64_t
     return o + ((ml + 255) & ~size_t(255));
 }
 
+// The plan a call would use, for tf_paged_mla_plan_info (host arithmetic only).
+int attend_plan_info(int S, int R, int H, const int64_t *h_len, int sms, bool invariant, tf_attend_plan *info,
+                     int64_t *range_bounds, int64_t *split_keys) {
+    static_assert(TF_PLAN_MAX_RANGES == attn::MAX_CTAS, "the header's bound is the launch's");
+    if (sms <= 0) sms = device_sms();
+    if (sms > attn::MAX_CTAS) sms = attn::MAX_CTAS;
+    int64_t rb[attn::MAX_CTAS + 1];
+    const attn::Plan pl = attn::plan_of(S, R, H, h_len, sms, invariant, rb);
+    const int groups = (R * H + attn::NCOL - 1) / attn::NCOL;
+    info->mode = pl.mode;
+    info->ctas = pl.nctas;
+    info->nranges = pl.mode == attn::MODE_RANGES ? pl.nranges : 0;
+    info->groups = groups;
+    info->work = pl.total;
+    info->slots = (int64_t)pl.slots;
+    if (range_bounds && pl.mode == attn::MODE_RANGES)
+        for (int i = 0; i <= pl.nranges; ++i) range_bounds[i] = rb[i];
+    if (split_keys && pl.mode == attn::MODE_SPLITS)
+        for (int s = 0; s < S; ++s) split_keys[s] = attn::split_of(h_len[s], groups).split;
+    return TF_OK;
+}
+
 // The driver's tensor-map encoder, looked up once: a function-local static is initialised
 // exactly once even when several host threads make their first call together.
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {

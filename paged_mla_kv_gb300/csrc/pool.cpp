@@ -229,6 +229,16 @@ extern "C" size_t tf_paged_mla_workspace_bytes(const tf_kvpool *p, int32_t S, in
     return part;
 }
 
+extern "C" int tf_paged_mla_plan_info(int32_t S, int32_t R, int32_t H, const int64_t *h_len, int32_t sms,
+                                      int32_t invariant, tf_attend_plan *info, int64_t *range_bounds,
+                                      int64_t *split_keys) {
+    if (!h_len || !info || S < 1 || S > TF_MAX_STREAMS || R < 1 || H < 1 || H > TF_MAX_HEADS) return TF_E_ARG;
+    if ((int64_t)S * R * H > (int64_t)1 << 30) return TF_E_ARG;
+    for (int s = 0; s < S; ++s)
+        if (h_len[s] < R || h_len[s] > kMaxStreamRows) return TF_E_RANGE;
+    return attend_plan_info(S, R, H, h_len, sms, invariant != 0, info, range_bounds, split_keys);
+}
+
 extern "C" int tf_paged_mla_attend(tf_kvpool *p, int32_t cache, const int32_t *d_pt, int32_t max_pages,
                                    const int64_t *h_len, int32_t S, int32_t R, int32_t H, const void *d_q,
                                    float scale, void *d_out, float *d_lse, void *d_ws, size_t ws_bytes,

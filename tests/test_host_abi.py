@@ -350,3 +350,80 @@ def test_headers_compile_as_c_and_the_library_links_from_c(L, tmp_path):
     got = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
     want = [2056, 1052672, 12 * 1344 * 589824 + 256, 12 * 1344 * 329728 + 256, 2 * 3 * 8 * 8, B.TF_E_ARG, 1]
     assert [int(x) for x in got] == want
+
+
+def _weighted_sizes(bounds, lens, seg=3):
+    """Tiles of each range plus `seg` for every stream that starts inside it (a segment start
+    costs a query reload and an extra epilogue, about three tiles)."""
+    tiles = -(-np.asarray(lens, np.int64) // 64)
+    starts = np.concatenate([[0], np.cumsum(tiles)[:-1]])
+    return [int(bounds[i + 1] - bounds[i]) + seg * int(np.sum((starts >= bounds[i]) & (starts < bounds[i + 1])))
+            for i in range(len(bounds) - 1)]
+
+
+@pytest.mark.parametrize("name", ["decode_batch", "long_window", "full_model", "tiny_decode"])
+def test_decode_plan_deals_every_tile_once_in_balanced_ranges(L, name):
+    from paged_mla_kv_gb300 import synth as Y
+    w = Y.WORKLOADS[name]()
+    pl = B.tf_paged_mla_plan_info(w.S, w.R, w.H, w.lens, sms=152)
+    tiles = int(np.sum(-(-w.lens // 64)))
+    assert pl["mode"] == 0 and pl["work"] == tiles and pl["groups"] == -(-w.R * w.H // 64)
+    b = pl["bounds"]
+    assert b[0] == 0 and b[-1] == tiles and np.all(np.diff(b) >= 1)     # every tile in exactly one range
+    assert pl["ctas"] == pl["nranges"] * pl["groups"] <= 152
+    assert pl["nranges"] == min(-(-tiles // 4), 152 // pl["groups"])     # at least 4 tiles a range
+    wsz = _weighted_sizes(b, w.lens)
+    assert max(wsz) - min(wsz) <= 8, (min(wsz), max(wsz))
+    assert pl["slots"] in (0, 2 * pl["ctas"])                           # two partial slots a CTA
+
+
+def test_plan_and_workspace_agree(L):
+    from paged_mla_kv_gb300 import synth as Y
+    w = Y.WORKLOADS["decode_batch"]()
+    pl = B.tf_paged_mla_plan_info(w.S, w.R, w.H, w.lens)               # the same SM count as the sizing
+    slots = pl["slots"]
+    assert slots > 0
+    want = slots * 64 * 512 * 4 + (-(-(slots * 64 * 2 * 4) // 256)) * 256
+    assert B.tf_paged_mla_workspace_bytes(None, w.S, w.R, w.H, w.lens) == want
+
+
+def test_prefill_plan_deals_whole_units(L):
+    from paged_mla_kv_gb300 import synth as Y
+    w = Y.WORKLOADS["prefill_100k"]()
+    pl = B.tf_paged_mla_plan_info(w.S, w.R, w.H, w.lens, sms=152)
+    assert pl["mode"] == 1 and pl["groups"] == 2048 and pl["work"] == 2048
+    assert pl["ctas"] == 152 and pl["slots"] == 0
+    assert B.tf_paged_mla_workspace_bytes(None, w.S, w.R, w.H, w.lens) == 0
+
+
+def test_invariant_splits_depend_on_the_stream_alone(L):
+    """On a batch-invariant pool a stream's split is a function of its own length, R and H: the
+    same in any batch, a multiple of 256 keys, and the items are the splits of every group."""
+    from paged_mla_kv_gb300 import synth as Y
+    w = Y.WORKLOADS["decode_batch"]()
+    pl = B.tf_paged_mla_plan_info(w.S, w.R, w.H, w.lens, sms=152, invariant=True)
+    assert pl["mode"] == 2
+    sk = pl["split_keys"]
+    for s in range(w.S):
+        alone = B.tf_paged_mla_plan_info(1, w.R, w.H, w.lens[s:s + 1], sms=152, invariant=True)
+        assert alone["split_keys"][0] == sk[s] and sk[s] % 256 == 0
+        other = B.tf_paged_mla_plan_info(2, w.R, w.H, [int(w.lens[s]), 777], sms=7, invariant=True)
+        assert other["split_keys"][0] == sk[s]
+    nsplit = -(-w.lens // sk)
+    assert pl["ctas"] == pl["work"] == int(np.sum(nsplit)) * pl["groups"]
+    assert pl["slots"] == int(np.sum(nsplit[nsplit > 1])) * pl["groups"]
+    # a prefill chunk with 128 or more column groups is one split
+    p = Y.WORKLOADS["prefill_208k"]()
+    pp = B.tf_paged_mla_plan_info(p.S, p.R, p.H, p.lens, invariant=True)
+    assert pp["mode"] == 2 and pp["split_keys"][0] == p.lens[0] and pp["slots"] == 0
+
+
+def test_plan_info_refuses_bad_sizes(L):
+    lens = np.array([100, 200], np.int64)
+    info = B.tf_attend_plan()
+    lp = lens.ctypes.data_as(ctypes.c_void_p)
+    assert L.tf_paged_mla_plan_info(2, 1, 129, lp, 0, 0, ctypes.byref(info), None, None) == B.TF_E_ARG
+    assert L.tf_paged_mla_plan_info(0, 1, 16, lp, 0, 0, ctypes.byref(info), None, None) == B.TF_E_ARG
+    assert L.tf_paged_mla_plan_info(2, 1, 16, lp, 0, 0, None, None, None) == B.TF_E_ARG
+    assert L.tf_paged_mla_plan_info(2, 101, 16, lp, 0, 0, ctypes.byref(info), None, None) == B.TF_E_RANGE
+    assert L.tf_paged_mla_plan_info(2, 1, 16, lp, 0, 0, ctypes.byref(info), None, None) == B.TF_OK
