@@ -322,8 +322,9 @@ int tf_diag_wait_timeout(tf_kvpool *pool, int64_t limit_cycles, void *cuda_strea
  * range_bounds (may be NULL): with mode 0, the nranges + 1 tile numbers that bound the ranges,
  * tiles numbered stream by stream (at most TF_PLAN_MAX_RANGES + 1 entries).
  * split_keys (may be NULL): with mode 2, the keys of one split of each stream [S].
- * TF_E_ARG for a null h_len or info, or S, R, H outside the attention's limits; TF_E_RANGE for a
- * length below R or above INT32_MAX. */
+ * TF_E_ARG for a null h_len or info, or S, R, H outside the attention's limits; TF_E_UNSUPPORTED
+ * for S * R * H above 2^30 (as tf_paged_mla_attend); TF_E_RANGE for a length below R or above
+ * INT32_MAX. */
 #define TF_PLAN_MAX_RANGES 240
 typedef struct {
     int32_t mode, ctas, nranges, groups;

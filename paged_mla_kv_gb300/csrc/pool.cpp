@@ -233,7 +233,7 @@ extern "C" int tf_paged_mla_plan_info(int32_t S, int32_t R, int32_t H, const int
                                       int32_t invariant, tf_attend_plan *info, int64_t *range_bounds,
                                       int64_t *split_keys) {
     if (!h_len || !info || S < 1 || S > TF_MAX_STREAMS || R < 1 || H < 1 || H > TF_MAX_HEADS) return TF_E_ARG;
-    if ((int64_t)S * R * H > (int64_t)1 << 30) return TF_E_ARG;
+    if ((int64_t)S * R * H > (int64_t)1 << 30) return TF_E_UNSUPPORTED;   // as tf_paged_mla_attend
     for (int s = 0; s < S; ++s)
         if (h_len[s] < R || h_len[s] > kMaxStreamRows) return TF_E_RANGE;
     return attend_plan_info(S, R, H, h_len, sms, invariant != 0, info, range_bounds, split_keys);
