@@ -1149,7 +1149,8 @@ constexpr int64_t SEG_COST = 3;   // a segment start, in key tiles
 
 inline Plan plan_of(int S, int R, int H, const int64_t *h_len, int sms, bool invariant, int64_t *rb = nullptr) {
     Plan pl;
-    const int groups = (R * H + NCOL - 1) / NCOL;
+    // R * H itself can pass INT32_MAX; callers refuse S * R * H above 2^30, so groups fits an int
+    const int groups = (int)(((int64_t)R * H + NCOL - 1) / NCOL);
     pl.slots = 0;
     pl.rep = 1;
     pl.nranges = 0;
@@ -1226,6 +1227,12 @@ inline Plan plan_of(int S, int R, int H, const int64_t *h_len, int sms, bool inv
 }
 
 inline size_t slot_bytes() { return (size_t)NCOL * kLat * sizeof(float); }
+// On a default pool the partials are at most two slots a CTA; the no-allocation entry point's
+// fixed scratch must hold that many, with the (m, l) pairs after them rounded to 256 bytes.
+static_assert(2 * (size_t)MAX_CTAS * NCOL * kLat * sizeof(float) +
+                      ((2 * (size_t)MAX_CTAS * NCOL * 2 * sizeof(float) + 255) & ~size_t(255)) <=
+                  (size_t)TF_STATIC_WS_BYTES,
+              "every default-pool call must fit the static scratch");
 
 }  // namespace attn
 
@@ -1257,7 +1264,7 @@ int attend_plan_info(int S, int R, int H, const int64_t *h_len, int sms, bool in
     if (sms > attn::MAX_CTAS) sms = attn::MAX_CTAS;
     int64_t rb[attn::MAX_CTAS + 1];
     const attn::Plan pl = attn::plan_of(S, R, H, h_len, sms, invariant, rb);
-    const int groups = (R * H + attn::NCOL - 1) / attn::NCOL;
+    const int groups = (int)(((int64_t)R * H + attn::NCOL - 1) / attn::NCOL);
     info->mode = pl.mode;
     info->ctas = pl.nctas;
     info->nranges = pl.mode == attn::MODE_RANGES ? pl.nranges : 0;

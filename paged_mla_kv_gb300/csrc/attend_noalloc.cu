@@ -24,7 +24,10 @@ void *static_ws_on_current_device() {
     std::lock_guard<std::mutex> g(g_mu);
     if (!g_ws_addr[dev]) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) {
+            cudaGetLastError();   // leave no sticky error behind for the caller's next CUDA check
+            return nullptr;
+        }
         g_ws_addr[dev] = p;
     }
     return g_ws_addr[dev];
@@ -36,6 +39,7 @@ extern "C" int tf_paged_mla_attend_static(tf_kvpool *pool, int32_t cache, const 
                                           const int64_t *h_len, int32_t S, int32_t R, int32_t H, const void *d_q,
                                           float scale, void *d_out, float *d_lse, void *cuda_stream) {
     if (!pool || !h_len || S < 1 || S > TF_MAX_STREAMS || R < 1 || H < 1 || H > TF_MAX_HEADS) return TF_E_ARG;
+    if ((int64_t)S * R * H > (int64_t)1 << 30) return TF_E_UNSUPPORTED;   // as tf_paged_mla_attend, before sizing
     // FP8 pages on a batch-invariant pool are expanded in a caller workspace
     if (tf::is_fp8(pool->desc) && (pool->desc.flags & TF_POOL_BATCH_INVARIANT)) return TF_E_UNSUPPORTED;
     for (int s = 0; s < S; ++s)

@@ -266,7 +266,7 @@ int launch_attend_fp8(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_p
     sh->base = shadow;
     sh->bytes = (size_t)sp.pages * kPageBytes;
     sh->err = pool->err;
-    sh->err_cleared = true;
+    sh->err_cleared.store(true);
     sh->prof = false;
 
     DequantParams p;

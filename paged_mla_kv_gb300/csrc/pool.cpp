@@ -220,6 +220,7 @@ static constexpr int64_t kMaxStreamRows = INT32_MAX;
 extern "C" size_t tf_paged_mla_workspace_bytes(const tf_kvpool *p, int32_t S, int32_t R, int32_t H,
                                                const int64_t *h_len) {
     if (S < 1 || S > TF_MAX_STREAMS || R < 1 || H < 1 || H > TF_MAX_HEADS || !h_len) return 0;
+    if ((int64_t)S * R * H > (int64_t)1 << 30) return 0;   // refused by tf_paged_mla_attend
     for (int s = 0; s < S; ++s)
         if (h_len[s] < R || h_len[s] > kMaxStreamRows) return 0;
     const bool invariant = p && (p->desc.flags & TF_POOL_BATCH_INVARIANT);
@@ -331,8 +332,8 @@ extern "C" int tf_last_error(tf_kvpool *p, int64_t *detail) {
     DevErr e{};
     if (cudaMemcpy(&e, p->err, sizeof e, cudaMemcpyDeviceToHost) != cudaSuccess) return TF_E_CUDA;
     if (cudaMemset(p->err, 0, sizeof(DevErr)) != cudaSuccess) return TF_E_CUDA;
-    if (!p->err_cleared) e = DevErr{};  // nothing launched yet: the word was never zeroed
-    p->err_cleared = true;
+    if (!p->err_cleared.load()) e = DevErr{};  // nothing launched yet: the word was never zeroed
+    p->err_cleared.store(true);
     if (detail) *detail = e.detail;
     return e.code;
 }

@@ -53,7 +53,7 @@ struct tf_kvpool {
     char *base = nullptr;
     size_t bytes = 0;
     tf::DevErr *err = nullptr;  // device address
-    bool err_cleared = false;   // the error word is zeroed on the first launch
+    std::atomic<bool> err_cleared{false};   // the error word is zeroed before the first launch
     std::vector<int32_t> refcnt;
     std::vector<int32_t> free_ring;  // FIFO of free ids
     size_t free_head = 0, free_count = 0;
@@ -76,11 +76,18 @@ namespace tf {
 
 std::atomic<int64_t> &launch_counter();
 
-// Called before every launch: zeroes the device error word once, on the launch stream.
+// Called before every launch.  The first launch on a pool zeroes the device error word and
+// waits for it, under the pool's lock, so no launch from any host thread or stream can run
+// before the word is clear (a launch queued on another stream could otherwise record an error
+// that the zeroing then erases).  Because of that wait the first launch on a pool must not be
+// made while its stream is being captured.
 inline int prepare_launch(tf_kvpool *pool, cudaStream_t st) {
-    if (pool->err_cleared) return TF_OK;
+    if (pool->err_cleared.load(std::memory_order_acquire)) return TF_OK;
+    std::lock_guard<std::mutex> g(pool->mu);
+    if (pool->err_cleared.load(std::memory_order_relaxed)) return TF_OK;
     if (cudaMemsetAsync(pool->err, 0, sizeof(DevErr), st) != cudaSuccess) return TF_E_CUDA;
-    pool->err_cleared = true;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return TF_E_CUDA;
+    pool->err_cleared.store(true, std::memory_order_release);
     return TF_OK;
 }
 

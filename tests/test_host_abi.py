@@ -199,6 +199,14 @@ def test_bad_arguments_are_refused_before_launch(L):
     assert _args_refused(L, h, A, 0, fake, wide, lq, 2, 1, 16, fake, 0.1, fake, None, fake, 1 << 40,
                          None) == B.TF_E_UNSUPPORTED
     assert L.tf_paged_mla_workspace_bytes(h, 2, 1, 16, lq) == 0
+    # S * R * H above 2^30: both the sizing call and the allocation-free entry point refuse it
+    # before any plan arithmetic (R * H alone would overflow the plan's int column count)
+    lbig = np.array([1 << 25], np.int64)
+    lb = lbig.ctypes.data_as(ctypes.c_void_p)
+    assert L.tf_paged_mla_workspace_bytes(h, 1, 1 << 25, 128, lb) == 0
+    assert L.tf_paged_mla_workspace_bytes(None, 1, 1 << 25, 128, lb) == 0
+    assert _args_refused(L, h, L.tf_paged_mla_attend_static, 0, fake, 1 << 16, lb, 1, 1 << 25, 128, fake, 0.1,
+                         fake, None, None) == B.TF_E_UNSUPPORTED
     nidx = np.array([8, 8], np.int32)
     assert _args_refused(L, h, L.tf_paged_mla_attend_sparse, 0, fake, wide, lq, fake, 8,
                          nidx.ctypes.data_as(ctypes.c_void_p), 2, 16, fake, 0.1, fake, None, fake, 1 << 40,

@@ -56,6 +56,21 @@ def test_static_scratch_matches_workspace_entry_point_twice():
         assert (lse - ref_lse).abs().max().item() <= 2e-3
         # the same kernels over the same bytes: identical bits
         assert np.array_equal(bits(out), bits(ref_out))
+    # a third call of another shape: other streams and lengths move the range cuts and change
+    # how many slots hold partials, so a slot that kept a stale partial would show here
+    w3 = Y.custom("noalloc_shape", 80, lens=[70000, 5, 2100, 333, 12000], R=1, H=64)
+    res3 = Resident(w3)
+    need3 = B.tf_paged_mla_workspace_bytes(res3.pool, w3.S, w3.R, w3.H, w3.lens)
+    assert 0 < need3 <= B.TF_STATIC_WS_BYTES
+    q3 = res3.q()
+    ref_out, ref_lse = res3.attend(q3)
+    out = torch.full_like(ref_out, float("nan"))
+    lse = torch.full_like(ref_lse, float("nan"))
+    assert _static_call(res3, q3, out, lse) == B.TF_OK
+    torch.cuda.synchronize()
+    no_device_error(res3.pool)
+    assert np.array_equal(bits(out), bits(ref_out))
+    assert np.array_equal(bits(lse), bits(ref_lse))
 
 
 def test_static_scratch_covers_every_default_launch():
