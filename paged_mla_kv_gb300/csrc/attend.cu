@@ -11,15 +11,16 @@
 // (row, head) columns) of one stream over a run of its key tiles; how the tiles are dealt out
 // (RANGES, UNITS, SPLITS, SPARSE) is described at the Params below.  Keys stream through
 // 64-row tiles: 9 boxes of [64 keys x 64 values] bf16 (8 latent + 1 rope), loaded by TMA with
-// 128-byte swizzle from the tile's pool page into a 2-stage ring, landing in a part of 3 boxes
-// (rope + latent 0-1) and a part of 6; the rope box is released after QK^T and each latent
-// box pair as soon as its PV M-tile finishes, so the next tile's loads start early.  The same
-// shared-memory tile feeds both contractions on the 5th-generation tensor cores:
-//   S   = Q . K^T     tcgen05.mma M=64 (the columns), N=64 keys, K=576, Q and the tile
-//                     K-major; S accumulates in TMEM (2 buffers)
+// 128-byte swizzle from the tile's pool page into a ring of 11 latent box-pair slots and 3 rope
+// slots (2.75 tiles in flight).  The queries' latent values 0-383 sit in TMEM as the A operand
+// of QK^T; only their last two latent boxes and the rope box stay in shared memory, which is
+// what pays for the deeper ring.  The same shared-memory tile feeds both contractions on the
+// 5th-generation tensor cores:
+//   S   = Q . K^T     tcgen05.mma M=64 (the columns), N=64 keys, K=576, A from TMEM (values
+//                     0-383) or shared memory (the rest), the tile K-major; S in TMEM
 //   O^T += V^T . P^T  tcgen05.mma M=128 latent values x 4, N = columns rounded up to 16,
-//                     K=64 keys, the tile read MN-major as V^T, P (bf16, in shared memory)
-//                     K-major; O^T accumulates in TMEM (4 x 64 columns)
+//                     K=64 keys, the tile read MN-major as V^T, P (bf16, written into the tile's
+//                     rope slot once QK^T has read it) K-major; O^T accumulates in TMEM (4 x 64 columns)
 // Softmax is online in fp32 registers, each of four warps reading one TMEM lane quadrant
 // (two rows and 16 of their keys a thread), with a lazily moved reference maximum: O^T is
 // rescaled only when a tile's maximum passes the reference by more than 2^8, by a separate
@@ -28,9 +29,12 @@
 // combine kernel merges in key order.
 //
 // Warp roles (352 threads; 480 on FP8 pages): warps 0-3 rescale O^T when asked and run the
-// epilogue (one TMEM lane quadrant each); warps 4-7 softmax; warp 8 the TMA producer; warp 9
-// the TMEM allocation and the QK^T issuer; warp 10 the PV issuer; on FP8 pages warps 11-14
-// expand each tile's codes to bf16 in shared memory.
+// epilogue (one TMEM lane quadrant each); warps 4-7 softmax, and at each segment start write
+// the segment's queries into TMEM; warp 8 the TMA producer; warp 9 the TMEM allocation and the
+// QK^T issuer; warp 10 the PV issuer; on FP8 pages warps 11-14 expand each tile's codes to bf16
+// in shared memory.  The MMA issuers walk their issue loops as whole warps with one elected lane
+// issuing, in rolled loops: on this GPU both kept MMA issue markedly faster than a lone lane
+// running unrolled issue code.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -50,31 +54,41 @@ namespace tf {
 
 namespace attn {
 
-constexpr int BK = 64;                          // keys a tile (N of the QK^T MMA; an MMA
-                                                // costs about the same to issue at N=32 or 64)
+constexpr int BK = 64;                          // keys a tile (N of the QK^T MMA: an MMA costs
+                                                // about 49 cycles at N = 64 whether M is 64 or 128)
 constexpr int NCOL = 64;                        // (row, head) columns a CTA
 constexpr int NBOX = 9;                         // 64-wide boxes of a 576-wide row
 constexpr int BOX_BYTES = BK * 128;             // [64 rows][64 bf16], 128B swizzle
-constexpr int QBOX_BYTES = NCOL * 128;          // [64 rows][64 bf16]
-constexpr int Q_BYTES = NBOX * QBOX_BYTES;      // 73,728
-constexpr int P_BYTES = NCOL * 128;             // 64 rows (columns) of 64 keys, bf16
-constexpr int STAGE_BYTES = NBOX * BOX_BYTES;   // 73,728
-constexpr int NSTAGE = 2;
+constexpr int PAIR_BYTES = 2 * BOX_BYTES;       // latent boxes 2j and 2j+1 of a tile, side by side
+constexpr int QBOX_BYTES = NCOL * 128;          // [64 columns][64 bf16]
+// The queries: latent values 0-383 (boxes 0-5) sit in TMEM as the A operand of QK^T, written
+// by the softmax warps at each segment start; latent boxes 6-7 and the rope box stay in shared
+// memory (TMA).  Moving 48 KB of queries out of shared memory is what deepens the key ring.
+constexpr int Q_TMEM_BOXES = 6;
+constexpr int Q_SMEM_BOXES = NBOX - Q_TMEM_BOXES;   // [latent 6 | latent 7 | rope]
+// The key ring: a tile is its rope box (in a rope slot) and four latent box pairs (in pair
+// slots).  Pair slots are taken in order, four a tile (2.75 tiles in flight); a rope slot a tile
+// (3 in flight).  Once QK^T has read a tile's rope box, the slot holds the tile's P for PV, so
+// P is triple-buffered and the softmax never waits for the previous PV.
+constexpr int NPAIR = 11;
+constexpr int NROPE = 3;
 constexpr int SMEM_Q = 0;
-constexpr int SMEM_P = SMEM_Q + Q_BYTES;        // directly after Q: QK^T rows 64-127 of the last box read it
-constexpr int SMEM_KV = SMEM_P + P_BYTES;
-constexpr int SMEM_CTRL = SMEM_KV + NSTAGE * STAGE_BYTES;  // 229,376
+constexpr int SMEM_ROPE = SMEM_Q + Q_SMEM_BOXES * QBOX_BYTES;   // 24,576
+constexpr int SMEM_PAIR = SMEM_ROPE + NROPE * BOX_BYTES;          // 49,152
+constexpr int SMEM_CTRL = SMEM_PAIR + NPAIR * PAIR_BYTES;         // 229,376
 constexpr float TAU = 8.0f;                     // lazy-rescale threshold, log2 units
 constexpr int TMEM_COLS = 512;
 constexpr int TMEM_O = 0;                       // O^T M-tile j at 64 j (j < 4)
-constexpr int TMEM_S = 256;                     // S buffers at 256 and 320
+constexpr int TMEM_S = 256;                     // S (one buffer, 64 columns)
+constexpr int TMEM_Q = 320;                     // queries' latent values 0-383: column c holds values 2c, 2c+1
+static_assert(TMEM_Q + Q_TMEM_BOXES * 32 == TMEM_COLS, "the queries fill TMEM's last columns");
 constexpr int THREADS = 352;
-// FP8 pages: four more warps (11-14) expand each tile's E4M3 codes into the BF16 boxes in place.
-// The codes land by TMA, unswizzled, in the upper half of the latent boxes' room,
-// [F8_STAGING, +32 KB) = BF16 boxes 4-7: dense tiles as 8 boxes of 64 rows x 64 bytes (codes
-// 64b.. of row r at 4 KB b + 64 r), gathered tiles as 2 blocks of 64 rows x 256 bytes (codes
-// 256q.. of row r at 16 KB q + 256 r; a quarter of the gathers).  BF16 box b (codes 64b..64b+63)
-// is written in order, two boxes a round, so each write covers only codes already read (the
+// FP8 pages: four more warps (11-14) expand each tile's E4M3 codes into its BF16 boxes in place.
+// The codes land by TMA, unswizzled, in the tile's pair slots 2-3 (the room of BF16 boxes 4-7):
+// dense tiles as 8 boxes of 64 rows x 64 bytes (codes 64b.. of row r at pair slot 2 + b/4, byte
+// 4 KB (b%4) + 64 r), gathered tiles as 2 blocks of 64 rows x 256 bytes (codes 256q.. of row r at
+// pair slot 2 + q, byte 256 r; a quarter of the gathers).  BF16 box b (codes 64b..64b+63) is
+// written in order, one pair slot a round, so each write covers only codes already read (the
 // last round, boxes 6-7, reads all its rows first).
 constexpr int THREADS_F8 = THREADS + 128;
 constexpr int F8_THREADS = THREADS_F8 - THREADS;   // two threads a tile row
@@ -82,33 +96,45 @@ constexpr int F8_BOX_BYTES = BK * 64;            // dense: [64 rows][64 codes]
 constexpr int F8_BLK = 256;                      // gathered: codes a box row (the unswizzled maximum)
 constexpr int F8_BLK_BYTES = BK * F8_BLK;        // [64 rows][256 codes] = 16 KB
 constexpr int F8_NBLK = kLat / F8_BLK;           // 2
-constexpr int F8_STAGING = 4 * BOX_BYTES;        // 32,768
-static_assert(F8_STAGING + 8 * F8_BOX_BYTES == 8 * BOX_BYTES, "the codes fill BF16 boxes 4-7 exactly");
-static_assert(F8_NBLK * F8_BLK_BYTES == 8 * F8_BOX_BYTES, "both layouts fill the same room");
-// A key tile lands in two parts: part 0 the rope box (free once QK^T has read it) and
-// latent boxes 0-1 (the first pair PV releases), part 1 latent boxes 2-7.  QK^T starts
-// on part 0 while the rest of the tile is still loading; the previous tile's latent
-// boxes are released pair by pair as soon as the PV M-tile that reads them is done.
-__device__ __constant__ int kBoxOrder[NBOX] = {8, 0, 1, 2, 3, 4, 5, 6, 7};
-constexpr int kPart0Boxes = 3;
+static_assert(4 * F8_BOX_BYTES == PAIR_BYTES && F8_BLK_BYTES == PAIR_BYTES, "a pair slot holds 4 code boxes or a block");
 constexpr int MIN_TILES = 4;                    // fewest key tiles a CTA is given
 constexpr int SPLIT_UNIT = 256;                 // batch-invariant split sizes are multiples of this
 static_assert(SPLIT_UNIT % BK == 0, "splits must be tile-aligned");
 constexpr int MAX_CTAS = 240;                   // CTAs a launch (one a SM); sizes the workspace
 constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(64, BK, false, false);
 
+// Ring positions of global tile gt (the CTA's tiles counted across its segments): pair j sits in
+// slot (4 gt + j) mod NPAIR for the ((4 gt + j) / NPAIR)-th time, the rope box in slot gt mod NROPE
+// for the (gt / NROPE)-th time.  A slot's full and empty barriers complete once a use, so a wait
+// for use u has parity u & 1.
+__device__ __forceinline__ int pair_slot(int gt, int j) { return (4 * gt + j) % NPAIR; }
+__device__ __forceinline__ uint32_t pair_use(int gt, int j) { return (uint32_t)((4 * gt + j) / NPAIR); }
+__device__ __forceinline__ int rope_slot(int gt) { return gt % NROPE; }
+__device__ __forceinline__ uint32_t rope_use(int gt) { return (uint32_t)(gt / NROPE); }
+// Shared-memory offset of key box b (0-7 latent, 8 rope) of global tile gt.
+__device__ __forceinline__ int box_off(int gt, int b) {
+    return b == 8 ? SMEM_ROPE + rope_slot(gt) * BOX_BYTES : SMEM_PAIR + pair_slot(gt, b >> 1) * PAIR_BYTES + (b & 1) * BOX_BYTES;
+}
+
+// FP8: the tile's 64 row scales land (a bulk copy or the producer's stores) in the last 256
+// bytes of its pair slot 1.  The expansion warps read them before the first round, and pair
+// slot 1 is not written before the second.
+__device__ __forceinline__ int scales_off(int gt) { return SMEM_PAIR + pair_slot(gt, 1) * PAIR_BYTES + PAIR_BYTES - BK * 4; }
+
 struct Ctrl {
-    float scales[NSTAGE][BK];          // FP8: the tile's row scales (a bulk copy; 16-byte aligned)
-    uint64_t f8_full[NSTAGE];          // FP8: codes and scales landed
-    uint64_t part_full[NSTAGE][2];     // part 0: rope + latent boxes 0-1 landed; part 1: latent boxes 2-7
-    uint64_t lat_empty[NSTAGE][4];     // latent box pair (2j, 2j+1) free: PV M-tile j done
-    uint64_t rope_empty[NSTAGE];       // rope box free: QK^T done
-    uint64_t s_full[2], s_free[2];
-    uint64_t corr_req[2], p_full, pv_done, q_full, q_free, stats_full, drain;
+    uint64_t f8_full[NROPE];           // FP8: codes and scales landed
+    uint64_t rope_full[NROPE];         // the rope box landed
+    uint64_t rope_empty[NROPE];        // PV of the slot's tile is done (its rope box and P are free)
+    uint64_t pair_full[NPAIR];         // a latent box pair landed (FP8: expanded)
+    uint64_t pair_empty[NPAIR];        // PV M-tile of the pair is done
+    uint64_t p_full[NROPE];            // P of the slot's tile written and O^T rescaled for it
+    uint64_t corr_req[NROPE];          // the tile's softmax statistics posted for the rescale warps
+    uint64_t s_full, s_free;           // S computed / read out of TMEM
+    uint64_t q_full, q_tmem_full, q_free, stats_full, stats_free, drain;
     uint32_t tmem_base;
     int abort;
-    int flag[2];
-    float alpha[2][NCOL];
+    int flag[NROPE];
+    float alpha[NROPE][NCOL];
     float row_inv_l[2][NCOL];          // by segment parity
 };
 constexpr int SMEM_TOTAL = SMEM_CTRL + (int)sizeof(Ctrl) + 1024;
@@ -152,6 +178,7 @@ struct Params {
     const int32_t *idx;         // SPARSE: [S][max_idx] row numbers of each stream's listed keys
     int32_t max_idx;
     const int32_t *pt;
+    const __nv_bfloat16 *q;     // [S*R*H][576]: the TMEM part of each column group is read from here
     __nv_bfloat16 *out;
     float *lse;
     float *ws_o;          // [slots][64][512]
@@ -283,15 +310,21 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tm, ui
 
 #define ALLW(x) __all_sync(0xffffffffu, (x))
 
-// Barrier phases: a parity wait only tells the current phase from the one before it,
-// so a barrier may be neither two phases ahead of a waiter nor two phases short of
-// the phase it waits for.  Per-tile barriers count the CTA's tiles across all its
-// segments (gt), per-segment ones (q_full, q_free, stats_full) its segments (si).
-// corr_req is double-buffered because softmax may post tiles t and t+1 before the
-// rescale group reads t; the epilogue waits stats_full before the segment's last
-// pv_done for the second reason; the first PV of a segment cannot start before the
-// rescale group, done with the previous segment's epilogue, posts its p_full, so
-// the accumulator is never overwritten while it is still being read.
+// Barrier phases: a parity wait only tells the current phase from the one before it, so a
+// barrier may be neither two phases ahead of a waiter nor two phases short of the phase it
+// waits for.  Slot barriers count the slot's uses; s_full / s_free the CTA's tiles (gt);
+// q_full, q_tmem_full, q_free, stats_full, stats_free its segments (si).  What keeps each
+// within one phase:
+//  - p_full and corr_req are indexed like the rope slots: the softmax of tile gt + 3 needs the
+//    tile to land in rope slot gt mod 3, which needs PV(gt), which needs p_full(gt) (from the
+//    softmax and the rescale warps) to have been consumed;
+//  - "PV of tile gt is done" is rope_empty of its slot: the rescale warps (before moving O^T)
+//    and the epilogue wait on it, and tile gt having landed means its slot's previous use is
+//    released, so the barrier is never two phases short;
+//  - the softmax waits stats_free (the epilogue read the previous segment's statistics) before
+//    posting a segment's stats_full, so stats_full is never two phases ahead of the epilogue;
+//  - the first PV of a segment waits p_full, which the rescale warps post only after their
+//    epilogue of the previous segment has read the accumulator.
 
 template <int MODE, bool FP8 = false>
 __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kernel(const __grid_constant__ Params p) {
@@ -314,28 +347,28 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
     DevErr *const errp = p.err;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NSTAGE; ++i) {
-            ptx::mbar_init(&c.part_full[i][0], kPart0Boxes);
-            ptx::mbar_init(&c.part_full[i][1], NBOX - kPart0Boxes);
-            for (int jm = 0; jm < 4; ++jm) ptx::mbar_init(&c.lat_empty[i][jm], 1);
+        for (int i = 0; i < NROPE; ++i) {
+            ptx::mbar_init(&c.rope_full[i], 1);
             ptx::mbar_init(&c.rope_empty[i], 1);
+            ptx::mbar_init(&c.p_full[i], 5);       // four softmax warps and the rescale warps
+            ptx::mbar_init(&c.corr_req[i], 4);
             // FP8: the codes' copies (and, for listed rows, the producer's scale stores)
             if (FP8) ptx::mbar_init(&c.f8_full[i], MODE == MODE_SPARSE ? 2 : 1);
+            c.flag[i] = 0;
         }
-        for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(&c.s_full[i], 1);
-            ptx::mbar_init(&c.s_free[i], 4);
+        for (int i = 0; i < NPAIR; ++i) {
+            ptx::mbar_init(&c.pair_full[i], 1);    // the TMA warp (BF16) or the expansion warps (FP8)
+            ptx::mbar_init(&c.pair_empty[i], 1);
         }
-        ptx::mbar_init(&c.corr_req[0], 4);
-        ptx::mbar_init(&c.corr_req[1], 4);
-        ptx::mbar_init(&c.p_full, 5);
-        ptx::mbar_init(&c.pv_done, 1);
+        ptx::mbar_init(&c.s_full, 1);
+        ptx::mbar_init(&c.s_free, 4);
         ptx::mbar_init(&c.q_full, 1);
+        ptx::mbar_init(&c.q_tmem_full, 4);
         ptx::mbar_init(&c.q_free, 1);
         ptx::mbar_init(&c.stats_full, 4);
+        ptx::mbar_init(&c.stats_free, 4);
         ptx::mbar_init(&c.drain, 2);
         c.abort = 0;
-        c.flag[0] = c.flag[1] = 0;
         ptx::fence_mbar_init();
     }
     if (warp == 9) {
@@ -352,6 +385,25 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
 
     if (warp == 8) {
         // ================= TMA producer =================
+        // Slot uses armed last (-1: never), so that no copy is left writing shared memory at exit.
+        int armed_rope[NROPE], armed_f8[NROPE], armed_pair[NPAIR];
+        for (int i = 0; i < NROPE; ++i) armed_rope[i] = armed_f8[i] = -1;
+        for (int i = 0; i < NPAIR; ++i) armed_pair[i] = -1;
+        int q_armed = -1;   // last segment whose queries were loaded
+        bool stop = false;
+        // wait until the slot's previous use is released (lane 0), then arm it for `bytes`
+        auto take_rope = [&](int gt, uint32_t bytes) -> bool {
+            const int rs = rope_slot(gt);
+            const uint32_t u = rope_use(gt);
+            if (u > 0 && !ptx::mbar_wait(&c.rope_empty[rs], (u - 1) & 1, abort, errp, 1)) return false;
+            ptx::mbar_arrive_expect_tx(&c.rope_full[rs], bytes);
+            armed_rope[rs] = (int)u;
+            return true;
+        };
+        auto free_pair = [&](int gt, int j) -> bool {
+            const uint32_t u = pair_use(gt, j);
+            return u == 0 || ptx::mbar_wait(&c.pair_empty[pair_slot(gt, j)], (u - 1) & 1, abort, errp, 1);
+        };
         if constexpr (MODE == MODE_SPARSE) {
             // Gathered key tiles: list position k0 + 2l and + 1 belong to lane l; rows 4j..4j+3
             // of every box are one gather4 by lane j (< 16), from the table's page of each row.
@@ -362,10 +414,6 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             }
             const uint64_t pol_kv = ptx::policy_evict_first();
             const uint64_t pol_q = ptx::policy_evict_last();
-            int armed[NSTAGE][2], armed_f8[NSTAGE];
-            for (int i = 0; i < NSTAGE; ++i) armed[i][0] = armed[i][1] = armed_f8[i] = -1;
-            int q_armed = -1;
-            bool stop = false;
             int gt = 0, si = 0;
             SegIter<MODE> it(p);
             Seg q;
@@ -375,10 +423,11 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                     if (si > 0 && !ptx::mbar_wait(&c.q_free, (si - 1) & 1, abort, errp, 15)) {
                         okq = 0;
                     } else {
-                        ptx::mbar_arrive_expect_tx(&c.q_full, Q_BYTES);
+                        ptx::mbar_arrive_expect_tx(&c.q_full, Q_SMEM_BOXES * QBOX_BYTES);
                         const int qrow = q.s * R_ * H_ + q.g * NCOL;
-                        for (int b = 0; b < NBOX; ++b)
-                            ptx::tma_load_2d(smem + SMEM_Q + b * QBOX_BYTES, &p.tm_q, &c.q_full, b * 64, qrow, pol_q);
+                        for (int b = 0; b < Q_SMEM_BOXES; ++b)
+                            ptx::tma_load_2d(smem + SMEM_Q + b * QBOX_BYTES, &p.tm_q, &c.q_full,
+                                             (Q_TMEM_BOXES + b) * 64, qrow, pol_q);
                     }
                 }
                 if (!__shfl_sync(0xffffffffu, okq, 0)) break;
@@ -386,8 +435,7 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                 const int32_t *list = p.idx + (size_t)q.s * p.max_idx;
                 const int rows = p.st[q.s].split;
                 for (int tl = 0; tl < q.nt; ++tl, ++gt) {
-                    const int st = gt % NSTAGE;
-                    const uint32_t ph = ((gt / NSTAGE) - 1) & 1;
+                    const int rs = rope_slot(gt);
                     const int64_t k0 = q.kb + (int64_t)tl * BK;
                     int ylat[2], yrope[2], badv = 0;
                     const char *sc_addr[2] = {nullptr, nullptr};
@@ -437,80 +485,74 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                     const int ro0 = __shfl_sync(0xffffffffu, yrope[0], 2 * jl), ro1 = __shfl_sync(0xffffffffu, yrope[1], 2 * jl);
                     const int ro2 = __shfl_sync(0xffffffffu, yrope[0], 2 * jl + 1),
                               ro3 = __shfl_sync(0xffffffffu, yrope[1], 2 * jl + 1);
-                    uint8_t *dst = smem + SMEM_KV + st * STAGE_BYTES;
                     if constexpr (FP8) {
-                        // the whole stage must be free (the codes and their expansion cover it)
+                        // the tile's rope slot and all four pair slots must be free (the codes and
+                        // their expansion cover the pairs)
                         int okw = 1;
-                        if (lane == 0 && gt >= NSTAGE) {
-                            okw = ptx::mbar_wait(&c.rope_empty[st], ph, abort, errp, 1);
-                            for (int jm = 0; okw && jm < 4; ++jm)
-                                okw = ptx::mbar_wait(&c.lat_empty[st][jm], ph, abort, errp, 1);
+                        if (lane == 0) {
+                            okw = take_rope(gt, BOX_BYTES);
+                            for (int j = 0; okw && j < 4; ++j) okw = free_pair(gt, j);
+                            if (okw) {
+                                ptx::mbar_arrive_expect_tx(&c.f8_full[rs], F8_NBLK * F8_BLK_BYTES);
+                                armed_f8[rs] = (int)rope_use(gt);
+                            }
                         }
                         if (!__shfl_sync(0xffffffffu, okw, 0)) {
                             stop = true;
                             break;
                         }
-                        if (lane == 0) {
-                            ptx::mbar_arrive_expect_tx(&c.part_full[st][0], BOX_BYTES);
-                            ptx::mbar_arrive_expect_tx(&c.f8_full[st], F8_NBLK * F8_BLK_BYTES);
-                        }
                         __syncwarp();
                         if (lane < 16) {
-                            ptx::tma_gather4(dst + 8 * BOX_BYTES + lane * 512, &p.tm_rope_rows, &c.part_full[st][0], 0,
+                            ptx::tma_gather4(smem + box_off(gt, 8) + lane * 512, &p.tm_rope_rows, &c.rope_full[rs], 0,
                                              ro0, ro1, ro2, ro3, pol_kv);
-                            // rows 4j..4j+3 of code block q: 4 x 256 bytes, unswizzled
+                            // rows 4j..4j+3 of code block qb: 4 x 256 bytes, unswizzled, in pair slot 2 + qb
                             for (int qb = 0; qb < F8_NBLK; ++qb)
-                                ptx::tma_gather4(dst + F8_STAGING + qb * F8_BLK_BYTES + lane * 4 * F8_BLK,
-                                                 &p.tm_lat_rows, &c.f8_full[st], qb * F8_BLK, la0, la1, la2, la3,
+                                ptx::tma_gather4(smem + SMEM_PAIR + pair_slot(gt, 2 + qb) * PAIR_BYTES + lane * 4 * F8_BLK,
+                                                 &p.tm_lat_rows, &c.f8_full[rs], qb * F8_BLK, la0, la1, la2, la3,
                                                  pol_kv);
                         }
                         // the row scales: each lane its two listed rows; a second arrival
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) c.scales[st][2 * lane + h] = __ldg(reinterpret_cast<const float *>(sc_addr[h]));
+                        for (int h = 0; h < 2; ++h)
+                            reinterpret_cast<float *>(smem + scales_off(gt))[2 * lane + h] =
+                                __ldg(reinterpret_cast<const float *>(sc_addr[h]));
                         __threadfence_block();
                         __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(&c.f8_full[st]);
-                        armed[st][0] = gt;
-                        armed_f8[st] = gt;
-                        continue;
-                    }
-                    for (int bi = 0; bi < NBOX; ++bi) {
-                        const int b = kBoxOrder[bi];
-                        const int part = bi < kPart0Boxes ? 0 : 1;
+                        if (lane == 0) ptx::mbar_arrive(&c.f8_full[rs]);
+                    } else {
+                    // the rope box, then the latent pairs in order
+                    for (int j = -1; j < 4; ++j) {
                         int okw = 1;
                         if (lane == 0) {
-                            if (gt >= NSTAGE) {
-                                uint64_t *e = (b == 8) ? &c.rope_empty[st] : &c.lat_empty[st][b >> 1];
-                                if (!ptx::mbar_wait(e, ph, abort, errp, 1)) okw = 0;
+                            if (j < 0) {
+                                okw = take_rope(gt, BOX_BYTES);
+                            } else {
+                                okw = free_pair(gt, j);
+                                if (okw) {
+                                    const int ps = pair_slot(gt, j);
+                                    ptx::mbar_arrive_expect_tx(&c.pair_full[ps], PAIR_BYTES);
+                                    armed_pair[ps] = (int)pair_use(gt, j);
+                                }
                             }
-                            if (okw) ptx::mbar_arrive_expect_tx(&c.part_full[st][part], BOX_BYTES);
                         }
                         if (!__shfl_sync(0xffffffffu, okw, 0)) {
                             stop = true;
                             break;
                         }
                         if (lane < 16) {
-                            if (b == 8)
-                                ptx::tma_gather4(dst + 8 * BOX_BYTES + lane * 512, &p.tm_rope_rows, &c.part_full[st][part],
+                            if (j < 0) {
+                                ptx::tma_gather4(smem + box_off(gt, 8) + lane * 512, &p.tm_rope_rows, &c.rope_full[rs],
                                                  0, ro0, ro1, ro2, ro3, pol_kv);
-                            else
-                                ptx::tma_gather4(dst + b * BOX_BYTES + lane * 512, &p.tm_lat_rows, &c.part_full[st][part],
-                                                 b * 64, la0, la1, la2, la3, pol_kv);
+                            } else {
+                                uint64_t *full = &c.pair_full[pair_slot(gt, j)];
+                                for (int h = 0; h < 2; ++h)
+                                    ptx::tma_gather4(smem + box_off(gt, 2 * j + h) + lane * 512, &p.tm_lat_rows, full,
+                                                     (2 * j + h) * 64, la0, la1, la2, la3, pol_kv);
+                            }
                         }
-                        armed[st][part] = gt;
+                    }
                     }
                     if (stop) break;
-                }
-            }
-            // no copy may still be writing shared memory when the CTA exits
-            if (lane == 0) {
-                if (q_armed >= 0) ptx::mbar_wait(&c.q_full, q_armed & 1, abort, errp, 10, 1ll << 28);
-                for (int i = 0; i < NSTAGE; ++i) {
-                    for (int h = 0; h < 2; ++h)
-                        if (armed[i][h] >= 0)
-                            ptx::mbar_wait(&c.part_full[i][h], (armed[i][h] / NSTAGE) & 1, abort, errp, 11, 1ll << 28);
-                    if (armed_f8[i] >= 0)
-                        ptx::mbar_wait(&c.f8_full[i], (armed_f8[i] / NSTAGE) & 1, abort, errp, 18, 1ll << 28);
                 }
             }
         } else if (lane == 0) {
@@ -521,26 +563,21 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             // groups of the same stream read too are kept
             const uint64_t pol_kv = ngroups > 2 ? ptx::policy_evict_last() : ptx::policy_evict_first();
             const uint64_t pol_q = ptx::policy_evict_last();
-            int armed[NSTAGE][2];   // last global tile each part barrier was armed for (-1: never)
-            int armed_f8[NSTAGE];   // FP8: the same for the codes' barrier
-            for (int i = 0; i < NSTAGE; ++i) armed[i][0] = armed[i][1] = armed_f8[i] = -1;
-            int q_armed = -1;       // last segment whose queries were loaded
-            bool stop = false;
             int gt = 0, si = 0;
             SegIter<MODE> it(p);
             Seg q;
             for (; !stop && it.next(p, q); ++si) {
-                // the query tile is reloaded once the previous segment's QK^T has read it
+                // the queries' shared-memory boxes are reloaded once the previous segment's QK^T has read them
                 if (si > 0 && !ptx::mbar_wait(&c.q_free, (si - 1) & 1, abort, errp, 15)) break;
-                ptx::mbar_arrive_expect_tx(&c.q_full, Q_BYTES);
+                ptx::mbar_arrive_expect_tx(&c.q_full, Q_SMEM_BOXES * QBOX_BYTES);
                 const int qrow = q.s * R_ * H_ + q.g * NCOL;
-                for (int b = 0; b < NBOX; ++b)
-                    ptx::tma_load_2d(smem + SMEM_Q + b * QBOX_BYTES, &p.tm_q, &c.q_full, b * 64, qrow, pol_q);
+                for (int b = 0; b < Q_SMEM_BOXES; ++b)
+                    ptx::tma_load_2d(smem + SMEM_Q + b * QBOX_BYTES, &p.tm_q, &c.q_full, (Q_TMEM_BOXES + b) * 64, qrow,
+                                     pol_q);
                 q_armed = si;
                 int cur_lp = -1, page = 0;
                 for (int tl = 0; tl < q.nt; ++tl, ++gt) {
-                    const int st = gt % NSTAGE;
-                    const uint32_t ph = ((gt / NSTAGE) - 1) & 1;
+                    const int rs = rope_slot(gt);
                     const int64_t k0 = q.kb + (int64_t)tl * BK;
                     const int lp = (int)(k0 >> 9), row = (int)(k0 & 511);
                     if (lp != cur_lp) {
@@ -554,134 +591,153 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                         }
                         page = raw;
                     }
-                    uint8_t *dst = smem + SMEM_KV + st * STAGE_BYTES;
                     if constexpr (FP8) {
-                        // the codes overwrite BF16 boxes 4-7 and their expansion every box: the
-                        // whole stage must be free; the rope box lands as on BF16 pages (part 0)
-                        if (gt >= NSTAGE) {
-                            bool okw = ptx::mbar_wait(&c.rope_empty[st], ph, abort, errp, 1);
-                            for (int jm = 0; okw && jm < 4; ++jm)
-                                okw = ptx::mbar_wait(&c.lat_empty[st][jm], ph, abort, errp, 1);
-                            if (!okw) {
+                        // the codes land in pair slots 2-3 and their expansion covers all four
+                        // pairs: every slot of the tile must be free; the rope box lands as on BF16 pages
+                        bool okw = take_rope(gt, BOX_BYTES);
+                        for (int j = 0; okw && j < 4; ++j) okw = free_pair(gt, j);
+                        if (!okw) {
+                            stop = true;
+                            break;
+                        }
+                        tma_load_4d(smem + box_off(gt, 8), &p.tm_rope, &c.rope_full[rs], 0, row, page, cache, pol_kv);
+                        ptx::mbar_arrive_expect_tx(&c.f8_full[rs], 8 * F8_BOX_BYTES + BK * 4);
+                        for (int b = 0; b < 8; ++b)
+                            tma_load_4d(smem + SMEM_PAIR + pair_slot(gt, 2 + (b >> 2)) * PAIR_BYTES + (b & 3) * F8_BOX_BYTES,
+                                        &p.tm_lat, &c.f8_full[rs], b * 64, row, page, cache, pol_kv);
+                        ptx::bulk_g2s(smem + scales_off(gt),
+                                      p.pool_base + ((size_t)cache * num_pages + page) * kF8PageBytes + kF8ScaleOff +
+                                          (size_t)row * 4,
+                                      BK * 4, &c.f8_full[rs]);
+                        armed_f8[rs] = (int)rope_use(gt);
+                    } else {
+                        // the rope box first (QK^T starts on it), then the latent pairs in order
+                        if (!take_rope(gt, BOX_BYTES)) {
+                            stop = true;
+                            break;
+                        }
+                        tma_load_4d(smem + box_off(gt, 8), &p.tm_rope, &c.rope_full[rs], 0, row, page, cache, pol_kv);
+#pragma unroll 1
+                        for (int j = 0; j < 4; ++j) {
+                            if (!free_pair(gt, j)) {
                                 stop = true;
                                 break;
                             }
-                        }
-                        ptx::mbar_arrive_expect_tx(&c.part_full[st][0], BOX_BYTES);
-                        tma_load_4d(dst + 8 * BOX_BYTES, &p.tm_rope, &c.part_full[st][0], 0, row, page, cache, pol_kv);
-                        armed[st][0] = gt;
-                        ptx::mbar_arrive_expect_tx(&c.f8_full[st], 8 * F8_BOX_BYTES + BK * 4);
-                        for (int b = 0; b < 8; ++b)
-                            tma_load_4d(dst + F8_STAGING + b * F8_BOX_BYTES, &p.tm_lat, &c.f8_full[st], b * 64, row,
-                                        page, cache, pol_kv);
-                        ptx::bulk_g2s(&c.scales[st][0],
-                                      p.pool_base + ((size_t)cache * num_pages + page) * kF8PageBytes + kF8ScaleOff +
-                                          (size_t)row * 4,
-                                      BK * 4, &c.f8_full[st]);
-                        armed_f8[st] = gt;
-                    } else {
-                        for (int bi = 0; bi < NBOX; ++bi) {
-                            const int b = kBoxOrder[bi];
-                            if (gt >= NSTAGE) {
-                                uint64_t *e = (b == 8) ? &c.rope_empty[st] : &c.lat_empty[st][b >> 1];
-                                if (!ptx::mbar_wait(e, ph, abort, errp, 1)) {
-                                    stop = true;
-                                    break;
-                                }
-                            }
-                            uint64_t *full = &c.part_full[st][bi < kPart0Boxes ? 0 : 1];
-                            ptx::mbar_arrive_expect_tx(full, BOX_BYTES);
-                            if (b == 8)
-                                tma_load_4d(dst + 8 * BOX_BYTES, &p.tm_rope, full, 0, row, page, cache, pol_kv);
-                            else
-                                tma_load_4d(dst + b * BOX_BYTES, &p.tm_lat, full, b * 64, row, page, cache, pol_kv);
-                            armed[st][bi < kPart0Boxes ? 0 : 1] = gt;
+                            const int ps = pair_slot(gt, j);
+                            ptx::mbar_arrive_expect_tx(&c.pair_full[ps], PAIR_BYTES);
+                            armed_pair[ps] = (int)pair_use(gt, j);
+                            for (int h = 0; h < 2; ++h)
+                                tma_load_4d(smem + box_off(gt, 2 * j + h), &p.tm_lat, &c.pair_full[ps], (2 * j + h) * 64,
+                                            row, page, cache, pol_kv);
                         }
                         if (stop) break;
                     }
                 }
             }
-            // no copy may still be writing shared memory when the CTA exits
-            if (q_armed >= 0) ptx::mbar_wait(&c.q_full, q_armed & 1, abort, errp, 10, 1ll << 28);
-            for (int i = 0; i < NSTAGE; ++i) {
-                for (int h = 0; h < 2; ++h)
-                    if (armed[i][h] >= 0)
-                        ptx::mbar_wait(&c.part_full[i][h], (armed[i][h] / NSTAGE) & 1, abort, errp, 11, 1ll << 28);
-                if (armed_f8[i] >= 0)
-                    ptx::mbar_wait(&c.f8_full[i], (armed_f8[i] / NSTAGE) & 1, abort, errp, 18, 1ll << 28);
-            }
         }
+        // no copy may still be writing shared memory when the CTA exits
+        if (lane == 0) {
+            if (q_armed >= 0) ptx::mbar_wait(&c.q_full, q_armed & 1, abort, errp, 10, 1ll << 28);
+            for (int i = 0; i < NROPE; ++i) {
+                if (armed_rope[i] >= 0) ptx::mbar_wait(&c.rope_full[i], armed_rope[i] & 1, abort, errp, 11, 1ll << 28);
+                if (armed_f8[i] >= 0) ptx::mbar_wait(&c.f8_full[i], armed_f8[i] & 1, abort, errp, 18, 1ll << 28);
+            }
+            for (int i = 0; i < NPAIR; ++i)
+                if (armed_pair[i] >= 0) ptx::mbar_wait(&c.pair_full[i], armed_pair[i] & 1, abort, errp, 11, 1ll << 28);
+        }
+        __syncwarp();
     } else if (warp == 9 || warp == 10) {
         // ================= MMA issuers =================
-        // Warp 9 issues QK^T tile by tile as key tiles land; warp 10 issues PV as the
-        // softmax publishes P.  Each accumulator gets its contributions in a fixed order,
-        // so timing never changes a bit.
+        // Warp 9 issues QK^T tile by tile as key boxes land; warp 10 issues PV as the softmax
+        // publishes P.  Each accumulator gets its contributions in a fixed order, so timing
+        // never changes a bit.
         const bool qk_role = warp == 9;
         const uint64_t q_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_Q), 16, 1024);
-        const uint64_t kv_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_KV), 16, 1024);
-        const uint64_t v_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_KV), BOX_BYTES, 1024);
-        const uint64_t p_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_P), 16, 1024);
-        // QK^T of global tile tq (tile tl of segment q), parts [p0, p1): S[64 columns][64 keys]
-        // (M = 64: rows 16w..16w+15 in lanes 0-15 of TMEM quadrant w)
-        auto qk_tile = [&](int tq, int tl, const Seg &q, int p0, int p1) -> bool {
-            const int st = tq % NSTAGE;
-            if (p0 == 0 && tq >= 2 && !ALLW(ptx::mbar_wait(&c.s_free[tq & 1], ((tq - 2) >> 1) & 1, abort, errp, 4)))
-                return false;
+        const uint64_t kv_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem), 16, 1024);
+        const uint64_t v_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_PAIR), BOX_BYTES, 1024);
+        const uint64_t p_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_ROPE), 16, 1024);
+        // QK^T of global tile tq (tile tl of segment q): S[64 columns][64 keys] (M = 64: rows
+        // 16w..16w+15 in lanes 0-15 of TMEM quadrant w).  Box order: rope (queries' rope box in
+        // shared memory), latent pairs 0-2 (queries in TMEM), latent pair 3 (queries in shared memory).
+        auto qk_tile = [&](int tq, int tl, const Seg &q) -> bool {
+            if (tq >= 1 && !ptx::mbar_wait_warp(&c.s_free, (tq - 1) & 1, abort, errp, 4)) return false;
+            // S has been read out (s_free) and the queries are in TMEM (q_tmem_full, waited before a
+            // segment's first tile): order the MMAs after those tcgen05 loads and stores.  The key
+            // slots need no such fence: their bytes come by TMA, ordered by the mbarriers.
+            ptx::tc_fence_after();
             const int64_t rem = q.len - (q.kb + (int64_t)tl * BK);
-            for (int part = p0; part < p1; ++part) {
-                if (!ALLW(ptx::mbar_wait(&c.part_full[st][part], (tq / NSTAGE) & 1, abort, errp, 3))) return false;
-                const int b0 = part == 0 ? 0 : kPart0Boxes, b1 = part == 0 ? kPart0Boxes : NBOX;
+            const int rs = rope_slot(tq);
+            const uint32_t ru = rope_use(tq);
+            int ps = pair_slot(tq, 0);
+            uint32_t pu = pair_use(tq, 0);
+            const uint32_t d = tmem + TMEM_S;
+            // rolled loops: this warp's code stays a few instruction-cache lines, reused every tile
+#pragma unroll 1
+            for (int j = -1; j < 4; ++j) {
+                uint64_t *full = j < 0 ? &c.rope_full[rs] : &c.pair_full[ps];
+                if (!ptx::mbar_wait_warp(full, (j < 0 ? ru : pu) & 1, abort, errp, 3)) return false;
+                const int slot_off = j < 0 ? SMEM_ROPE + rs * BOX_BYTES : SMEM_PAIR + ps * PAIR_BYTES;
+                const int nb = j < 0 ? 1 : 2;
                 if (rem < BK) {
                     // rows past the stream's end may hold NaN poison: zero them so that
                     // P = 0 times V stays 0 in the PV contraction
                     const int valid = (int)rem;
-                    for (int bi = b0; bi < b1; ++bi) {
-                        uint4 *bx = reinterpret_cast<uint4 *>(smem + SMEM_KV + st * STAGE_BYTES + kBoxOrder[bi] * BOX_BYTES);
+                    for (int h = 0; h < nb; ++h) {
+                        uint4 *bx = reinterpret_cast<uint4 *>(smem + slot_off + h * BOX_BYTES);
                         for (int k = lane; k < (BK - valid) * 8; k += 32) bx[valid * 8 + k] = make_uint4(0, 0, 0, 0);
                     }
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                 }
-                ptx::tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t d = tmem + TMEM_S + (tq & 1) * BK;
-                    for (int bi = b0; bi < b1; ++bi) {
-                        const int b = kBoxOrder[bi];
-                        const uint64_t kvd = kv_desc0 + (uint64_t)((st * STAGE_BYTES + b * BOX_BYTES) >> 4);
-                        const uint64_t qd = q_desc0 + (uint64_t)((b * QBOX_BYTES) >> 4);
+                // the whole warp walks the issue path; one elected lane issues each MMA
+#pragma unroll 1
+                for (int h = 0; h < nb; ++h) {
+                    const int b = j < 0 ? 8 : 2 * j + h;
+                    const uint64_t bd = kv_desc0 + (uint64_t)((slot_off + h * BOX_BYTES) >> 4);
+                    if (b < Q_TMEM_BOXES) {
+                        const uint32_t a = tmem + TMEM_Q + 32 * b;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) ptx::mma_bf16_ts_warp(d, a + 8 * k, bd + 2 * k, IDESC_QK, 1u);
+                    } else {
+                        const uint64_t ad = q_desc0 + (uint64_t)(((b == 8 ? 2 : b - Q_TMEM_BOXES) * QBOX_BYTES) >> 4);
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            ptx::mma_bf16_ss(d, qd + (uint64_t)k * 2, kvd + (uint64_t)k * 2, IDESC_QK,
-                                             (bi == 0 && k == 0) ? 0u : 1u);
-                    }
-                    if (part == 1) {
-                        ptx::mma_commit(&c.s_full[tq & 1]);
-                        ptx::mma_commit(&c.rope_empty[st]);
-                        if (tl == q.nt - 1) ptx::mma_commit(&c.q_free);
+                            ptx::mma_bf16_ss_warp(d, ad + 2 * k, bd + 2 * k, IDESC_QK, (b == 8 && k == 0) ? 0u : 1u);
                     }
                 }
+                if (j == 3) {
+                    ptx::mma_commit_warp(&c.s_full);
+                    if (tl == q.nt - 1) ptx::mma_commit_warp(&c.q_free);
+                }
                 __syncwarp();
+                if (j >= 0 && ++ps == NPAIR) {
+                    ps = 0;
+                    ++pu;
+                }
             }
             return true;
         };
-        // PV of global tile tv (tile tl of segment q); the latent box pair of M-tile jm is
-        // released as soon as its MMAs finish; a segment's first tile starts the accumulator
+        // PV of global tile tv (tile tl of segment q); each latent pair is released as soon as its
+        // M-tile's MMAs finish, the rope slot (P) after the last; a segment's first tile starts
+        // the accumulator
         auto pv_tile = [&](int tv, int tl, uint32_t idesc_pv) -> bool {
-            if (!ALLW(ptx::mbar_wait(&c.p_full, tv & 1, abort, errp, 5))) return false;
+            const int rs = rope_slot(tv);
+            if (!ptx::mbar_wait_warp(&c.p_full[rs], rope_use(tv) & 1, abort, errp, 5)) return false;
             ptx::tc_fence_after();
-            if (lane == 0) {
-                const int st = tv % NSTAGE;
-                const uint64_t vd = v_desc0 + (uint64_t)(st * (STAGE_BYTES >> 4));
+            {
+                const uint64_t pd = p_desc0 + (uint64_t)((rs * BOX_BYTES) >> 4);
                 const uint32_t acc0 = tl == 0 ? 0u : 1u;
-#pragma unroll
+#pragma unroll 1
                 for (int jm = 0; jm < 4; ++jm) {
+                    const int ps = pair_slot(tv, jm);
+                    const uint64_t vd = v_desc0 + (uint64_t)((ps * PAIR_BYTES) >> 4);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
-                        ptx::mma_bf16_ss(tmem + TMEM_O + jm * 64, vd + (uint64_t)((2 * jm * BOX_BYTES + k * 2048) >> 4),
-                                         p_desc0 + (uint64_t)((k * 32) >> 4), idesc_pv, k > 0 ? 1u : acc0);
-                    ptx::mma_commit(&c.lat_empty[st][jm]);
+                        ptx::mma_bf16_ss_warp(tmem + TMEM_O + jm * 64, vd + (uint64_t)((k * 2048) >> 4),
+                                              pd + (uint64_t)((k * 32) >> 4), idesc_pv, k > 0 ? 1u : acc0);
+                    ptx::mma_commit_warp(&c.pair_empty[ps]);
                 }
-                ptx::mma_commit(&c.pv_done);
+                ptx::mma_commit_warp(&c.rope_empty[rs]);
             }
             __syncwarp();
             return true;
@@ -694,8 +750,9 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             const int ncols = min(NCOL, ncols_all - q.g * NCOL);
             const uint32_t idesc_pv = ptx::idesc_bf16_f32(128, (ncols + 15) & ~15, true, false);
             if (qk_role) {
-                ok = ALLW(ptx::mbar_wait(&c.q_full, si & 1, abort, errp, 2));
-                for (int tl = 0; ok && tl < q.nt; ++tl) ok = qk_tile(gt + tl, tl, q, 0, 2);
+                ok = ptx::mbar_wait_warp(&c.q_full, si & 1, abort, errp, 2) &&
+                     ptx::mbar_wait_warp(&c.q_tmem_full, si & 1, abort, errp, 2);
+                for (int tl = 0; ok && tl < q.nt; ++tl) ok = qk_tile(gt + tl, tl, q);
             } else {
                 for (int tl = 0; ok && tl < q.nt; ++tl) ok = pv_tile(gt + tl, tl, idesc_pv);
             }
@@ -711,8 +768,7 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
         // ================= FP8 expansion (warps 11-14): half a tile row a thread =================
         // Box b's 64 codes of row r become bf16(code * scale_r), written 128B-swizzled into BF16
         // box b (16-byte chunk j of the row at j ^ (r & 7)); thread (r, hf) does codes 32hf..+31.
-        // Each finished box is one arrival on the part barrier the MMA issuers wait for, after a
-        // proxy fence.
+        // Each finished pair is one arrival on its full barrier, after a proxy fence.
         const int ft = (int)threadIdx.x - THREADS;
         const int r = ft >> 1, hf = ft & 1;
         bool ok = true;
@@ -721,24 +777,23 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
         Seg q;
         while (ok && it.next(p, q)) {
             for (int tl = 0; tl < q.nt; ++tl, ++gt) {
-                const int st = gt % NSTAGE;
-                const bool landed = ptx::mbar_wait(&c.f8_full[st], (gt / NSTAGE) & 1, abort, errp, 16);
+                const int rs = rope_slot(gt);
+                const bool landed = ptx::mbar_wait_warp(&c.f8_full[rs], rope_use(gt) & 1, abort, errp, 16);
                 if (ptx::named_bar_or(2, F8_THREADS, !landed || *abort)) {
                     ok = false;
                     break;
                 }
-                uint8_t *stage = smem + SMEM_KV + st * STAGE_BYTES;
-                const float sc = c.scales[st][r];
-                // two boxes a round: {0,1} (part 0), then {2,3}, {4,5}, {6,7} (part 1)
+                const float sc = reinterpret_cast<const float *>(smem + scales_off(gt))[r];
+                // one pair a round: {0,1}, {2,3}, {4,5}, {6,7}
 #pragma unroll 1
                 for (int b0 = 0; b0 < 8; b0 += 2) {
                     uint4 cv[2][2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int b = b0 + u;   // codes 64b.. of row r, in the dense or the gathered layout
-                        const int off = MODE == MODE_SPARSE ? (b >> 2) * F8_BLK_BYTES + r * F8_BLK + (b & 3) * 64
-                                                            : b * F8_BOX_BYTES + r * 64;
-                        const uint4 *src = reinterpret_cast<const uint4 *>(stage + F8_STAGING + off + hf * 32);
+                        const int off = SMEM_PAIR + pair_slot(gt, 2 + (b >> 2)) * PAIR_BYTES +
+                                        (MODE == MODE_SPARSE ? r * F8_BLK + (b & 3) * 64 : (b & 3) * F8_BOX_BYTES + r * 64);
+                        const uint4 *src = reinterpret_cast<const uint4 *>(smem + off + hf * 32);
                         cv[u][0] = src[0];
                         cv[u][1] = src[1];
                     }
@@ -762,7 +817,7 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                     if (b0 == 6) ptx::named_bar(2, F8_THREADS);
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        uint8_t *dst = stage + (b0 + u) * BOX_BYTES + r * 128;
+                        uint8_t *dst = smem + box_off(gt, b0 + u) + r * 128;
 #pragma unroll
                         for (int jj = 0; jj < 4; ++jj) {
                             const int j = 4 * hf + jj;
@@ -772,10 +827,7 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                     }
                     ptx::fence_proxy_async_smem();
                     ptx::named_bar(2, F8_THREADS);
-                    if (ft == 0) {
-                        ptx::mbar_arrive(&c.part_full[st][b0 < 2 ? 0 : 1]);
-                        ptx::mbar_arrive(&c.part_full[st][b0 < 2 ? 0 : 1]);
-                    }
+                    if (ft == 0) ptx::mbar_arrive(&c.pair_full[pair_slot(gt, b0 >> 1)]);
                 }
             }
         }
@@ -794,6 +846,34 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
         for (; ok && it.next(p, q); ++si) {
             const int col0 = q.g * NCOL;
             const int ncols = ncols_all - col0;
+            {
+                // The segment's queries, latent values 0-383, into TMEM (A of QK^T): lane i < 16 of
+                // this quadrant holds column 16 q4 + i.  Every QK^T of the previous segment has
+                // completed: this warp has seen its last S.
+                const int m = 16 * q4 + (lane & 15);
+                const bool live = lane < 16 && m < ncols;
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((size_t)q.s * ncols_all + col0 + (live ? m : 0)) * kDk);
+#pragma unroll 1
+                for (int c2 = 0; c2 < Q_TMEM_BOXES; c2 += 2) {
+                    uint32_t v[2][32];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint4 x = live ? __ldg(src + (c2 + h) * 8 + i) : make_uint4(0, 0, 0, 0);
+                            v[h][4 * i] = x.x;
+                            v[h][4 * i + 1] = x.y;
+                            v[h][4 * i + 2] = x.z;
+                            v[h][4 * i + 3] = x.w;
+                        }
+                    ptx::tmem_st32(lane_base + TMEM_Q + 32 * c2, v[0]);
+                    ptx::tmem_st32(lane_base + TMEM_Q + 32 * (c2 + 1), v[1]);
+                }
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&c.q_tmem_full);
+            }
             const bool act0 = r0 < ncols, act1 = r1 < ncols;
             // last visible key of each row's column
             const int64_t pos0 = q.len - R_ + (act0 ? (col0 + r0) / H_ : 0);
@@ -801,18 +881,19 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
             for (int tl = 0; tl < q.nt; ++tl) {
                 const int t = gt + tl;
+                const int rs = rope_slot(t);
                 const int64_t k0 = q.kb + (int64_t)tl * BK;
-                if (!ALLW(ptx::mbar_wait(&c.s_full[t & 1], (t >> 1) & 1, abort, errp, 7))) {
+                if (!ptx::mbar_wait_warp(&c.s_full, t & 1, abort, errp, 7)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 uint32_t r[32];
-                ptx::tmem_ld_16x256b_x8(lane_base + TMEM_S + (t & 1) * BK, r);
+                ptx::tmem_ld_16x256b_x8(lane_base + TMEM_S, r);
                 ptx::tmem_ld_wait();
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&c.s_free[t & 1]);
+                if (lane == 0) ptx::mbar_arrive(&c.s_free);
                 // keys outside a row's range become -inf; the maximum is taken before
                 // scaling (the scale is positive) and the scale is folded into the
                 // exponent's FFMA: p = 2^(s * scale*log2(e) - m_ref)
@@ -862,11 +943,10 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                     l1 *= a1;
                 }
                 if ((lane & 3) == 0) {
-                    c.alpha[t & 1][r0] = a0;
-                    c.alpha[t & 1][r1] = a1;
+                    c.alpha[rs][r0] = a0;
+                    c.alpha[rs][r1] = a1;
                 }
-                if (__any_sync(0xffffffffu, (a0 != 1.f || a1 != 1.f) && tl > 0) && lane == 0)
-                    atomicOr(&c.flag[t & 1], 1);
+                if (__any_sync(0xffffffffu, (a0 != 1.f || a1 != 1.f) && tl > 0) && lane == 0) atomicOr(&c.flag[rs], 1);
                 const float mr0 = (m0 == -INFINITY) ? 0.f : m0, mr1 = (m1 == -INFINITY) ? 0.f : m1;
                 uint32_t pk0[8], pk1[8];
 #pragma unroll
@@ -881,14 +961,12 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                     pk1[j] = ptx::pack_bf16x2(e10, e11);
                 }
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&c.corr_req[t & 1]);
-                if (t >= 1 && !ALLW(ptx::mbar_wait(&c.pv_done, (t - 1) & 1, abort, errp, 8))) {
-                    ok = false;
-                    break;
-                }
-                // P rows as bf16, 128B-swizzled K-major: keys 8j.. of row r in 16-byte chunk j ^ (r & 7)
-                uint8_t *p0 = smem + SMEM_P + r0 * 128 + 2 * kq;
-                uint8_t *p1 = smem + SMEM_P + r1 * 128 + 2 * kq;
+                if (lane == 0) ptx::mbar_arrive(&c.corr_req[rs]);
+                // P rows as bf16, 128B-swizzled K-major, into the tile's rope slot (QK^T has read
+                // the rope box: S is complete): keys 8j.. of row r in 16-byte chunk j ^ (r & 7)
+                uint8_t *pb = smem + SMEM_ROPE + rs * BOX_BYTES;
+                uint8_t *p0 = pb + r0 * 128 + 2 * kq;
+                uint8_t *p1 = pb + r1 * 128 + 2 * kq;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     *reinterpret_cast<uint32_t *>(p0 + ((j ^ (r0 & 7)) << 4)) = pk0[j];
@@ -896,7 +974,7 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                 }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&c.p_full);
+                if (lane == 0) ptx::mbar_arrive(&c.p_full[rs]);
             }
             if (!ok) break;
             // the row sums: each thread holds 16 of a row's keys a tile
@@ -904,6 +982,11 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
             l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
             l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+            // the epilogue of the previous segment must have read its statistics
+            if (si > 0 && !ptx::mbar_wait_warp(&c.stats_free, (si - 1) & 1, abort, errp, 17)) {
+                ok = false;
+                break;
+            }
             if ((lane & 3) == 0) {
                 c.row_inv_l[si & 1][r0] = l0 > 0.f ? 1.f / l0 : 0.f;
                 c.row_inv_l[si & 1][r1] = l1 > 0.f ? 1.f / l1 : 0.f;
@@ -937,10 +1020,13 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             const int npv = (ncols + 15) & ~15;
             for (int tl = 0; tl < q.nt; ++tl) {
                 const int t = gt + tl;
-                if (!ALLW(ptx::mbar_wait(&c.corr_req[t & 1], (t >> 1) & 1, abort, errp, 12))) ok = false;
-                const bool do_corr = ok && c.flag[t & 1] != 0;
+                const int rs = rope_slot(t);
+                if (!ptx::mbar_wait_warp(&c.corr_req[rs], rope_use(t) & 1, abort, errp, 12)) ok = false;
+                const bool do_corr = ok && c.flag[rs] != 0;   // set only for tl > 0
                 if (do_corr) {
-                    if (!ALLW(ptx::mbar_wait(&c.pv_done, (t - 1) & 1, abort, errp, 13))) ok = false;
+                    // O^T holds every tile before t once PV(t - 1) is done
+                    if (!ptx::mbar_wait_warp(&c.rope_empty[rope_slot(t - 1)], rope_use(t - 1) & 1, abort, errp, 13))
+                        ok = false;
                     if (ok) {
                         ptx::tc_fence_after();
                         for (int jm = 0; jm < 4; ++jm)
@@ -951,7 +1037,7 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                                 ptx::tmem_ld_wait();
 #pragma unroll
                                 for (int k = 0; k < 32; ++k)
-                                    v[k] = __float_as_uint(__uint_as_float(v[k]) * c.alpha[t & 1][h2 + k]);
+                                    v[k] = __float_as_uint(__uint_as_float(v[k]) * c.alpha[rs][h2 + k]);
                                 ptx::tmem_st32(a, v);
                             }
                         ptx::tmem_st_wait();
@@ -965,16 +1051,15 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                     break;
                 }
                 if (threadIdx.x == 0) {
-                    c.flag[t & 1] = 0;
-                    ptx::mbar_arrive(&c.p_full);
+                    c.flag[rs] = 0;
+                    ptx::mbar_arrive(&c.p_full[rs]);
                 }
             }
+            const int tlast = gt + q.nt - 1;
             if (ok && !*abort) {
-                // stats_full first: the softmax warps post it only after they saw the
-                // second-to-last PV of the segment complete, so pv_done is then at most one
-                // phase short of the last one and its parity wait cannot pass early
-                if (!ALLW(ptx::mbar_wait(&c.stats_full, si & 1, abort, errp, 14))) ok = false;
-                if (ok && !ALLW(ptx::mbar_wait(&c.pv_done, (gt + q.nt - 1) & 1, abort, errp, 9))) ok = false;
+                if (!ptx::mbar_wait_warp(&c.stats_full, si & 1, abort, errp, 14)) ok = false;
+                if (ok && !ptx::mbar_wait_warp(&c.rope_empty[rope_slot(tlast)], rope_use(tlast) & 1, abort, errp, 9))
+                    ok = false;
             }
             if (ptx::named_bar_or(1, 128, !ok || *abort)) {
                 ok = false;
@@ -1001,6 +1086,9 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                         }
                     }
                 }
+            // the statistics are read: the softmax may post the next segment's
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&c.stats_free);
             gt += q.nt;
         }
     }
@@ -1423,6 +1511,7 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
         if (!encode(&p.tm_q, const_cast<void *>(d_q), 2, dims, strides, box)) return TF_E_CUDA;
     }
     p.pt = d_pt;
+    p.q = static_cast<const __nv_bfloat16 *>(d_q);
     p.out = static_cast<__nv_bfloat16 *>(d_out);
     p.lse = d_lse;
     p.err = pool->err;

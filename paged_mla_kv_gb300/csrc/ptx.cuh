@@ -55,9 +55,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // clock cycles (2^31 by default: about a second at 2 GHz).  The clock is the SM's
 // own cycle counter, read only every 256 polls so the common path is the poll
 // itself.  On expiry: record TF_E_TIMEOUT (detail = site), set *abort, return false.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, DevErr *err,
-                                          int site, long long limit = (1ll << 31)) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The polling loop is out of line: the kernels wait at many sites, and one copy of the loop
+// keeps their hot code small in the instruction cache; the first poll stays inline.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort, DevErr *err,
+                                            int site, long long limit) {
     const long long t0 = clock64();
     for (uint32_t spins = 1;; ++spins) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -70,6 +71,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
             }
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, DevErr *err,
+                                          int site, long long limit = (1ll << 31)) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort, err, site, limit);
+}
+
+// The same wait for a whole warp: every lane polls and the warp leaves with one decision.
+// (A single polling lane with the others parked at __syncwarp was measured slower: the warp saw
+// completed phases hundreds of cycles later.)
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort, DevErr *err,
+                                               int site, long long limit = (1ll << 31)) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, err, site, limit));
 }
 
 // ---- programmatic dependent launch ------------------------------------------
@@ -206,6 +221,50 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]; issued by one thread.  A of an M = 64 MMA uses the lanes
+// of the M = 64 accumulator (row m at lane 32 (m / 16) + m % 16), K along the columns, two
+// bf16 values a 32-bit column (value k in column k / 2, the low half for even k).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Warp-wide forms: every lane of the warp executes them with the same operands and one elected
+// lane issues.  Keeping the whole warp converged on the issue path lets the compiler hold the
+// descriptors as warp-uniform values.
+__device__ __forceinline__ void mma_bf16_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_bf16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_warp(uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
         : "memory");
 }
 
