@@ -122,10 +122,9 @@ __device__ __forceinline__ int box_off(int gt, int b) {
 __device__ __forceinline__ int scales_off(int gt) { return SMEM_PAIR + pair_slot(gt, 1) * PAIR_BYTES + PAIR_BYTES - BK * 4; }
 
 struct Ctrl {
-    uint64_t f8_full[NROPE];           // FP8: codes and scales landed
-    uint64_t rope_full[NROPE];         // the rope box landed
+    uint64_t f8_full[NROPE];           // FP8: the tile's codes, scales and rope box landed
+    uint64_t tile_full[NROPE];         // every box of the tile landed (FP8: expanded); by rope slot
     uint64_t rope_empty[NROPE];        // PV of the slot's tile is done (its rope box and P are free)
-    uint64_t pair_full[NPAIR];         // a latent box pair landed (FP8: expanded)
     uint64_t pair_empty[NPAIR];        // PV M-tile of the pair is done
     uint64_t p_full[NROPE];            // P of the slot's tile written and O^T rescaled for it
     uint64_t corr_req[NROPE];          // the tile's softmax statistics posted for the rescale warps
@@ -348,7 +347,9 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NROPE; ++i) {
-            ptx::mbar_init(&c.rope_full[i], 1);
+            // BF16: the TMA warp's one arrival with the tile's bytes; FP8: one arrival a pair the
+            // expansion warps finish
+            ptx::mbar_init(&c.tile_full[i], FP8 ? 4 : 1);
             ptx::mbar_init(&c.rope_empty[i], 1);
             ptx::mbar_init(&c.p_full[i], 5);       // four softmax warps and the rescale warps
             ptx::mbar_init(&c.corr_req[i], 4);
@@ -357,7 +358,6 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             c.flag[i] = 0;
         }
         for (int i = 0; i < NPAIR; ++i) {
-            ptx::mbar_init(&c.pair_full[i], 1);    // the TMA warp (BF16) or the expansion warps (FP8)
             ptx::mbar_init(&c.pair_empty[i], 1);
         }
         ptx::mbar_init(&c.s_full, 1);
@@ -386,18 +386,21 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
     if (warp == 8) {
         // ================= TMA producer =================
         // Slot uses armed last (-1: never), so that no copy is left writing shared memory at exit.
-        int armed_rope[NROPE], armed_f8[NROPE], armed_pair[NPAIR];
-        for (int i = 0; i < NROPE; ++i) armed_rope[i] = armed_f8[i] = -1;
-        for (int i = 0; i < NPAIR; ++i) armed_pair[i] = -1;
+        int armed_tile[NROPE], armed_f8[NROPE];
+        for (int i = 0; i < NROPE; ++i) armed_tile[i] = armed_f8[i] = -1;
         int q_armed = -1;   // last segment whose queries were loaded
         bool stop = false;
         // wait until the slot's previous use is released (lane 0), then arm it for `bytes`
-        auto take_rope = [&](int gt, uint32_t bytes) -> bool {
+        // wait until the tile's rope slot is released by PV of its previous tile (lane 0); BF16
+        // pages then arm the tile's landing barrier for all nine boxes
+        auto take_rope = [&](int gt) -> bool {
             const int rs = rope_slot(gt);
             const uint32_t u = rope_use(gt);
             if (u > 0 && !ptx::mbar_wait(&c.rope_empty[rs], (u - 1) & 1, abort, errp, 1)) return false;
-            ptx::mbar_arrive_expect_tx(&c.rope_full[rs], bytes);
-            armed_rope[rs] = (int)u;
+            if (!FP8) {
+                ptx::mbar_arrive_expect_tx(&c.tile_full[rs], NBOX * BOX_BYTES);
+                armed_tile[rs] = (int)u;
+            }
             return true;
         };
         auto free_pair = [&](int gt, int j) -> bool {
@@ -490,10 +493,10 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                         // their expansion cover the pairs)
                         int okw = 1;
                         if (lane == 0) {
-                            okw = take_rope(gt, BOX_BYTES);
+                            okw = take_rope(gt);
                             for (int j = 0; okw && j < 4; ++j) okw = free_pair(gt, j);
                             if (okw) {
-                                ptx::mbar_arrive_expect_tx(&c.f8_full[rs], F8_NBLK * F8_BLK_BYTES);
+                                ptx::mbar_arrive_expect_tx(&c.f8_full[rs], F8_NBLK * F8_BLK_BYTES + BOX_BYTES);
                                 armed_f8[rs] = (int)rope_use(gt);
                             }
                         }
@@ -503,7 +506,7 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                         }
                         __syncwarp();
                         if (lane < 16) {
-                            ptx::tma_gather4(smem + box_off(gt, 8) + lane * 512, &p.tm_rope_rows, &c.rope_full[rs], 0,
+                            ptx::tma_gather4(smem + box_off(gt, 8) + lane * 512, &p.tm_rope_rows, &c.f8_full[rs], 0,
                                              ro0, ro1, ro2, ro3, pol_kv);
                             // rows 4j..4j+3 of code block qb: 4 x 256 bytes, unswizzled, in pair slot 2 + qb
                             for (int qb = 0; qb < F8_NBLK; ++qb)
@@ -524,16 +527,7 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                     for (int j = -1; j < 4; ++j) {
                         int okw = 1;
                         if (lane == 0) {
-                            if (j < 0) {
-                                okw = take_rope(gt, BOX_BYTES);
-                            } else {
-                                okw = free_pair(gt, j);
-                                if (okw) {
-                                    const int ps = pair_slot(gt, j);
-                                    ptx::mbar_arrive_expect_tx(&c.pair_full[ps], PAIR_BYTES);
-                                    armed_pair[ps] = (int)pair_use(gt, j);
-                                }
-                            }
+                            okw = j < 0 ? take_rope(gt) : free_pair(gt, j);
                         }
                         if (!__shfl_sync(0xffffffffu, okw, 0)) {
                             stop = true;
@@ -541,12 +535,11 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                         }
                         if (lane < 16) {
                             if (j < 0) {
-                                ptx::tma_gather4(smem + box_off(gt, 8) + lane * 512, &p.tm_rope_rows, &c.rope_full[rs],
+                                ptx::tma_gather4(smem + box_off(gt, 8) + lane * 512, &p.tm_rope_rows, &c.tile_full[rs],
                                                  0, ro0, ro1, ro2, ro3, pol_kv);
                             } else {
-                                uint64_t *full = &c.pair_full[pair_slot(gt, j)];
                                 for (int h = 0; h < 2; ++h)
-                                    ptx::tma_gather4(smem + box_off(gt, 2 * j + h) + lane * 512, &p.tm_lat_rows, full,
+                                    ptx::tma_gather4(smem + box_off(gt, 2 * j + h) + lane * 512, &p.tm_lat_rows, &c.tile_full[rs],
                                                      (2 * j + h) * 64, la0, la1, la2, la3, pol_kv);
                             }
                         }
@@ -594,14 +587,14 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                     if constexpr (FP8) {
                         // the codes land in pair slots 2-3 and their expansion covers all four
                         // pairs: every slot of the tile must be free; the rope box lands as on BF16 pages
-                        bool okw = take_rope(gt, BOX_BYTES);
+                        bool okw = take_rope(gt);
                         for (int j = 0; okw && j < 4; ++j) okw = free_pair(gt, j);
                         if (!okw) {
                             stop = true;
                             break;
                         }
-                        tma_load_4d(smem + box_off(gt, 8), &p.tm_rope, &c.rope_full[rs], 0, row, page, cache, pol_kv);
-                        ptx::mbar_arrive_expect_tx(&c.f8_full[rs], 8 * F8_BOX_BYTES + BK * 4);
+                        ptx::mbar_arrive_expect_tx(&c.f8_full[rs], BOX_BYTES + 8 * F8_BOX_BYTES + BK * 4);
+                        tma_load_4d(smem + box_off(gt, 8), &p.tm_rope, &c.f8_full[rs], 0, row, page, cache, pol_kv);
                         for (int b = 0; b < 8; ++b)
                             tma_load_4d(smem + SMEM_PAIR + pair_slot(gt, 2 + (b >> 2)) * PAIR_BYTES + (b & 3) * F8_BOX_BYTES,
                                         &p.tm_lat, &c.f8_full[rs], b * 64, row, page, cache, pol_kv);
@@ -612,22 +605,19 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                         armed_f8[rs] = (int)rope_use(gt);
                     } else {
                         // the rope box first (QK^T starts on it), then the latent pairs in order
-                        if (!take_rope(gt, BOX_BYTES)) {
+                        if (!take_rope(gt)) {
                             stop = true;
                             break;
                         }
-                        tma_load_4d(smem + box_off(gt, 8), &p.tm_rope, &c.rope_full[rs], 0, row, page, cache, pol_kv);
+                        tma_load_4d(smem + box_off(gt, 8), &p.tm_rope, &c.tile_full[rs], 0, row, page, cache, pol_kv);
 #pragma unroll 1
                         for (int j = 0; j < 4; ++j) {
                             if (!free_pair(gt, j)) {
                                 stop = true;
                                 break;
                             }
-                            const int ps = pair_slot(gt, j);
-                            ptx::mbar_arrive_expect_tx(&c.pair_full[ps], PAIR_BYTES);
-                            armed_pair[ps] = (int)pair_use(gt, j);
                             for (int h = 0; h < 2; ++h)
-                                tma_load_4d(smem + box_off(gt, 2 * j + h), &p.tm_lat, &c.pair_full[ps], (2 * j + h) * 64,
+                                tma_load_4d(smem + box_off(gt, 2 * j + h), &p.tm_lat, &c.tile_full[rs], (2 * j + h) * 64,
                                             row, page, cache, pol_kv);
                         }
                         if (stop) break;
@@ -639,11 +629,9 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
         if (lane == 0) {
             if (q_armed >= 0) ptx::mbar_wait(&c.q_full, q_armed & 1, abort, errp, 10, 1ll << 28);
             for (int i = 0; i < NROPE; ++i) {
-                if (armed_rope[i] >= 0) ptx::mbar_wait(&c.rope_full[i], armed_rope[i] & 1, abort, errp, 11, 1ll << 28);
+                if (armed_tile[i] >= 0) ptx::mbar_wait(&c.tile_full[i], armed_tile[i] & 1, abort, errp, 11, 1ll << 28);
                 if (armed_f8[i] >= 0) ptx::mbar_wait(&c.f8_full[i], armed_f8[i] & 1, abort, errp, 18, 1ll << 28);
             }
-            for (int i = 0; i < NPAIR; ++i)
-                if (armed_pair[i] >= 0) ptx::mbar_wait(&c.pair_full[i], armed_pair[i] & 1, abort, errp, 11, 1ll << 28);
         }
         __syncwarp();
     } else if (warp == 9 || warp == 10) {
@@ -660,61 +648,45 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
         // 16w..16w+15 in lanes 0-15 of TMEM quadrant w).  Box order: rope (queries' rope box in
         // shared memory), latent pairs 0-2 (queries in TMEM), latent pair 3 (queries in shared memory).
         auto qk_tile = [&](int tq, int tl, const Seg &q) -> bool {
-            if (tq >= 1 && !ptx::mbar_wait_warp(&c.s_free, (tq - 1) & 1, abort, errp, 4)) return false;
-            // S has been read out (s_free) and the queries are in TMEM (q_tmem_full, waited before a
-            // segment's first tile): order the MMAs after those tcgen05 loads and stores.  The key
-            // slots need no such fence: their bytes come by TMA, ordered by the mbarriers.
-            ptx::tc_fence_after();
-            const int64_t rem = q.len - (q.kb + (int64_t)tl * BK);
             const int rs = rope_slot(tq);
-            const uint32_t ru = rope_use(tq);
-            int ps = pair_slot(tq, 0);
-            uint32_t pu = pair_use(tq, 0);
-            const uint32_t d = tmem + TMEM_S;
-            // rolled loops: this warp's code stays a few instruction-cache lines, reused every tile
-#pragma unroll 1
-            for (int j = -1; j < 4; ++j) {
-                uint64_t *full = j < 0 ? &c.rope_full[rs] : &c.pair_full[ps];
-                if (!ptx::mbar_wait_warp(full, (j < 0 ? ru : pu) & 1, abort, errp, 3)) return false;
-                const int slot_off = j < 0 ? SMEM_ROPE + rs * BOX_BYTES : SMEM_PAIR + ps * PAIR_BYTES;
-                const int nb = j < 0 ? 1 : 2;
-                if (rem < BK) {
-                    // rows past the stream's end may hold NaN poison: zero them so that
-                    // P = 0 times V stays 0 in the PV contraction
-                    const int valid = (int)rem;
-                    for (int h = 0; h < nb; ++h) {
-                        uint4 *bx = reinterpret_cast<uint4 *>(smem + slot_off + h * BOX_BYTES);
-                        for (int k = lane; k < (BK - valid) * 8; k += 32) bx[valid * 8 + k] = make_uint4(0, 0, 0, 0);
-                    }
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
+            // S has been read out (s_free) and every box of the tile has landed (one barrier a tile:
+            // a wait costs about as long as four MMAs, so the tile's 36 MMAs go out in one run)
+            if (tq >= 1 && !ptx::mbar_wait_warp(&c.s_free, (tq - 1) & 1, abort, errp, 4)) return false;
+            if (!ptx::mbar_wait_warp(&c.tile_full[rs], rope_use(tq) & 1, abort, errp, 3)) return false;
+            const int64_t rem = q.len - (q.kb + (int64_t)tl * BK);
+            if (rem < BK) {
+                // rows past the stream's end may hold NaN poison: zero them so that P = 0 times V
+                // stays 0 in the PV contraction
+                const int valid = (int)rem;
+                for (int b = 0; b < NBOX; ++b) {
+                    uint4 *bx = reinterpret_cast<uint4 *>(smem + box_off(tq, b));
+                    for (int k = lane; k < (BK - valid) * 8; k += 32) bx[valid * 8 + k] = make_uint4(0, 0, 0, 0);
                 }
-                // the whole warp walks the issue path; one elected lane issues each MMA
-#pragma unroll 1
-                for (int h = 0; h < nb; ++h) {
-                    const int b = j < 0 ? 8 : 2 * j + h;
-                    const uint64_t bd = kv_desc0 + (uint64_t)((slot_off + h * BOX_BYTES) >> 4);
-                    if (b < Q_TMEM_BOXES) {
-                        const uint32_t a = tmem + TMEM_Q + 32 * b;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) ptx::mma_bf16_ts_warp(d, a + 8 * k, bd + 2 * k, IDESC_QK, 1u);
-                    } else {
-                        const uint64_t ad = q_desc0 + (uint64_t)(((b == 8 ? 2 : b - Q_TMEM_BOXES) * QBOX_BYTES) >> 4);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            ptx::mma_bf16_ss_warp(d, ad + 2 * k, bd + 2 * k, IDESC_QK, (b == 8 && k == 0) ? 0u : 1u);
-                    }
-                }
-                if (j == 3) {
-                    ptx::mma_commit_warp(&c.s_full);
-                    if (tl == q.nt - 1) ptx::mma_commit_warp(&c.q_free);
-                }
+                ptx::fence_proxy_async_smem();
                 __syncwarp();
-                if (j >= 0 && ++ps == NPAIR) {
-                    ps = 0;
-                    ++pu;
-                }
             }
+            // order the MMAs after the softmax's TMEM loads of S (s_free) and the queries' TMEM
+            // stores (q_tmem_full, waited before a segment's first tile); the key boxes come by
+            // TMA and need no such fence
+            ptx::tc_fence_after();
+            const uint32_t d = tmem + TMEM_S;
+            // the rope box (queries' rope box in shared memory) starts S, then the latent pairs;
+            // a rolled loop keeps this warp's code small in the instruction cache
+            ptx::mma4_bf16_ss_warp(d, q_desc0 + (uint64_t)((2 * QBOX_BYTES) >> 4),
+                                   kv_desc0 + (uint64_t)((SMEM_ROPE + rs * BOX_BYTES) >> 4), IDESC_QK, 1u);
+            int ps = pair_slot(tq, 0);
+#pragma unroll 1
+            for (int b = 0; b < 8; ++b) {
+                const uint64_t bd = kv_desc0 + (uint64_t)((SMEM_PAIR + ps * PAIR_BYTES + (b & 1) * BOX_BYTES) >> 4);
+                if (b < Q_TMEM_BOXES)
+                    ptx::mma4_bf16_ts_warp(d, tmem + TMEM_Q + 32 * b, bd, IDESC_QK);
+                else
+                    ptx::mma4_bf16_ss_warp(d, q_desc0 + (uint64_t)(((b - Q_TMEM_BOXES) * QBOX_BYTES) >> 4), bd, IDESC_QK,
+                                           0u);
+                if ((b & 1) && ++ps == NPAIR) ps = 0;
+            }
+            ptx::mma_commit_warp(&c.s_full);
+            if (tl == q.nt - 1) ptx::mma_commit_warp(&c.q_free);
             return true;
         };
         // PV of global tile tv (tile tl of segment q); each latent pair is released as soon as its
@@ -731,10 +703,8 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                 for (int jm = 0; jm < 4; ++jm) {
                     const int ps = pair_slot(tv, jm);
                     const uint64_t vd = v_desc0 + (uint64_t)((ps * PAIR_BYTES) >> 4);
-#pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        ptx::mma_bf16_ss_warp(tmem + TMEM_O + jm * 64, vd + (uint64_t)((k * 2048) >> 4),
-                                              pd + (uint64_t)((k * 32) >> 4), idesc_pv, k > 0 ? 1u : acc0);
+                    // K = 64 keys in four steps: 16 keys of V^T (2 KB of the pair slot), 16 keys of P (32 bytes)
+                    ptx::mma4_bf16_ss_step_warp(tmem + TMEM_O + jm * 64, vd, pd, idesc_pv, acc0, 2048 >> 4, 32 >> 4);
                     ptx::mma_commit_warp(&c.pair_empty[ps]);
                 }
                 ptx::mma_commit_warp(&c.rope_empty[rs]);
@@ -827,7 +797,7 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                     }
                     ptx::fence_proxy_async_smem();
                     ptx::named_bar(2, F8_THREADS);
-                    if (ft == 0) ptx::mbar_arrive(&c.pair_full[pair_slot(gt, b0 >> 1)]);
+                    if (ft == 0) ptx::mbar_arrive(&c.tile_full[rs]);
                 }
             }
         }
