@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the short runs of the other workloads reported under 'workloads'")
     return ap.parse_args()
 
 
@@ -456,30 +458,15 @@ def topk_main(args, rank, world, pg, peaks, peak_src):
         print(json.dumps(line), flush=True)
 
 
-def main():
-    args = parse()
-    rank, world, local = dist_env()
-    if args.impl == "reference":
-        reference_arm(args, rank, world)
-        return
+def measure(name, steps, warmup, with_e2e, pg, world, peaks, peak_src):
+    """One workload on this GPU: `steps` timed steps after `warmup` (CUDA events; L2 flushed
+    between steps when the inputs fit in it), each kernel kind's own duration in a second pass,
+    the clocks over both, and, with `with_e2e`, the end-to-end step with host buffers."""
     import torch
-    torch.cuda.set_device(local)
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-        pg = dist
     from paged_mla_kv_gb300 import binding as B
-    from paged_mla_kv_gb300 import build as BUILD
     from paged_mla_kv_gb300.harness import Resident
-    BUILD.build()
-    peaks, peak_src = load_peaks()
-    if args.workload in TOPK:
-        topk_main(args, rank, world, pg, peaks, peak_src)
-        if pg is not None:
-            pg.destroy_process_group()
-        return
-    w = make_workload(args.workload)
+    rank = int(os.environ.get("RANK", "0"))
+    w = make_workload(name)
     prefill = w.R > 2
     units = step_units(w)
     res = Resident(w, poison=True, fp8=bool(w.extra.get("fp8")))
@@ -528,7 +515,7 @@ def main():
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     barrier()
     n0 = B.tf_launch_count()
@@ -537,15 +524,15 @@ def main():
         # inputs larger than L2: K steps back to back between one pair of events
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for i in range(args.steps):
+        for i in range(steps):
             step()
         e1.record()
         barrier()
         total_ms = e0.elapsed_time(e1)
     else:
         # L2 flushed between steps, outside each step's pair of events
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        for i in range(args.steps):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
             flush.zero_()
             ev[i][0].record()
             step()
@@ -559,7 +546,7 @@ def main():
     # out of the timed region above, and the kinds' times may add up to more than a step)
     res.pool.profile(True)
     read_kernel_times(res.pool)
-    nprof = min(args.steps, 200)
+    nprof = min(steps, 200)
     for i in range(nprof):
         if flush is not None:
             flush.zero_()
@@ -573,7 +560,7 @@ def main():
     if rc != 0:
         raise SystemExit(f"device error {rc} ({detail})")
     total_ms = max_over_ranks(total_ms, pg, "cuda")
-    ms = total_ms / args.steps
+    ms = total_ms / steps
     if prefill:
         value = whole_job_rate(units["flops"], world, ms) / 1e12
         unit = "TFLOP/s"
@@ -588,21 +575,21 @@ def main():
         achieved = units["attend_flops"] / (avg_att / 1e3) / 1e12
         peak = peaks.get("bf16_tflops_sustained", 1700.0)
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": ncu_traffic(args.workload), "peak_kind": f"{peak_src} bf16 sustained",
+                "traffic": ncu_traffic(name), "peak_kind": f"{peak_src} bf16 sustained",
                 "kernel": "mla_attend_kernel",
                 "avg_launch_ms": avg_att}
     else:
         achieved = units["attend_bytes"] / (avg_att / 1e3) / 1e9
         peak = peaks.get("hbm_gbs", 6800.0)
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": ncu_traffic(args.workload), "peak_kind": f"{peak_src} HBM copy",
+                "traffic": ncu_traffic(name), "peak_kind": f"{peak_src} HBM copy",
                 "kernel": ("mla_attend_kernel, FP8 instance (codes expanded in shared memory)"
                            if w.extra.get("fp8") else "mla_attend_kernel"),
                 "avg_launch_ms": avg_att}
 
     # end to end through the C-ABI with host buffers: queries and new rows in, outputs out
     e2e = None
-    if not args.no_e2e:
+    if not not with_e2e:
         hq = [q.cpu().pin_memory() for q in qs]
         hrows = [(a.cpu().pin_memory(), b.cpu().pin_memory()) for a, b in cur]
         nb = 2   # double buffers: step i+1's inputs and step i-1's outputs move while step i runs
@@ -655,36 +642,99 @@ def main():
                 d2h(i)
             main.wait_event(out_read[(n - 1) % nb])
 
-        run_e2e(max(2, args.warmup))
+        run_e2e(max(2, warmup))
         barrier()
         if flush is None:
             # inputs larger than L2: the steps run back to back, copies overlapped, one pair of events
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(main)
-            run_e2e(args.steps)
+            run_e2e(steps)
             e1.record(main)
             barrier()
-            e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, pg, "cuda")
+            e_ms = max_over_ranks(e0.elapsed_time(e1) / steps, pg, "cuda")
         else:
             # the L2 flush between steps stays outside the events: each step is copied in,
             # run and copied out on its own
-            e2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-            for i in range(args.steps):
+            e2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            for i in range(steps):
                 flush.zero_()
                 e2[i][0].record(main)
                 run_e2e(1)
                 e2[i][1].record(main)
             barrier()
-            e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2) / args.steps, pg, "cuda")
+            e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2) / steps, pg, "cuda")
         h2d = sum(q.numel() * 2 for q in qs) + sum(a.numel() * 2 + b.numel() * 2 for a, b in cur)
         d2h = out.numel() * 2 + lse.numel() * 4
         ev_ = world * (units["flops"] / 1e12 if prefill else units["bytes"] / 1e9) / (e_ms / 1e3)
         e2e = {"value": ev_, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
 
+    return dict(w=w, units=units, ms=ms, value=value, unit=unit, tokens_s=tokens_s, launches=launches, roof=roof,
+                e2e=e2e, clocks=clocks, times=times, nprof=nprof, flush=flush is not None, prefill=prefill)
+
+
+# The rest of the metric ("...; prefill TFLOP/s") in the same run: short in-process runs of the
+# other configurations, after the headline decode batch, reported under "workloads".  Steps are
+# few (each still W >= 3 warm-ups, CUDA events, the L2 rule of the headline) so the whole run
+# stays within a couple of minutes; no end-to-end pass and no CPU baseline for these.
+EXTRA_WORKLOADS = (("long_window", 50), ("prefill_100k", 5), ("prefill_208k", 5), ("full_model", 10))
+
+
+def extra_workloads(args, pg, world, peaks, peak_src):
+    if args.no_extra or args.workload != "decode_batch":
+        return None
+    import gc
+    import torch
+    out = {}
+    for name, steps in EXTRA_WORKLOADS:
+        gc.collect()
+        torch.cuda.empty_cache()
+        r = measure(name, steps, 3, False, pg, world, peaks, peak_src)
+        roof = dict(r["roof"])
+        if r["prefill"]:
+            burst = peaks.get("bf16_tflops", 1900.0)
+            roof["frac_of_burst"] = roof["achieved"] / burst
+            roof["peak_burst"] = burst
+        out[name] = {"ms_per_step": r["ms"], "value": r["value"], "unit": r["unit"], "steps": steps, "warmup": 3,
+                     "tokens_per_s": r["tokens_s"], "gpu_launches": r["launches"], "roofline": roof,
+                     "clocks": r["clocks"], "kernels_per_step": kernels_per_step(r["times"], r["nprof"]),
+                     "l2": "flushed between steps" if r["flush"] else "inputs larger than L2",
+                     "config": {"S": r["w"].S, "R": r["w"].R, "H": r["w"].H, "caches": r["w"].num_caches,
+                                "lens_sum": int(np.sum(r["w"].lens))}}
+        del r
+    return out
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+    import torch
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    from paged_mla_kv_gb300 import binding as B
+    from paged_mla_kv_gb300 import build as BUILD
+    from paged_mla_kv_gb300.harness import Resident
+    BUILD.build()
+    peaks, peak_src = load_peaks()
+    if args.workload in TOPK:
+        topk_main(args, rank, world, pg, peaks, peak_src)
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+    r = measure(args.workload, args.steps, args.warmup, not args.no_e2e, pg, world, peaks, peak_src)
+    w, units, ms, value, unit = r["w"], r["units"], r["ms"], r["value"], r["unit"]
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = OracleSample(w, args.cpu_seconds).measure()
 
+    # the other configurations, on one GPU only (the scaling runs time the headline alone)
+    extra = extra_workloads(args, pg, world, peaks, peak_src) if world == 1 else None
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -692,10 +742,13 @@ def main():
                 "config": {"workload": w.name, "S": w.S, "R": w.R, "H": w.H, "caches": w.num_caches,
                            "lens_sum": int(np.sum(w.lens)), "kv_bytes": units["kv"],
                            "unique_kv_bytes": units.get("unique_kv", units["kv"]),
-                           "l2": "flushed between steps" if flush is not None else "inputs larger than L2",
+                           "l2": "flushed between steps" if r["flush"] else "inputs larger than L2",
                            "parallelism": f"replicas x{world}", "tokens_per_step": units["tokens"]},
-                "tokens_per_s": tokens_s, "gpu_launches": launches, "roofline": roof, "cpu_baseline": cpu,
-                "e2e": e2e, "clocks": clocks, "kernels_per_step": kernels_per_step(times, nprof)}
+                "tokens_per_s": r["tokens_s"], "gpu_launches": r["launches"], "roofline": r["roof"],
+                "cpu_baseline": cpu, "e2e": r["e2e"], "clocks": r["clocks"],
+                "kernels_per_step": kernels_per_step(r["times"], r["nprof"])}
+        if extra:
+            line["workloads"] = extra
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()

@@ -59,6 +59,38 @@ def test_long_window_all_heads():
     compare(w, out, lse)
 
 
+@pytest.mark.parametrize("variant", ["sharp", "ramp"])
+def test_decode_batch_peaked_scores(variant):
+    """The decode batch with peaked scores, so the running maximum moves and the lazy rescale
+    of O^T runs inside the streams' long key runs: q ~ N(0, 1) with scale 0.5 (scores of
+    std ~1.2), or a ramp (rope column 0 grows with position, later keys dominate)."""
+    w = Y.decode_batch()
+    if variant == "sharp":
+        w.q_std, w.scale = 1.0, 0.5
+    else:
+        w.ramp = 600.0
+    res = Resident(w)
+    out, lse = run_step(res)
+    no_device_error(res.pool)
+    compare(w, out, lse)
+
+
+@pytest.mark.parametrize("variant", ["sharp", "ramp"])
+def test_long_window_peaked_scores(variant):
+    """The long window (one 1,048,576-key stream, R = 2) with peaked scores: with the ramp
+    the scores climb ~25 nats across the window, so the reference maximum moves several
+    times along the 16,384 key tiles of stream 0 and O^T is rescaled in flight."""
+    w = Y.long_window()
+    if variant == "sharp":
+        w.q_std, w.scale = 1.0, 0.5
+    else:
+        w.ramp = 600.0
+    res = Resident(w)
+    out, lse = run_step(res)
+    no_device_error(res.pool)
+    compare(w, out, lse)
+
+
 @pytest.mark.parametrize("name", ["prefill_100k", "prefill_208k"])
 def test_prefill_sampled_rows(name):
     w = Y.WORKLOADS[name]()

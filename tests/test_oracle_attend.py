@@ -246,3 +246,19 @@ def test_sparse_list_order_does_not_matter_and_unlisted_rows_do_not_count():
     s = np.array([0.25 * (wide(q[0, 1, :512]) @ wide(lat[i]) + wide(q[0, 1, 512:]) @ wide(rope[i])) for i in idx])
     assert l1[1] == pytest.approx(float(logsumexp(s)), abs=1e-12)
     assert np.allclose(o1[1], softmax(s) @ np.array([wide(lat[i]) for i in idx]), rtol=0, atol=1e-12)
+
+
+def test_the_draft_test_tolerance_catches_an_off_by_one_causal_limit():
+    # The GPU test of the draft row (tests/test_gpu_parity.py, drafted == plain) bounds the
+    # rel-L2 between the two outputs and to the oracle by 1e-2.  On its workload (3,333 rows of
+    # N(0, 0.1) values, queries N(0, 0.1), scale 1/24) the weights are near uniform, so a draft
+    # row that saw one key too many -- the planted off-by-one, here in the oracle's inputs --
+    # moves by about 1/sqrt(3,333) = 1.7% in rel-L2 and fails that bound.
+    w = Y.custom("draft", 45, lens=[3333], R=2, H=64)
+    lat, rope = w.stream_rows(0, 0)
+    q = w.q()[0][:1]                                     # the draft row's queries, [1][64][576]
+    heads = np.arange(0, 64, 8, dtype=np.int32)          # eight heads keep this fast
+    right, _ = attend_stream(q, lat[:3332], rope[:3332], w.scale, heads)
+    wrong, _ = attend_stream(q, lat, rope, w.scale, heads)  # one key past the causal limit
+    rel = np.linalg.norm(wrong - right) / np.linalg.norm(right)
+    assert rel > 1e-2, rel
