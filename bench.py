@@ -80,6 +80,10 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> floa
 # gpu__time_duration.sum`; the FP8 decode launch under `--set full`); 3212b017dcca9adb differs from
 # it in host code only (the cubins built without line info hash the same).
 NCU_TRAFFIC = {
+    # attention on source 3fb36de603d76239, decode batch: `--metrics dram__bytes_read.sum,
+    # dram__bytes_write.sum,gpu__time_duration.sum --cache-control none` (L2 as the back-to-back
+    # steps leave it); profiles/mla_attend_decode_batch.md
+    "3fb36de603d76239": {"decode_batch": 360_180_736 + 1_144_320},
     "3212b017dcca9adb": {"decode_batch": 374_700_544 + 3_504_128,
                          "fp8_decode": 207_994_112 + 4_065_024,
                          "prefill_100k": 1_845_974_272 + 135_486_464,
