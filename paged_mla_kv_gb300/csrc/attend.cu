@@ -11,13 +11,13 @@
 // (row, head) columns) of one stream over a run of its key tiles; how the tiles are dealt out
 // (RANGES, UNITS, SPLITS, SPARSE) is described at the Params below.  Keys stream through
 // 64-row tiles: 9 boxes of [64 keys x 64 values] bf16 (8 latent + 1 rope), loaded by TMA with
-// 128-byte swizzle from the tile's pool page into a ring of 11 latent box-pair slots and 3 rope
-// slots (2.75 tiles in flight).  The queries' latent values 0-383 sit in TMEM as the A operand
-// of QK^T; only their last two latent boxes and the rope box stay in shared memory, which is
+// 128-byte swizzle from the tile's pool page into a ring of 10 latent box-pair slots and 3 rope
+// slots (2.5 tiles in flight).  The queries' latent values 0-255 sit in TMEM as the A operand
+// of QK^T; only their last four latent boxes and the rope box stay in shared memory, which is
 // what pays for the deeper ring.  The same shared-memory tile feeds both contractions on the
 // 5th-generation tensor cores:
 //   S   = Q . K^T     tcgen05.mma M=64 (the columns), N=64 keys, K=576, A from TMEM (values
-//                     0-383) or shared memory (the rest), the tile K-major; S in TMEM
+//                     0-255) or shared memory (the rest), the tile K-major; S in TMEM (2 buffers)
 //   O^T += V^T . P^T  tcgen05.mma M=128 latent values x 4, N = columns rounded up to 16,
 //                     K=64 keys, the tile read MN-major as V^T, P (bf16, written into the tile's
 //                     rope slot once QK^T has read it) K-major; O^T accumulates in TMEM (4 x 64 columns)
@@ -61,26 +61,28 @@ constexpr int NBOX = 9;                         // 64-wide boxes of a 576-wide r
 constexpr int BOX_BYTES = BK * 128;             // [64 rows][64 bf16], 128B swizzle
 constexpr int PAIR_BYTES = 2 * BOX_BYTES;       // latent boxes 2j and 2j+1 of a tile, side by side
 constexpr int QBOX_BYTES = NCOL * 128;          // [64 columns][64 bf16]
-// The queries: latent values 0-383 (boxes 0-5) sit in TMEM as the A operand of QK^T, written
-// by the softmax warps at each segment start; latent boxes 6-7 and the rope box stay in shared
-// memory (TMA).  Moving 48 KB of queries out of shared memory is what deepens the key ring.
-constexpr int Q_TMEM_BOXES = 6;
-constexpr int Q_SMEM_BOXES = NBOX - Q_TMEM_BOXES;   // [latent 6 | latent 7 | rope]
+// The queries: latent values 0-255 (boxes 0-3) sit in TMEM as the A operand of QK^T, written
+// by the softmax warps at each segment start; latent boxes 4-7 and the rope box stay in shared
+// memory (TMA).  Moving 32 KB of queries out of shared memory is what deepens the key ring; the
+// rest of TMEM holds O^T and two S buffers, so QK^T of the next tile never waits for the
+// softmax to read S out.
+constexpr int Q_TMEM_BOXES = 4;
+constexpr int Q_SMEM_BOXES = NBOX - Q_TMEM_BOXES;   // [latent 4 .. 7 | rope]
 // The key ring: a tile is its rope box (in a rope slot) and four latent box pairs (in pair
-// slots).  Pair slots are taken in order, four a tile (2.75 tiles in flight); a rope slot a tile
+// slots).  Pair slots are taken in order, four a tile (2.5 tiles in flight); a rope slot a tile
 // (3 in flight).  Once QK^T has read a tile's rope box, the slot holds the tile's P for PV, so
 // P is triple-buffered and the softmax never waits for the previous PV.
-constexpr int NPAIR = 11;
+constexpr int NPAIR = 10;
 constexpr int NROPE = 3;
 constexpr int SMEM_Q = 0;
-constexpr int SMEM_ROPE = SMEM_Q + Q_SMEM_BOXES * QBOX_BYTES;   // 24,576
-constexpr int SMEM_PAIR = SMEM_ROPE + NROPE * BOX_BYTES;          // 49,152
+constexpr int SMEM_ROPE = SMEM_Q + Q_SMEM_BOXES * QBOX_BYTES;   // 40,960
+constexpr int SMEM_PAIR = SMEM_ROPE + NROPE * BOX_BYTES;          // 65,536
 constexpr int SMEM_CTRL = SMEM_PAIR + NPAIR * PAIR_BYTES;         // 229,376
 constexpr float TAU = 8.0f;                     // lazy-rescale threshold, log2 units
 constexpr int TMEM_COLS = 512;
 constexpr int TMEM_O = 0;                       // O^T M-tile j at 64 j (j < 4)
-constexpr int TMEM_S = 256;                     // S (one buffer, 64 columns)
-constexpr int TMEM_Q = 320;                     // queries' latent values 0-383: column c holds values 2c, 2c+1
+constexpr int TMEM_S = 256;                     // S buffers at 256 and 320 (64 columns each)
+constexpr int TMEM_Q = 384;                     // queries' latent values 0-255: column c holds values 2c, 2c+1
 static_assert(TMEM_Q + Q_TMEM_BOXES * 32 == TMEM_COLS, "the queries fill TMEM's last columns");
 constexpr int THREADS = 352;
 // FP8 pages: four more warps (11-14) expand each tile's E4M3 codes into its BF16 boxes in place.
@@ -128,7 +130,7 @@ struct Ctrl {
     uint64_t pair_empty[NPAIR];        // PV M-tile of the pair is done
     uint64_t p_full[NROPE];            // P of the slot's tile written and O^T rescaled for it
     uint64_t corr_req[NROPE];          // the tile's softmax statistics posted for the rescale warps
-    uint64_t s_full, s_free;           // S computed / read out of TMEM
+    uint64_t s_full[2], s_free[2];     // S buffer computed / read out of TMEM
     uint64_t q_full, q_tmem_full, q_free, stats_full, stats_free, drain;
     uint32_t tmem_base;
     int abort;
@@ -360,8 +362,10 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
         for (int i = 0; i < NPAIR; ++i) {
             ptx::mbar_init(&c.pair_empty[i], 1);
         }
-        ptx::mbar_init(&c.s_full, 1);
-        ptx::mbar_init(&c.s_free, 4);
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&c.s_full[i], 1);
+            ptx::mbar_init(&c.s_free[i], 4);
+        }
         ptx::mbar_init(&c.q_full, 1);
         ptx::mbar_init(&c.q_tmem_full, 4);
         ptx::mbar_init(&c.q_free, 1);
@@ -645,13 +649,14 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
         const uint64_t v_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_PAIR), BOX_BYTES, 1024);
         const uint64_t p_desc0 = ptx::sdesc_sw128(ptx::smem_u32(smem + SMEM_ROPE), 16, 1024);
         // QK^T of global tile tq (tile tl of segment q): S[64 columns][64 keys] (M = 64: rows
-        // 16w..16w+15 in lanes 0-15 of TMEM quadrant w).  Box order: rope (queries' rope box in
-        // shared memory), latent pairs 0-2 (queries in TMEM), latent pair 3 (queries in shared memory).
+        // 16w..16w+15 in lanes 0-15 of TMEM quadrant w; buffer tq % 2).  Box order: rope (queries'
+        // rope box in shared memory), latent pairs 0-1 (queries in TMEM), pairs 2-3 (shared memory).
         auto qk_tile = [&](int tq, int tl, const Seg &q) -> bool {
             const int rs = rope_slot(tq);
-            // S has been read out (s_free) and every box of the tile has landed (one barrier a tile:
-            // a wait costs about as long as four MMAs, so the tile's 36 MMAs go out in one run)
-            if (tq >= 1 && !ptx::mbar_wait_warp(&c.s_free, (tq - 1) & 1, abort, errp, 4)) return false;
+            // the tile's S buffer has been read out (by the softmax of tile tq - 2) and every box of
+            // the tile has landed (one barrier a tile: a wait costs about as long as four MMAs, so
+            // the tile's 36 MMAs go out in one run)
+            if (tq >= 2 && !ptx::mbar_wait_warp(&c.s_free[tq & 1], ((tq - 2) >> 1) & 1, abort, errp, 4)) return false;
             if (!ptx::mbar_wait_warp(&c.tile_full[rs], rope_use(tq) & 1, abort, errp, 3)) return false;
             const int64_t rem = q.len - (q.kb + (int64_t)tl * BK);
             if (rem < BK) {
@@ -669,10 +674,10 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             // stores (q_tmem_full, waited before a segment's first tile); the key boxes come by
             // TMA and need no such fence
             ptx::tc_fence_after();
-            const uint32_t d = tmem + TMEM_S;
+            const uint32_t d = tmem + TMEM_S + (tq & 1) * BK;
             // the rope box (queries' rope box in shared memory) starts S, then the latent pairs;
             // a rolled loop keeps this warp's code small in the instruction cache
-            ptx::mma4_bf16_ss_warp(d, q_desc0 + (uint64_t)((2 * QBOX_BYTES) >> 4),
+            ptx::mma4_bf16_ss_warp(d, q_desc0 + (uint64_t)(((Q_SMEM_BOXES - 1) * QBOX_BYTES) >> 4),
                                    kv_desc0 + (uint64_t)((SMEM_ROPE + rs * BOX_BYTES) >> 4), IDESC_QK, 1u);
             int ps = pair_slot(tq, 0);
 #pragma unroll 1
@@ -685,7 +690,7 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                                            0u);
                 if ((b & 1) && ++ps == NPAIR) ps = 0;
             }
-            ptx::mma_commit_warp(&c.s_full);
+            ptx::mma_commit_warp(&c.s_full[tq & 1]);
             if (tl == q.nt - 1) ptx::mma_commit_warp(&c.q_free);
             return true;
         };
@@ -817,7 +822,7 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             const int col0 = q.g * NCOL;
             const int ncols = ncols_all - col0;
             {
-                // The segment's queries, latent values 0-383, into TMEM (A of QK^T): lane i < 16 of
+                // The segment's queries, latent values 0-255, into TMEM (A of QK^T): lane i < 16 of
                 // this quadrant holds column 16 q4 + i.  Every QK^T of the previous segment has
                 // completed: this warp has seen its last S.
                 const int m = 16 * q4 + (lane & 15);
@@ -853,17 +858,17 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                 const int t = gt + tl;
                 const int rs = rope_slot(t);
                 const int64_t k0 = q.kb + (int64_t)tl * BK;
-                if (!ptx::mbar_wait_warp(&c.s_full, t & 1, abort, errp, 7)) {
+                if (!ptx::mbar_wait_warp(&c.s_full[t & 1], (t >> 1) & 1, abort, errp, 7)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 uint32_t r[32];
-                ptx::tmem_ld_16x256b_x8(lane_base + TMEM_S, r);
+                ptx::tmem_ld_16x256b_x8(lane_base + TMEM_S + (t & 1) * BK, r);
                 ptx::tmem_ld_wait();
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&c.s_free);
+                if (lane == 0) ptx::mbar_arrive(&c.s_free[t & 1]);
                 // keys outside a row's range become -inf; the maximum is taken before
                 // scaling (the scale is positive) and the scale is folded into the
                 // exponent's FFMA: p = 2^(s * scale*log2(e) - m_ref)
