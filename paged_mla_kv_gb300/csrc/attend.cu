@@ -441,29 +441,58 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                 q_armed = si;
                 const int32_t *list = p.idx + (size_t)q.s * p.max_idx;
                 const int rows = p.st[q.s].split;
+                // list position k0 + 2 lane + h of tile tl2; past the list's end a listed row is
+                // loaded again (the softmax masks it)
+                auto list_at = [&](int tl2, int h) -> int {
+                    const int64_t pos = q.kb + (int64_t)tl2 * BK + 2 * lane + h;
+                    return __ldg(list + (pos < q.len ? pos : 0));
+                };
+                // the pool page of a listed row (-1 for a row outside the stream)
+                auto page_of = [&](int r) -> int {
+                    if (r < 0 || r >= rows) return -1;
+                    const int lp = r >> 9;
+                    return windowed ? q.s * max_pages + lp : __ldg(pt + (int64_t)q.s * max_pages + lp);
+                };
+                // the list entries run two tiles and their pages one tile ahead of the copies, so
+                // these dependent loads overlap the waits for free slots instead of delaying each tile
+                int rc[2], pc[2], rn[2], pn[2] = {0, 0}, rnn[2] = {0, 0};
+#pragma unroll
+                for (int h = 0; h < 2; ++h) rc[h] = list_at(0, h);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    pc[h] = page_of(rc[h]);
+                    rn[h] = q.nt > 1 ? list_at(1, h) : 0;
+                }
                 for (int tl = 0; tl < q.nt; ++tl, ++gt) {
+                    if (tl > 0) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            rc[h] = rn[h];
+                            pc[h] = pn[h];
+                            rn[h] = rnn[h];
+                        }
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        pn[h] = tl + 1 < q.nt ? page_of(rn[h]) : 0;
+                        rnn[h] = tl + 2 < q.nt ? list_at(tl + 2, h) : 0;
+                    }
                     const int rs = rope_slot(gt);
-                    const int64_t k0 = q.kb + (int64_t)tl * BK;
                     int ylat[2], yrope[2], badv = 0;
                     const char *sc_addr[2] = {nullptr, nullptr};
                     bool bad = false;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        // past the list's end a listed row is loaded again; the softmax masks it
-                        const int64_t pos = k0 + 2 * lane + h;
-                        const int r = __ldg(list + (pos < q.len ? pos : 0));
-                        int pg = 0;
+                        const int r = rc[h];
+                        int pg = pc[h];
                         if (r < 0 || r >= rows) {
                             bad = true;
                             badv = r;
-                        } else {
-                            const int lp = r >> 9;
-                            pg = windowed ? q.s * max_pages + lp : __ldg(pt + (int64_t)q.s * max_pages + lp);
-                            if (pg < 0 || pg >= num_pages) {
-                                bad = true;
-                                badv = pg;
-                                pg = 0;
-                            }
+                            pg = 0;
+                        } else if (pg < 0 || pg >= num_pages) {
+                            bad = true;
+                            badv = pg;
+                            pg = 0;
                         }
                         const int base = cache * num_pages + pg;
                         // rows of the views: 1,024-byte latent rows (576 a page) and 128-byte rope
