@@ -255,6 +255,12 @@ struct SegIter {
             x = x0;
         }
     }
+    // after next() returned a segment: is it this CTA's last?
+    __device__ __forceinline__ bool last(const Params &p) const {
+        if (MODE == MODE_RANGES || MODE == MODE_SPARSE) return x >= x1;
+        if (MODE == MODE_UNITS) return (int64_t)blockIdx.x + (int64_t)k * gridDim.x >= p.total;
+        return true;
+    }
     __device__ __forceinline__ bool next(const Params &p, Seg &q) {
         if (MODE == MODE_RANGES || MODE == MODE_SPARSE) {
             if (x >= x1) return false;
@@ -1071,25 +1077,49 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             }
             ptx::tc_fence_after();
             const float *inv_l = c.row_inv_l[si & 1];
-            for (int jm = 0; jm < 4; ++jm)
-                for (int h2 = 0; h2 < npv; h2 += 32) {
-                    uint32_t v[32];
-                    ptx::tmem_ld32(lane_base + TMEM_O + jm * 64 + h2, v);
-                    ptx::tmem_ld_wait();
-                    const int dim = jm * 128 + q4 * 32 + lane;
+            if (q.slot >= 0 && it.last(p)) {
+                // The CTA's last segment, cut: its fp32 partial (128 KB) goes out by one bulk copy
+                // from shared memory, staged in the key ring, which no tile uses any more (the
+                // last PV is done and the TMA warp loads nothing after it).  Every CTA ends with
+                // this write at about the same time; one bulk copy a CTA moves it faster than
+                // 4,096 warp stores.
+                float *stage = reinterpret_cast<float *>(smem + SMEM_PAIR);
+                for (int jm = 0; jm < 4; ++jm)
+                    for (int h2 = 0; h2 < NCOL; h2 += 32) {
+                        uint32_t v[32];
+                        ptx::tmem_ld32(lane_base + TMEM_O + jm * 64 + h2, v);
+                        ptx::tmem_ld_wait();
+                        const int dim = jm * 128 + q4 * 32 + lane;
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const int col = h2 + k;
-                        if (col >= ncols) continue;
-                        const float o = __uint_as_float(v[k]);
-                        if (q.slot < 0) {
-                            const size_t orow = (size_t)q.s * ncols_all + col0 + col;
-                            outp[orow * kLat + dim] = __float2bfloat16_rn(o * inv_l[col]);
-                        } else {
-                            ws_o[((size_t)q.slot * NCOL + col) * kLat + dim] = o;
+                        for (int k = 0; k < 32; ++k) stage[(h2 + k) * kLat + dim] = __uint_as_float(v[k]);
+                    }
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar(1, 128);
+                if (threadIdx.x == 0) {
+                    ptx::bulk_s2g(ws_o + (size_t)q.slot * NCOL * kLat, stage, NCOL * kLat * sizeof(float));
+                    ptx::bulk_s2g_wait();
+                }
+            } else {
+                for (int jm = 0; jm < 4; ++jm)
+                    for (int h2 = 0; h2 < npv; h2 += 32) {
+                        uint32_t v[32];
+                        ptx::tmem_ld32(lane_base + TMEM_O + jm * 64 + h2, v);
+                        ptx::tmem_ld_wait();
+                        const int dim = jm * 128 + q4 * 32 + lane;
+    #pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            const int col = h2 + k;
+                            if (col >= ncols) continue;
+                            const float o = __uint_as_float(v[k]);
+                            if (q.slot < 0) {
+                                const size_t orow = (size_t)q.s * ncols_all + col0 + col;
+                                outp[orow * kLat + dim] = __float2bfloat16_rn(o * inv_l[col]);
+                            } else {
+                                ws_o[((size_t)q.slot * NCOL + col) * kLat + dim] = o;
+                            }
                         }
                     }
-                }
+            }
             // the statistics are read: the softmax may post the next segment's
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&c.stats_free);
