@@ -312,15 +312,19 @@ int tf_diag_wait_timeout(tf_kvpool *pool, int64_t limit_cycles, void *cuda_strea
 /* The work plan tf_paged_mla_attend would use for these lengths, for inspection: host
  * arithmetic only, nothing launched.  sms: the SMs to plan for (<= 0: the current device's,
  * or TF_PLAN_MAX_RANGES without one); invariant != 0: a TF_POOL_BATCH_INVARIANT pool.
- *   info->mode     0 key-tile ranges (decode, MTP rows), 1 whole (stream, column group) units
- *                  round robin (prefill chunks), 2 per-stream splits (batch-invariant pools)
+ *   info->mode     0 key-tile ranges (decode, MTP rows), 1 key-tile ranges over (stream,
+ *                  column group) units, one CTA a range (prefill chunks), 2 per-stream splits
+ *                  (batch-invariant pools)
  *   info->ctas     CTAs launched
- *   info->nranges  mode 0: ranges (each taken by info->groups CTAs side by side); else 0
+ *   info->nranges  mode 0: ranges (each taken by info->groups CTAs side by side); mode 1:
+ *                  ranges (= ctas); else 0
  *   info->groups   column groups a stream: ceil(R * H / 64)
  *   info->work     mode 0: 64-key tiles of the batch; mode 1: units; mode 2: (split, group) items
  *   info->slots    fp32 partial slots in the workspace (0: no combine pass)
- * range_bounds (may be NULL): with mode 0, the nranges + 1 tile numbers that bound the ranges,
- * tiles numbered stream by stream (at most TF_PLAN_MAX_RANGES + 1 entries).
+ * range_bounds (may be NULL): the nranges + 1 bounds of the ranges (at most TF_PLAN_MAX_RANGES
+ * + 1 entries).  Mode 0: tile numbers, tiles numbered stream by stream.  Mode 1: positions
+ * unit * 2^32 + tile, units numbered stream-major (unit = s * groups + g), each unit as many
+ * 64-key tiles as its last column sees (len - R + 1 + that column's row).
  * split_keys (may be NULL): with mode 2, the keys of one split of each stream [S].
  * TF_E_ARG for a null h_len or info, or S, R, H outside the attention's limits; TF_E_UNSUPPORTED
  * for S * R * H above 2^30 (as tf_paged_mla_attend); TF_E_RANGE for a length below R or above

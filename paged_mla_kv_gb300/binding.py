@@ -326,8 +326,8 @@ def tf_topk_blocked(logits, k: int, idx, val, lens=None, n: int | None = None, w
 
 def tf_paged_mla_plan_info(S: int, R: int, H: int, lens, sms: int = 0, invariant: bool = False) -> dict:
     """The attention's work plan for these lengths (host arithmetic, nothing launched): mode,
-    ctas, nranges, groups, work, slots, and the range bounds (mode 0) or each stream's split
-    keys (mode 2) as int64 arrays."""
+    ctas, nranges, groups, work, slots, and the range bounds (modes 0 and 1) or each stream's
+    split keys (mode 2) as int64 arrays."""
     a, p = _i64(lens)
     info = tf_attend_plan()
     bounds = np.zeros(TF_PLAN_MAX_RANGES + 1, np.int64)
@@ -336,7 +336,7 @@ def tf_paged_mla_plan_info(S: int, R: int, H: int, lens, sms: int = 0, invariant
                                         bounds.ctypes.data_as(ctypes.c_void_p),
                                         splits.ctypes.data_as(ctypes.c_void_p)), "tf_paged_mla_plan_info")
     out = {f: int(getattr(info, f)) for f, _ in tf_attend_plan._fields_}
-    out["bounds"] = bounds[:out["nranges"] + 1] if out["mode"] == 0 else None
+    out["bounds"] = bounds[:out["nranges"] + 1] if out["mode"] in (0, 1) else None
     out["split_keys"] = splits[:S] if out["mode"] == 2 else None
     return out
 

@@ -126,6 +126,8 @@ __device__ __forceinline__ int scales_off(int gt) { return SMEM_PAIR + pair_slot
 struct Ctrl {
     uint64_t f8_full[NROPE];           // FP8: the tile's codes, scales and rope box landed
     uint64_t tile_full[NROPE];         // every box of the tile landed (FP8: expanded); by rope slot
+    uint64_t tile_half[NROPE];         // prefill: the rope box and latent pairs 0-1 landed (tile_full:
+                                       // pairs 2-3)
     uint64_t rope_empty[NROPE];        // PV of the slot's tile is done (its rope box and P are free)
     uint64_t pair_empty[NPAIR];        // PV M-tile of the pair is done
     uint64_t p_full[NROPE];            // P of the slot's tile written and O^T rescaled for it
@@ -148,8 +150,12 @@ static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 //    taken by `rep` = groups CTAs side by side, one column group each, so the groups
 //    of a stream read the same tiles at the same time.  A (stream, group) unit cut by
 //    a range boundary leaves partials that a combine pass merges, in key order.
-//  - UNITS (many column groups: a prefill chunk).  Whole units, round robin over the
-//    CTAs; at any time the CTAs read the same stretch of keys.  No partials.
+//  - UNITS (many column groups: a prefill chunk).  The units, stream-major, each only as
+//    many key tiles as its last column sees, are numbered tile by tile and cut into equal
+//    ranges of CTAs, like RANGES with one CTA a range: every SM gets the same work, where
+//    whole units dealt round robin leave a tail round on some SMs only.  A cut inside a
+//    long unit falls on an eighth of it, so the CTAs read at a few key positions in step
+//    (the others' tiles come from L2).  A cut unit leaves partials, merged as in RANGES.
 //  - SPLITS (a pool made with TF_POOL_BATCH_INVARIANT).  Each stream's keys are cut
 //    into splits whose bounds depend on that stream's length alone, one CTA a
 //    (split, group) item, and the partials are merged in split order, so a stream's
@@ -192,12 +198,21 @@ struct Params {
     int32_t mode;
     int32_t nranges;      // RANGES: ranges of the numbering
     int32_t rep;          // RANGES: CTAs a range (the column groups)
-    int64_t rb[MAX_CTAS + 1];        // RANGES: range i is tiles [rb[i], rb[i+1])
+    int64_t rb[MAX_CTAS + 1];        // RANGES: range i is tiles [rb[i], rb[i+1]); UNITS: positions
     StreamPlan st[TF_MAX_STREAMS];
     int16_t order[TF_MAX_STREAMS];   // SPLITS: launch order (streams with longer splits first)
 };
 
-// The range that holds numbered tile x.
+// UNITS: keys unit (stream of `len` keys, column group g) reads, up to the last key its last
+// column sees (the R rows are the stream's last R positions; column c is row c / H).  len >= R.
+__host__ __device__ __forceinline__ int64_t unit_keys(int64_t len, int R, int H, int ncols, int g) {
+    const int64_t clast = (int64_t)g * NCOL + NCOL - 1 < ncols ? (int64_t)g * NCOL + NCOL - 1 : (int64_t)ncols - 1;
+    return len - R + clast / H + 1;
+}
+// UNITS: a position of the numbering, (unit, tile within it), as one ordered integer
+__host__ __device__ __forceinline__ int64_t unit_pos(int64_t u, int64_t t) { return (u << 32) | t; }
+
+// The range that holds numbered tile x (UNITS: position x).
 __device__ __forceinline__ int range_of(const Params &p, int64_t x) {
     int lo = 0, hi = p.nranges - 1;
     while (lo < hi) {
@@ -248,7 +263,7 @@ struct SegIter {
     int64_t x, x0, x1;
     int k;
     __device__ __forceinline__ explicit SegIter(const Params &p) : x(0), x0(0), x1(0), k(0) {
-        if (MODE == MODE_RANGES || MODE == MODE_SPARSE) {
+        if (MODE == MODE_RANGES || MODE == MODE_SPARSE || MODE == MODE_UNITS) {
             const int range = (int)blockIdx.x / p.rep;
             x0 = p.rb[range];
             x1 = p.rb[range + 1];
@@ -257,8 +272,7 @@ struct SegIter {
     }
     // after next() returned a segment: is it this CTA's last?
     __device__ __forceinline__ bool last(const Params &p) const {
-        if (MODE == MODE_RANGES || MODE == MODE_SPARSE) return x >= x1;
-        if (MODE == MODE_UNITS) return (int64_t)blockIdx.x + (int64_t)k * gridDim.x >= p.total;
+        if (MODE == MODE_RANGES || MODE == MODE_SPARSE || MODE == MODE_UNITS) return x >= x1;
         return true;
     }
     __device__ __forceinline__ bool next(const Params &p, Seg &q) {
@@ -269,16 +283,21 @@ struct SegIter {
             return true;
         }
         if (MODE == MODE_UNITS) {
-            const int64_t u = (int64_t)blockIdx.x + (int64_t)k * gridDim.x;
-            if (u >= p.total) return false;
-            ++k;
+            // the rest of unit u from tile t: up to the range's end or the unit's last tile
+            if (x >= x1) return false;
+            const int64_t u = x >> 32, t = x & 0xffffffffll;
             q.s = (int)(u / p.groups);
             q.g = (int)(u - (int64_t)q.s * p.groups);
             q.len = p.st[q.s].len;
-            q.nt = p.st[q.s].nt;
-            q.kb = 0;
-            q.ke = q.len;
-            q.slot = -1;
+            const int64_t keys = unit_keys(q.len, p.R, p.H, p.ncols, q.g);
+            const int64_t nt = (keys + BK - 1) / BK;
+            const int64_t te = (x1 >> 32) == u ? (x1 & 0xffffffffll) : nt;
+            q.nt = (int)(te - t);
+            q.kb = t * BK;
+            q.ke = min(keys, te * BK);
+            q.slot = (t == 0 && te == nt) ? -1 : 2 * (int)blockIdx.x + (k == 0 ? 0 : 1);
+            ++k;
+            x = te == nt ? unit_pos(u + 1, 0) : unit_pos(u, te);
             return true;
         }
         // SPLITS: one item a CTA
@@ -358,6 +377,7 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             // BF16: the TMA warp's one arrival with the tile's bytes; FP8: one arrival a pair the
             // expansion warps finish
             ptx::mbar_init(&c.tile_full[i], FP8 ? 4 : 1);
+            ptx::mbar_init(&c.tile_half[i], 1);
             ptx::mbar_init(&c.rope_empty[i], 1);
             ptx::mbar_init(&c.p_full[i], 5);       // four softmax warps and the rescale warps
             ptx::mbar_init(&c.corr_req[i], 4);
@@ -393,6 +413,10 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
     // on-chip setup done: from here on global memory (pool, tables, queries, outputs)
     ptx::griddep_wait();
 
+    // Prefill (UNITS, BF16) lands a tile in two halves: QK^T starts on the rope box and latent
+    // pairs 0-1 while pairs 2-3, whose slots the PV of the tile two back releases last, are
+    // still on their way.  Decode keeps one barrier a tile (a wait costs about four MMAs).
+    constexpr bool HALF = !FP8;
     if (warp == 8) {
         // ================= TMA producer =================
         // Slot uses armed last (-1: never), so that no copy is left writing shared memory at exit.
@@ -408,7 +432,12 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             const uint32_t u = rope_use(gt);
             if (u > 0 && !ptx::mbar_wait(&c.rope_empty[rs], (u - 1) & 1, abort, errp, 1)) return false;
             if (!FP8) {
-                ptx::mbar_arrive_expect_tx(&c.tile_full[rs], NBOX * BOX_BYTES);
+                if (HALF) {
+                    ptx::mbar_arrive_expect_tx(&c.tile_half[rs], 5 * BOX_BYTES);
+                    ptx::mbar_arrive_expect_tx(&c.tile_full[rs], 4 * BOX_BYTES);
+                } else {
+                    ptx::mbar_arrive_expect_tx(&c.tile_full[rs], NBOX * BOX_BYTES);
+                }
                 armed_tile[rs] = (int)u;
             }
             return true;
@@ -573,12 +602,13 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                             break;
                         }
                         if (lane < 16) {
+                            uint64_t *bar = HALF && j < 2 ? &c.tile_half[rs] : &c.tile_full[rs];
                             if (j < 0) {
-                                ptx::tma_gather4(smem + box_off(gt, 8) + lane * 512, &p.tm_rope_rows, &c.tile_full[rs],
-                                                 0, ro0, ro1, ro2, ro3, pol_kv);
+                                ptx::tma_gather4(smem + box_off(gt, 8) + lane * 512, &p.tm_rope_rows, bar, 0, ro0, ro1,
+                                                 ro2, ro3, pol_kv);
                             } else {
                                 for (int h = 0; h < 2; ++h)
-                                    ptx::tma_gather4(smem + box_off(gt, 2 * j + h) + lane * 512, &p.tm_lat_rows, &c.tile_full[rs],
+                                    ptx::tma_gather4(smem + box_off(gt, 2 * j + h) + lane * 512, &p.tm_lat_rows, bar,
                                                      (2 * j + h) * 64, la0, la1, la2, la3, pol_kv);
                             }
                         }
@@ -648,16 +678,18 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                             stop = true;
                             break;
                         }
-                        tma_load_4d(smem + box_off(gt, 8), &p.tm_rope, &c.tile_full[rs], 0, row, page, cache, pol_kv);
+                        tma_load_4d(smem + box_off(gt, 8), &p.tm_rope, HALF ? &c.tile_half[rs] : &c.tile_full[rs], 0, row,
+                                    page, cache, pol_kv);
 #pragma unroll 1
                         for (int j = 0; j < 4; ++j) {
                             if (!free_pair(gt, j)) {
                                 stop = true;
                                 break;
                             }
+                            uint64_t *bar = HALF && j < 2 ? &c.tile_half[rs] : &c.tile_full[rs];
                             for (int h = 0; h < 2; ++h)
-                                tma_load_4d(smem + box_off(gt, 2 * j + h), &p.tm_lat, &c.tile_full[rs], (2 * j + h) * 64,
-                                            row, page, cache, pol_kv);
+                                tma_load_4d(smem + box_off(gt, 2 * j + h), &p.tm_lat, bar, (2 * j + h) * 64, row, page,
+                                            cache, pol_kv);
                         }
                         if (stop) break;
                     }
@@ -668,7 +700,10 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
         if (lane == 0) {
             if (q_armed >= 0) ptx::mbar_wait(&c.q_full, q_armed & 1, abort, errp, 10, 1ll << 28);
             for (int i = 0; i < NROPE; ++i) {
-                if (armed_tile[i] >= 0) ptx::mbar_wait(&c.tile_full[i], armed_tile[i] & 1, abort, errp, 11, 1ll << 28);
+                if (armed_tile[i] >= 0) {
+                    if (HALF) ptx::mbar_wait(&c.tile_half[i], armed_tile[i] & 1, abort, errp, 11, 1ll << 28);
+                    ptx::mbar_wait(&c.tile_full[i], armed_tile[i] & 1, abort, errp, 11, 1ll << 28);
+                }
                 if (armed_f8[i] >= 0) ptx::mbar_wait(&c.f8_full[i], armed_f8[i] & 1, abort, errp, 18, 1ll << 28);
             }
         }
@@ -688,42 +723,58 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
         // rope box in shared memory), latent pairs 0-1 (queries in TMEM), pairs 2-3 (shared memory).
         auto qk_tile = [&](int tq, int tl, const Seg &q) -> bool {
             const int rs = rope_slot(tq);
-            // the tile's S buffer has been read out (by the softmax of tile tq - 2) and every box of
-            // the tile has landed (one barrier a tile: a wait costs about as long as four MMAs, so
-            // the tile's 36 MMAs go out in one run)
+            // the tile's S buffer has been read out (by the softmax of tile tq - 2)
             if (tq >= 2 && !ptx::mbar_wait_warp(&c.s_free[tq & 1], ((tq - 2) >> 1) & 1, abort, errp, 4)) return false;
-            if (!ptx::mbar_wait_warp(&c.tile_full[rs], rope_use(tq) & 1, abort, errp, 3)) return false;
             const int64_t rem = q.len - (q.kb + (int64_t)tl * BK);
-            if (rem < BK) {
-                // rows past the stream's end may hold NaN poison: zero them so that P = 0 times V
-                // stays 0 in the PV contraction
+            // rows past the stream's end may hold NaN poison: zero them in latent boxes [b0, b1) and
+            // the rope box, so that P = 0 times V stays 0 in the PV contraction
+            auto zero_box = [&](int b) {
                 const int valid = (int)rem;
-                for (int b = 0; b < NBOX; ++b) {
-                    uint4 *bx = reinterpret_cast<uint4 *>(smem + box_off(tq, b));
-                    for (int k = lane; k < (BK - valid) * 8; k += 32) bx[valid * 8 + k] = make_uint4(0, 0, 0, 0);
-                }
+                uint4 *bx = reinterpret_cast<uint4 *>(smem + box_off(tq, b));
+                for (int k = lane; k < (BK - valid) * 8; k += 32) bx[valid * 8 + k] = make_uint4(0, 0, 0, 0);
+            };
+            auto zero_tail = [&](int b0, int b1, bool rope) {
+                if (rem >= BK) return;
+                if (rope) zero_box(8);
+                for (int b = b0; b < b1; ++b) zero_box(b);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
-            }
+            };
+            const uint32_t d = tmem + TMEM_S + (tq & 1) * BK;
+            // latent boxes [b0, b1): 0-3 with the queries' values from TMEM, 4-7 from shared memory;
+            // a rolled loop keeps this warp's code small in the instruction cache
+            auto latent = [&](int b0, int b1) {
+                int ps = pair_slot(tq, b0 >> 1);
+#pragma unroll 1
+                for (int b = b0; b < b1; ++b) {
+                    const uint64_t bd = kv_desc0 + (uint64_t)((SMEM_PAIR + ps * PAIR_BYTES + (b & 1) * BOX_BYTES) >> 4);
+                    if (b < Q_TMEM_BOXES)
+                        ptx::mma4_bf16_ts_warp(d, tmem + TMEM_Q + 32 * b, bd, IDESC_QK);
+                    else
+                        ptx::mma4_bf16_ss_warp(d, q_desc0 + (uint64_t)(((b - Q_TMEM_BOXES) * QBOX_BYTES) >> 4), bd,
+                                               IDESC_QK, 0u);
+                    if ((b & 1) && ++ps == NPAIR) ps = 0;
+                }
+            };
+            // the tile (prefill: its first half) has landed: one barrier, as a wait costs about as
+            // long as four MMAs, so the MMAs go out in long runs
+            if (!ptx::mbar_wait_warp(HALF ? &c.tile_half[rs] : &c.tile_full[rs], rope_use(tq) & 1, abort, errp, 3))
+                return false;
+            zero_tail(0, HALF ? 4 : 8, true);
             // order the MMAs after the softmax's TMEM loads of S (s_free) and the queries' TMEM
             // stores (q_tmem_full, waited before a segment's first tile); the key boxes come by
             // TMA and need no such fence
             ptx::tc_fence_after();
-            const uint32_t d = tmem + TMEM_S + (tq & 1) * BK;
-            // the rope box (queries' rope box in shared memory) starts S, then the latent pairs;
-            // a rolled loop keeps this warp's code small in the instruction cache
+            // the rope box (queries' rope box in shared memory) starts S, then the latent pairs
             ptx::mma4_bf16_ss_warp(d, q_desc0 + (uint64_t)(((Q_SMEM_BOXES - 1) * QBOX_BYTES) >> 4),
                                    kv_desc0 + (uint64_t)((SMEM_ROPE + rs * BOX_BYTES) >> 4), IDESC_QK, 1u);
-            int ps = pair_slot(tq, 0);
-#pragma unroll 1
-            for (int b = 0; b < 8; ++b) {
-                const uint64_t bd = kv_desc0 + (uint64_t)((SMEM_PAIR + ps * PAIR_BYTES + (b & 1) * BOX_BYTES) >> 4);
-                if (b < Q_TMEM_BOXES)
-                    ptx::mma4_bf16_ts_warp(d, tmem + TMEM_Q + 32 * b, bd, IDESC_QK);
-                else
-                    ptx::mma4_bf16_ss_warp(d, q_desc0 + (uint64_t)(((b - Q_TMEM_BOXES) * QBOX_BYTES) >> 4), bd, IDESC_QK,
-                                           0u);
-                if ((b & 1) && ++ps == NPAIR) ps = 0;
+            if (HALF) {
+                latent(0, 4);
+                if (!ptx::mbar_wait_warp(&c.tile_full[rs], rope_use(tq) & 1, abort, errp, 3)) return false;
+                zero_tail(4, 8, false);
+                latent(4, 8);
+            } else {
+                latent(0, 8);
             }
             ptx::mma_commit_warp(&c.s_full[tq & 1]);
             if (tl == q.nt - 1) ptx::mma_commit_warp(&c.q_free);
@@ -1137,7 +1188,9 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
 // Merge a unit's partials (m_j, l_j, o_j), j in key order:
 //   M = max_j m_j,  w_j = 2^(m_j - M),  out = sum_j w_j o_j / sum_j w_j l_j,
 //   lse = (M + log2 sum_j w_j l_j) * ln 2.
-// One 256-thread block per (stream, column).  Warp w sums the partials j = w, w + 8,
+// One 256-thread block per (stream, column); UNITS: per (column of the group, range bound),
+// where a bound inside a unit that no earlier bound cuts stands for that unit.  Warp w sums
+// the partials j = w, w + 8,
 // ... (lane: 16 latent columns, four independent 16-byte loads a partial), then the
 // eight warp sums are added in warp order: a fixed order, so the result is the same
 // on every call.
@@ -1146,18 +1199,33 @@ constexpr int COMBINE_THREADS = 256;
 __global__ void __launch_bounds__(COMBINE_THREADS) mla_combine_kernel(const __grid_constant__ Params p) {
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
-    const int s = blockIdx.y;
-    const int gc = blockIdx.x;
+    int s = blockIdx.y, gc = blockIdx.x;
+    if (p.mode == MODE_UNITS) {
+        const int64_t x = p.rb[blockIdx.y + 1], xp = p.rb[blockIdx.y];
+        const int64_t u = x >> 32;
+        if ((x & 0xffffffffll) == 0 || ((xp >> 32) == u && (xp & 0xffffffffll) != 0)) return;
+        s = (int)(u / p.groups);
+        gc = (int)(u - (int64_t)s * p.groups) * NCOL + (int)blockIdx.x;
+    }
     if (gc >= p.ncols) return;
     const StreamPlan &sp = p.st[s];
     const int g = gc / NCOL, col = gc - g * NCOL;
-    int c0, c1, first_slot;
+    int c0, c1, first_slot, rg = g;
     if (p.mode == MODE_RANGES || p.mode == MODE_SPARSE) {
         // the ranges that hold the unit; their CTAs' partial slots
         const int64_t ub = sp.toff, ue = ub + sp.nt;
         c0 = range_of(p, ub);
         c1 = range_of(p, ue - 1);
         first_slot = 2 * (c0 * p.rep + g) + (ub == p.rb[c0] ? 0 : 1);
+    } else if (p.mode == MODE_UNITS) {
+        // the same over positions (unit, tile), one CTA a range
+        const int64_t u = (int64_t)s * p.groups + g;
+        const int64_t nt = (unit_keys(sp.len, p.R, p.H, p.ncols, g) + BK - 1) / BK;
+        const int64_t ub = unit_pos(u, 0);
+        c0 = range_of(p, ub);
+        c1 = range_of(p, unit_pos(u, nt - 1));
+        rg = 0;
+        first_slot = 2 * c0 + (ub == p.rb[c0] ? 0 : 1);
     } else {
         if (p.mode != MODE_SPLITS || sp.nsplit <= 1) return;
         c0 = 0;
@@ -1165,9 +1233,9 @@ __global__ void __launch_bounds__(COMBINE_THREADS) mla_combine_kernel(const __gr
         first_slot = sp.slot0 + g * sp.nsplit;
     }
     if (c0 == c1) return;
-    const bool ranges = p.mode == MODE_RANGES || p.mode == MODE_SPARSE;
+    const bool ranges = p.mode != MODE_SPLITS;
     const int n = c1 - c0 + 1;
-    auto slot_of = [&](int j) { return j == 0 ? first_slot : ranges ? 2 * ((c0 + j) * p.rep + g) : first_slot + j; };
+    auto slot_of = [&](int j) { return j == 0 ? first_slot : ranges ? 2 * ((c0 + j) * p.rep + rg) : first_slot + j; };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ float red_m[COMBINE_THREADS / 32];
     __shared__ float red_l[COMBINE_THREADS / 32];
@@ -1230,8 +1298,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS) mla_combine_kernel(const __gr
 }
 
 // ---- host-side plans ----
-// RANGES: a range holds at least MIN_TILES key tiles, and there are at most as many
-// CTAs as the device has SMs.  Launches with more than a quarter as many column
+// RANGES and UNITS: a range holds at least MIN_TILES key tiles, and there are at most as
+// many CTAs as the device has SMs.  Launches with more than a quarter as many column
 // groups as SMs run UNITS.
 struct Plan {
     int mode;
@@ -1269,6 +1337,69 @@ inline Split split_of(int64_t len, int groups) {
 
 constexpr int64_t SEG_COST = 3;   // a segment start, in key tiles
 
+// UNITS: cut the units' tiles (stream-major, each unit as many tiles as its last column
+// sees) into at most `sms` ranges, writing their bounds b[0..n] as unit_pos values and
+// returning n; *cut tells whether a bound falls inside a unit (which leaves partials).
+// Weights: a unit's start (a query load, an epilogue) counts SEG_COST tiles.  A bound inside
+// a unit of 32 or more tiles lies on one of its eighths, so the CTAs read at no more than
+// eight key positions in step (one DRAM read of a tile serves every CTA at its position).
+// The ranges are packed greedily up to a load limit, and the limit is the smallest under
+// which `n` ranges cover every unit (a binary search), so the longest range is as short as
+// the eighths allow.
+inline int plan_unit_ranges(int S, int R, int H, int groups, const int64_t *h_len, int sms, int64_t *b, bool *cut) {
+    const int64_t units = (int64_t)S * groups;
+    const int ncols = R * H;
+    std::vector<int64_t> nt(units), w0(units + 1);   // tiles of each unit; weighted start
+    w0[0] = 0;
+    for (int64_t u = 0; u < units; ++u) {
+        const int s = (int)(u / groups);
+        nt[u] = (unit_keys(h_len[s], R, H, ncols, (int)(u - (int64_t)s * groups)) + BK - 1) / BK;
+        w0[u + 1] = w0[u] + nt[u] + SEG_COST;
+    }
+    const int64_t W = w0[units];
+    auto weight = [&](int64_t x) {
+        const int64_t u = x >> 32, t = x & 0xffffffffll;
+        return t == 0 ? w0[u] : w0[u] + SEG_COST + t;
+    };
+    // the furthest allowed bound at weight <= lim (units + 1 past the end: none beyond x)
+    auto furthest = [&](int64_t lim) {
+        if (lim >= W) return unit_pos(units, 0);
+        const int64_t u = (int64_t)(std::upper_bound(w0.begin(), w0.end(), lim) - w0.begin()) - 1;
+        const int64_t r = lim - w0[u] - SEG_COST;
+        int64_t t = r < 0 ? 0 : (r > nt[u] ? nt[u] : r);
+        if (nt[u] >= 32) t = t * 8 / nt[u] * nt[u] / 8;
+        return t >= nt[u] ? unit_pos(u + 1, 0) : unit_pos(u, t);
+    };
+    // ranges needed under a load limit (cap + 1: more than cap)
+    auto count = [&](int64_t limit, int cap, int64_t *out) {
+        int64_t x = unit_pos(0, 0);
+        const int64_t end = unit_pos(units, 0);
+        int n = 0;
+        if (out) out[0] = x;
+        while (x < end) {
+            if (n == cap) return cap + 1;
+            const int64_t y = furthest(weight(x) + limit);
+            if (y <= x) return cap + 1;
+            x = y;
+            ++n;
+            if (out) out[n] = x;
+        }
+        return n;
+    };
+    const int64_t want = (W + MIN_TILES - 1) / MIN_TILES;
+    int cap = (int)(want < sms ? want : sms);
+    if (cap < 1) cap = 1;
+    int64_t lo = (W + cap - 1) / cap, hi = W;
+    while (lo < hi) {
+        const int64_t mid = lo + (hi - lo) / 2;
+        if (count(mid, cap, nullptr) <= cap) hi = mid; else lo = mid + 1;
+    }
+    const int n = count(lo, cap, b);
+    *cut = false;
+    for (int i = 1; i < n; ++i) *cut |= (b[i] & 0xffffffffll) != 0;
+    return n;
+}
+
 inline Plan plan_of(int S, int R, int H, const int64_t *h_len, int sms, bool invariant, int64_t *rb = nullptr) {
     Plan pl;
     // R * H itself can pass INT32_MAX; callers refuse S * R * H above 2^30, so groups fits an int
@@ -1290,7 +1421,11 @@ inline Plan plan_of(int S, int R, int H, const int64_t *h_len, int sms, bool inv
     if (groups * 4 > sms) {
         pl.mode = MODE_UNITS;
         pl.total = (int64_t)S * groups;
-        pl.nctas = (int)(pl.total < sms ? pl.total : sms);
+        int64_t rb_local[MAX_CTAS + 1];
+        bool cut = false;
+        pl.nranges = plan_unit_ranges(S, R, H, groups, h_len, sms, rb ? rb : rb_local, &cut);
+        pl.nctas = pl.nranges;
+        pl.slots = cut ? 2 * (size_t)pl.nctas : 0;
         return pl;
     }
     pl.mode = MODE_RANGES;
@@ -1389,11 +1524,12 @@ int attend_plan_info(int S, int R, int H, const int64_t *h_len, int sms, bool in
     const int groups = (int)(((int64_t)R * H + attn::NCOL - 1) / attn::NCOL);
     info->mode = pl.mode;
     info->ctas = pl.nctas;
-    info->nranges = pl.mode == attn::MODE_RANGES ? pl.nranges : 0;
+    const bool ranged = pl.mode == attn::MODE_RANGES || pl.mode == attn::MODE_UNITS;
+    info->nranges = ranged ? pl.nranges : 0;
     info->groups = groups;
     info->work = pl.total;
     info->slots = (int64_t)pl.slots;
-    if (range_bounds && pl.mode == attn::MODE_RANGES)
+    if (range_bounds && ranged)
         for (int i = 0; i <= pl.nranges; ++i) range_bounds[i] = rb[i];
     if (split_keys && pl.mode == attn::MODE_SPLITS)
         for (int s = 0; s < S; ++s) split_keys[s] = attn::split_of(h_len[s], groups).split;
@@ -1625,7 +1761,9 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
     }
     if (slots) {
         ProfScope prof(pool, kProfCombine, st);
-        const cudaError_t e = launch_pdl(mla_combine_kernel, dim3(R * H, S), dim3(COMBINE_THREADS), 0, st, p);
+        // UNITS: only the units a range bound cuts
+        const dim3 grid = pl.mode == MODE_UNITS ? dim3(NCOL, pl.nranges - 1) : dim3(R * H, S);
+        const cudaError_t e = launch_pdl(mla_combine_kernel, grid, dim3(COMBINE_THREADS), 0, st, p);
         launch_counter()++;
         if (e != cudaSuccess) return TF_E_CUDA;
     }

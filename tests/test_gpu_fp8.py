@@ -170,8 +170,8 @@ def test_invariant_pool_workspace_and_static_call():
 def test_fp8_attention_is_bf16_attention_over_the_expanded_rows(R, H):
     """The kernel reads FP8 codes and expands them to bf16(code * scale) in shared memory, then
     runs the BF16 pipeline: so it must equal, bit for bit, the BF16 attention over a pool that
-    holds those bf16 values.  R = 64 at 64 heads deals whole units (the prefill plan), the
-    others ranges of key tiles."""
+    holds those bf16 values.  R = 64 at 64 heads runs the prefill plan (ranges over
+    (stream, row) units), the others ranges of key tiles shared by the column groups."""
     lens = [700, 3000, 65]
     share = [(-1, 0), (0, 1), (-1, 0)]   # the owner's first page is full (700 rows)
     w8 = Y.custom(f"f8eq_{R}", 68 + R, lens=lens, R=R, H=H, share=share)

@@ -159,8 +159,9 @@ def _lens(seed, n, lo, hi):
 
 # Batches shaped to reach every branch of the work plan: many short streams (CTAs walking
 # several segments, with query reloads and mid-range epilogues), the most streams and heads
-# the API takes, column groups side by side (2, 4 and 10 groups, ragged last group), whole
-# units round robin (prefill-like, several streams), and the batch-invariant split plan.
+# the API takes, column groups side by side (2, 4 and 10 groups, ragged last group), ranges
+# over (stream, column group) units (prefill-like, several streams; 64 and 16 heads, so a group
+# is one row or four), and the batch-invariant split plan.
 PLAN_SHAPES = [
     ("segments", 60, _lens(60, 200, 1, 600), 1, 8, False),
     ("max_streams", 61, _lens(61, 512, 1, 300), 1, 16, False),
@@ -168,6 +169,7 @@ PLAN_SHAPES = [
     ("ragged_groups", 63, [3000, 40, 700], 5, 24, False),
     ("ten_groups", 64, [2500, 1300], 40, 16, False),
     ("units", 65, [1200, 700, 160], 160, 64, False),
+    ("units_h16", 69, [3000, 400], 200, 16, False),
     ("invariant_groups", 66, [5000, 17, 900, 12000], 2, 128, True),
     ("invariant_units", 67, [1200, 700, 160], 160, 64, True),
 ]

@@ -395,13 +395,72 @@ def test_plan_and_workspace_agree(L):
     assert B.tf_paged_mla_workspace_bytes(None, w.S, w.R, w.H, w.lens) == want
 
 
-def test_prefill_plan_deals_whole_units(L):
+def _unit_ranges(pl, lens, R, H):
+    """Per range of a mode-1 plan: (64-key tiles, segments, cut positions inside units), walking
+    the bounds over units that each hold as many tiles as their last column sees."""
+    G, ncols = pl["groups"], R * H
+
+    def nt(u):
+        s, g = divmod(u, G)
+        clast = min(64 * g + 63, ncols - 1)
+        return -(-(int(lens[s]) - R + clast // H + 1) // 64)
+
+    out = []
+    b = [divmod(int(x), 1 << 32) for x in pl["bounds"]]
+    for c in range(pl["nranges"]):
+        (u, t), end = b[c], b[c + 1]
+        tiles = segs = 0
+        while (u, t) < end:
+            e = end[1] if u == end[0] else nt(u)
+            tiles += e - t
+            segs += 1
+            u, t = u + 1, 0
+        out.append((tiles, segs))
+    cuts = [(u, t, nt(u)) for u, t in b[1:-1] if t != 0]
+    return out, cuts, sum(nt(u) for u in range(pl["work"]))
+
+
+@pytest.mark.parametrize("name", ["prefill_100k", "prefill_208k"])
+def test_prefill_plan_balances_tile_ranges(L, name):
+    """A prefill chunk's units are cut into equal ranges of key tiles, one CTA each: no CTA
+    carries a whole extra unit (2,048 or 1,024 units over 152 SMs dealt round robin leave 14
+    against 13.5, or 7 against 6.7), cuts inside a unit fall on its eighths, and each unit reads
+    only the tiles its last row sees."""
     from paged_mla_kv_gb300 import synth as Y
-    w = Y.WORKLOADS["prefill_100k"]()
+    w = Y.WORKLOADS[name]()
     pl = B.tf_paged_mla_plan_info(w.S, w.R, w.H, w.lens, sms=152)
-    assert pl["mode"] == 1 and pl["groups"] == 2048 and pl["work"] == 2048
-    assert pl["ctas"] == 152 and pl["slots"] == 0
-    assert B.tf_paged_mla_workspace_bytes(None, w.S, w.R, w.H, w.lens) == 0
+    assert pl["mode"] == 1 and pl["groups"] == w.R and pl["work"] == w.R
+    assert pl["ctas"] == pl["nranges"] == 152 and pl["slots"] == 2 * 152
+    assert pl["bounds"][0] == 0 and pl["bounds"][-1] == w.R << 32
+    ranges, cuts, total = _unit_ranges(pl, w.lens, w.R, w.H)
+    L0 = int(w.lens[0])
+    # row r of the chunk sees L0 - R + r + 1 keys; a 64-head group is one row
+    assert total == sum(-(-(L0 - w.R + r + 1) // 64) for r in range(w.R))
+    assert sum(t for t, _ in ranges) == total
+    loads = [t + 3 * n for t, n in ranges]     # a segment start weighs three tiles
+    mean = sum(loads) / len(loads)
+    unit = total / w.R
+    assert max(loads) <= mean + unit / 8 + 6   # within an eighth of a unit of the mean
+    assert max(loads) <= 1.01 * mean
+    assert max(loads) < 0.99 * (-(-w.R // 152)) * unit    # whole units round robin: 3-4% more
+    assert cuts and all(t in [k * n // 8 for k in range(1, 8)] for _, t, n in cuts)
+    # the workspace holds the partials of the plan made for the current device (or without one)
+    slots = B.tf_paged_mla_plan_info(w.S, w.R, w.H, w.lens)["slots"]
+    want = slots * 64 * 512 * 4 + (-(-(slots * 64 * 2 * 4) // 256)) * 256
+    assert slots > 0 and B.tf_paged_mla_workspace_bytes(None, w.S, w.R, w.H, w.lens) == want
+
+
+def test_unit_plan_ranges_cover_every_tile_once(L):
+    """Mode 1 on small and ragged shapes: the ranges tile the units' numbering without gaps or
+    overlaps, every range is non-empty, and short units are cut at tile granularity."""
+    for lens, R, H, sms in [([1200, 700, 160], 160, 64, 152), ([3000, 400], 200, 16, 152),
+                            ([5000], 300, 64, 7), ([300, 260, 256], 256, 64, 152), ([64] * 3, 64, 64, 152)]:
+        pl = B.tf_paged_mla_plan_info(len(lens), R, H, lens, sms=sms)
+        assert pl["mode"] == 1 and 1 <= pl["ctas"] == pl["nranges"] <= sms
+        ranges, cuts, total = _unit_ranges(pl, lens, R, H)
+        assert all(t > 0 for t, _ in ranges)
+        assert sum(t for t, _ in ranges) == total
+        assert pl["slots"] == (2 * pl["ctas"] if cuts else 0)
 
 
 def test_invariant_splits_depend_on_the_stream_alone(L):

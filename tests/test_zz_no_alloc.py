@@ -77,7 +77,7 @@ def test_static_scratch_covers_every_default_launch():
     BUILD.build()
     # on a default pool, partials come only from units cut by a CTA range boundary, two
     # a CTA at most, so the scratch serves any batch: many long streams, a 1M-token
-    # window, prefill chunks (whole units, no partials)
+    # window, prefill chunks (ranges of key tiles over the chunk's units)
     cases = [(np.full(512, 65536, np.int64), 1, 64), (np.array([1 << 20] + [8192] * 7, np.int64), 2, 64),
              (np.array([102048], np.int64), 2048, 64), (np.array([209024], np.int64), 1024, 64),
              (np.full(64, 300000, np.int64), 2, 128)]
