@@ -94,6 +94,12 @@ constexpr int THREADS = 352;
 // last round, boxes 6-7, reads all its rows first).
 constexpr int THREADS_F8 = THREADS + 128;
 constexpr int F8_THREADS = THREADS_F8 - THREADS;   // two threads a tile row
+// Listed rows on BF16 pages: warps 11-14 copy each tile's rows with cp.async, 16 rows a warp
+// (on this GPU 16-byte copies from four warps gather random 1 KB rows about twice as fast as
+// TMA gather4 issued by one warp).
+constexpr int LOAD_THREADS = 128;
+template <int MODE, bool FP8>
+constexpr int kernel_threads() { return FP8 || MODE == 3 ? THREADS + 128 : THREADS; }
 constexpr int F8_BOX_BYTES = BK * 64;            // dense: [64 rows][64 codes]
 constexpr int F8_BLK = 256;                      // gathered: codes a box row (the unswizzled maximum)
 constexpr int F8_BLK_BYTES = BK * F8_BLK;        // [64 rows][256 codes] = 16 KB
@@ -353,9 +359,11 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tm, ui
 //    epilogue of the previous segment has read the accumulator.
 
 template <int MODE, bool FP8 = false>
-__global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kernel_threads<MODE, FP8>(), 1) mla_attend_kernel(const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // listed rows on BF16 pages arrive by the loader warps' cp.async copies
+    constexpr bool CP_ROWS = MODE == MODE_SPARSE && !FP8;
     Ctrl &c = *reinterpret_cast<Ctrl *>(smem + SMEM_CTRL);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ptx::griddep_launch_dependents();
@@ -376,8 +384,8 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
         for (int i = 0; i < NROPE; ++i) {
             // BF16: the TMA warp's one arrival with the tile's bytes; FP8: one arrival a pair the
             // expansion warps finish
-            ptx::mbar_init(&c.tile_full[i], FP8 ? 4 : 1);
-            ptx::mbar_init(&c.tile_half[i], 1);
+            ptx::mbar_init(&c.tile_full[i], FP8 ? 4 : CP_ROWS ? LOAD_THREADS : 1);
+            ptx::mbar_init(&c.tile_half[i], CP_ROWS ? LOAD_THREADS : 1);
             ptx::mbar_init(&c.rope_empty[i], 1);
             ptx::mbar_init(&c.p_full[i], 5);       // four softmax warps and the rescale warps
             ptx::mbar_init(&c.corr_req[i], 4);
@@ -474,6 +482,7 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
                 }
                 if (!__shfl_sync(0xffffffffu, okq, 0)) break;
                 q_armed = si;
+                if constexpr (CP_ROWS) continue;   // the loader warps copy the rows
                 const int32_t *list = p.idx + (size_t)q.s * p.max_idx;
                 const int rows = p.st[q.s].split;
                 // list position k0 + 2 lane + h of tile tl2; past the list's end a listed row is
@@ -760,6 +769,8 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             // long as four MMAs, so the MMAs go out in long runs
             if (!ptx::mbar_wait_warp(HALF ? &c.tile_half[rs] : &c.tile_full[rs], rope_use(tq) & 1, abort, errp, 3))
                 return false;
+            // rows copied by cp.async (generic proxy) become visible to the tensor cores' reads
+            if (CP_ROWS) ptx::fence_proxy_async_smem();
             zero_tail(0, HALF ? 4 : 8, true);
             // order the MMAs after the softmax's TMEM loads of S (s_free) and the queries' TMEM
             // stores (q_tmem_full, waited before a segment's first tile); the key boxes come by
@@ -771,6 +782,7 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             if (HALF) {
                 latent(0, 4);
                 if (!ptx::mbar_wait_warp(&c.tile_full[rs], rope_use(tq) & 1, abort, errp, 3)) return false;
+                if (CP_ROWS) ptx::fence_proxy_async_smem();
                 zero_tail(4, 8, false);
                 latent(4, 8);
             } else {
@@ -824,6 +836,104 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
             ptx::mma_commit(&c.drain);
             ptx::mbar_wait(&c.drain, 0, abort, errp, 6, 1ll << 29);
         }
+        __syncwarp();
+    } else if (CP_ROWS && warp >= 11) {
+        // ================= listed-row loaders (warps 11-14): rows 16 lw .. 16 lw + 15 of each tile =================
+        // A listed row is 1,024 bytes of latent values and 128 of rope: 64 + 8 copies of 16 bytes
+        // into the 128-byte-swizzled boxes (chunk c of tile row r at r * 128 + 16 (c ^ (r mod 8))).
+        // The rope box and latent boxes 0-3 (pairs 0-1) complete tile_half, boxes 4-7 tile_full;
+        // each barrier counts one arrival a loader thread, made once its earlier copies are done.
+        const int lw = warp - 11;
+        const uint64_t pol_kv = ptx::policy_evict_first();
+        bool stop = false;
+        int gt = 0;
+        SegIter<MODE> it(p);
+        Seg q;
+        // lane 0 waits until pair j of tile gt (j < 0: its rope slot) is free, for the whole warp
+        auto slot_free = [&](int j) -> bool {
+            int ok = 1;
+            if (lane == 0) {
+                const uint32_t u = j < 0 ? rope_use(gt) : pair_use(gt, j);
+                uint64_t *bar = j < 0 ? &c.rope_empty[rope_slot(gt)] : &c.pair_empty[pair_slot(gt, j)];
+                ok = u == 0 || ptx::mbar_wait(bar, (u - 1) & 1, abort, errp, 19);
+            }
+            return __shfl_sync(0xffffffffu, ok, 0) != 0;
+        };
+        while (!stop && it.next(p, q)) {
+            const int32_t *list = p.idx + (size_t)q.s * p.max_idx;
+            const int rows = p.st[q.s].split;
+            for (int tl = 0; tl < q.nt; ++tl, ++gt) {
+                const int rs = rope_slot(gt);
+                // lane l < 16: tile row 16 lw + l, from its page (past the list's end a listed row
+                // is copied again; the softmax masks it)
+                const char *base = nullptr;   // the row's page
+                int ri = 0, bad = 0, badv = 0;
+                if (lane < 16) {
+                    const int64_t pos = q.kb + (int64_t)tl * BK + 16 * lw + lane;
+                    const int r = __ldg(list + (pos < q.len ? pos : 0));
+                    if (r < 0 || r >= rows) {
+                        bad = 1;
+                        badv = r;
+                    } else {
+                        const int lp = r >> 9;
+                        const int pg = windowed ? q.s * max_pages + lp : __ldg(pt + (int64_t)q.s * max_pages + lp);
+                        if (pg < 0 || pg >= num_pages) {
+                            bad = 1;
+                            badv = pg;
+                        } else {
+                            base = p.pool_base + ((size_t)cache * num_pages + pg) * kPageBytes;
+                            ri = r & 511;
+                        }
+                    }
+                }
+                const unsigned badm = __ballot_sync(0xffffffffu, bad);
+                if (badm) {
+                    const int v = __shfl_sync(0xffffffffu, badv, __ffs(badm) - 1);
+                    if (lane == 0) {
+                        ptx::record_error(errp, TF_E_DEVICE, v);
+                        *abort = 1;
+                    }
+                    stop = true;
+                    break;
+                }
+                // first half: the rope box (four rows an instruction) and latent values 0-255
+                if (!slot_free(-1) || !slot_free(0) || !slot_free(1)) {
+                    stop = true;
+                    break;
+                }
+#pragma unroll 4
+                for (int rr = 0; rr < 16; ++rr) {
+                    const char *b = reinterpret_cast<const char *>(__shfl_sync(0xffffffffu, (unsigned long long)base, rr));
+                    const int i = __shfl_sync(0xffffffffu, ri, rr), tr = 16 * lw + rr;
+                    ptx::cp_async16(smem + box_off(gt, lane >> 3) + tr * 128 + (((lane & 7) ^ (tr & 7)) << 4),
+                                    b + (size_t)i * (kLat * 2) + lane * 16, pol_kv);
+                }
+#pragma unroll
+                for (int g4 = 0; g4 < 4; ++g4) {
+                    const int rr = 4 * g4 + (lane >> 3);
+                    const char *b = reinterpret_cast<const char *>(__shfl_sync(0xffffffffu, (unsigned long long)base, rr));
+                    const int i = __shfl_sync(0xffffffffu, ri, rr), tr = 16 * lw + rr;
+                    ptx::cp_async16(smem + box_off(gt, 8) + tr * 128 + (((lane & 7) ^ (tr & 7)) << 4),
+                                    b + kLatBlockBytes + (size_t)i * (kRope * 2) + (lane & 7) * 16, pol_kv);
+                }
+                ptx::cp_async_arrive(&c.tile_half[rs]);
+                // second half: latent values 256-511 (pairs 2-3)
+                if (!slot_free(2) || !slot_free(3)) {
+                    stop = true;
+                    break;
+                }
+#pragma unroll 4
+                for (int rr = 0; rr < 16; ++rr) {
+                    const char *b = reinterpret_cast<const char *>(__shfl_sync(0xffffffffu, (unsigned long long)base, rr));
+                    const int i = __shfl_sync(0xffffffffu, ri, rr), tr = 16 * lw + rr;
+                    ptx::cp_async16(smem + box_off(gt, 4 + (lane >> 3)) + tr * 128 + (((lane & 7) ^ (tr & 7)) << 4),
+                                    b + (size_t)i * (kLat * 2) + 512 + lane * 16, pol_kv);
+                }
+                ptx::cp_async_arrive(&c.tile_full[rs]);
+            }
+        }
+        // no copy may still be writing shared memory when the CTA exits
+        ptx::cp_async_wait_all();
         __syncwarp();
     } else if (FP8 && warp >= 11) {
         // ================= FP8 expansion (warps 11-14): half a tile row a thread =================
@@ -1188,113 +1298,189 @@ __global__ void __launch_bounds__(FP8 ? THREADS_F8 : THREADS, 1) mla_attend_kern
 // Merge a unit's partials (m_j, l_j, o_j), j in key order:
 //   M = max_j m_j,  w_j = 2^(m_j - M),  out = sum_j w_j o_j / sum_j w_j l_j,
 //   lse = (M + log2 sum_j w_j l_j) * ln 2.
-// One 256-thread block per (stream, column); UNITS: per (column of the group, range bound),
-// where a bound inside a unit that no earlier bound cuts stands for that unit.  Warp w sums
-// the partials j = w, w + 8,
-// ... (lane: 16 latent columns, four independent 16-byte loads a partial), then the
-// eight warp sums are added in warp order: a fixed order, so the result is the same
-// on every call.
+// Lane l of a warp holds values 4 (l + 32 i) .. + 3 (i < 4) of one column.
+//  - Few partials a unit (at most 8, the common case for listed rows, short batches and prefill
+//    chunks): a block per (stream, column group, four columns), a warp a column, adding the
+//    partials one after another in key order; the lanes first fetch the (m_j, l_j) pairs side
+//    by side, 32 at a time.
+//  - More partials (long streams cut by many ranges): a 256-thread block per (stream, column);
+//    warp w adds
+//    the partials j = w, w + 8, ... in key order and the eight warp sums are added in warp
+//    order.
+// Either way the order is fixed, so the result is the same on every call.  UNITS: blockIdx.y is
+// a range bound, and a bound inside a unit that no earlier bound cuts stands for that unit.
 constexpr int COMBINE_THREADS = 256;
+constexpr int COMBINE_COLS = 4;         // columns a block of the warp-a-column form
+constexpr int COMBINE_NARROW_MAX = 8;   // partials a unit that form takes
 
-__global__ void __launch_bounds__(COMBINE_THREADS) mla_combine_kernel(const __grid_constant__ Params p) {
-    ptx::griddep_launch_dependents();
-    ptx::griddep_wait();
-    int s = blockIdx.y, gc = blockIdx.x;
+// The unit (stream s, group g) of a combine block and the workspace slots of its partials, in
+// key order: slot_of(j) for j < n.  False: nothing to merge (the unit is whole).
+struct CombineUnit {
+    int s, g, c0, n, first_slot, rg;
+    bool ranges;
+    __device__ __forceinline__ int slot_of(const Params &p, int j) const {
+        return j == 0 ? first_slot : ranges ? 2 * ((c0 + j) * p.rep + rg) : first_slot + j;
+    }
+};
+__device__ __forceinline__ bool combine_unit(const Params &p, CombineUnit &cu) {
     if (p.mode == MODE_UNITS) {
         const int64_t x = p.rb[blockIdx.y + 1], xp = p.rb[blockIdx.y];
         const int64_t u = x >> 32;
-        if ((x & 0xffffffffll) == 0 || ((xp >> 32) == u && (xp & 0xffffffffll) != 0)) return;
-        s = (int)(u / p.groups);
-        gc = (int)(u - (int64_t)s * p.groups) * NCOL + (int)blockIdx.x;
+        if ((x & 0xffffffffll) == 0 || ((xp >> 32) == u && (xp & 0xffffffffll) != 0)) return false;
+        cu.s = (int)(u / p.groups);
+        cu.g = (int)(u - (int64_t)cu.s * p.groups);
+    } else {
+        cu.s = blockIdx.z;
+        cu.g = blockIdx.y;
     }
-    if (gc >= p.ncols) return;
-    const StreamPlan &sp = p.st[s];
-    const int g = gc / NCOL, col = gc - g * NCOL;
-    int c0, c1, first_slot, rg = g;
+    const StreamPlan &sp = p.st[cu.s];
+    int c1;
+    cu.rg = cu.g;
     if (p.mode == MODE_RANGES || p.mode == MODE_SPARSE) {
         // the ranges that hold the unit; their CTAs' partial slots
         const int64_t ub = sp.toff, ue = ub + sp.nt;
-        c0 = range_of(p, ub);
+        cu.c0 = range_of(p, ub);
         c1 = range_of(p, ue - 1);
-        first_slot = 2 * (c0 * p.rep + g) + (ub == p.rb[c0] ? 0 : 1);
+        cu.first_slot = 2 * (cu.c0 * p.rep + cu.g) + (ub == p.rb[cu.c0] ? 0 : 1);
     } else if (p.mode == MODE_UNITS) {
         // the same over positions (unit, tile), one CTA a range
-        const int64_t u = (int64_t)s * p.groups + g;
-        const int64_t nt = (unit_keys(sp.len, p.R, p.H, p.ncols, g) + BK - 1) / BK;
+        const int64_t u = (int64_t)cu.s * p.groups + cu.g;
+        const int64_t nt = (unit_keys(sp.len, p.R, p.H, p.ncols, cu.g) + BK - 1) / BK;
         const int64_t ub = unit_pos(u, 0);
-        c0 = range_of(p, ub);
+        cu.c0 = range_of(p, ub);
         c1 = range_of(p, unit_pos(u, nt - 1));
-        rg = 0;
-        first_slot = 2 * c0 + (ub == p.rb[c0] ? 0 : 1);
+        cu.rg = 0;
+        cu.first_slot = 2 * cu.c0 + (ub == p.rb[cu.c0] ? 0 : 1);
     } else {
-        if (p.mode != MODE_SPLITS || sp.nsplit <= 1) return;
-        c0 = 0;
+        if (p.mode != MODE_SPLITS || sp.nsplit <= 1) return false;
+        cu.c0 = 0;
         c1 = sp.nsplit - 1;
-        first_slot = sp.slot0 + g * sp.nsplit;
+        cu.first_slot = sp.slot0 + cu.g * sp.nsplit;
     }
-    if (c0 == c1) return;
-    const bool ranges = p.mode != MODE_SPLITS;
-    const int n = c1 - c0 + 1;
-    auto slot_of = [&](int j) { return j == 0 ? first_slot : ranges ? 2 * ((c0 + j) * p.rep + rg) : first_slot + j; };
+    cu.n = c1 - cu.c0 + 1;
+    cu.ranges = p.mode != MODE_SPLITS;
+    return cu.n > 1;
+}
+
+__device__ __forceinline__ void combine_store(const Params &p, const CombineUnit &cu, int gc, int lane, float M,
+                                              float L, const float4 (&acc)[4]) {
+    const float inv = 1.f / L;
+    const size_t orow = (size_t)cu.s * p.ncols + gc;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(p.out + orow * kLat) + 2 * (lane + 32 * i);
+        o2[0] = __floats2bfloat162_rn(acc[i].x * inv, acc[i].y * inv);
+        o2[1] = __floats2bfloat162_rn(acc[i].z * inv, acc[i].w * inv);
+    }
+    if (lane == 0 && p.lse) p.lse[orow] = (M + log2f(L)) * 0.69314718055994531f;
+}
+
+// acc += w * o_j (the column's 512 values, lane's share)
+__device__ __forceinline__ void combine_add(float4 (&acc)[4], const float *o, int lane, float w) {
+    const float4 *o4 = reinterpret_cast<const float4 *>(o);
+    float4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __ldg(o4 + lane + 32 * i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc[i].x = __fmaf_rn(w, v[i].x, acc[i].x);
+        acc[i].y = __fmaf_rn(w, v[i].y, acc[i].y);
+        acc[i].z = __fmaf_rn(w, v[i].z, acc[i].z);
+        acc[i].w = __fmaf_rn(w, v[i].w, acc[i].w);
+    }
+}
+
+template <bool WIDE>
+__global__ void __launch_bounds__(WIDE ? COMBINE_THREADS : COMBINE_COLS * 32) mla_combine_kernel(const __grid_constant__ Params p) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
+    CombineUnit cu;
+    if (!combine_unit(p, cu)) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __shared__ float red_m[COMBINE_THREADS / 32];
-    __shared__ float red_l[COMBINE_THREADS / 32];
-    __shared__ float4 red_o[COMBINE_THREADS / 32][128];
-    float m = -INFINITY;
-    for (int j = threadIdx.x; j < n; j += COMBINE_THREADS)
-        m = fmaxf(m, __ldg(p.ws_ml + ((size_t)slot_of(j) * NCOL + col) * 2));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) red_m[warp] = m;
-    __syncthreads();
-    float M = red_m[0];
-#pragma unroll
-    for (int w = 1; w < COMBINE_THREADS / 32; ++w) M = fmaxf(M, red_m[w]);
+    const int col = WIDE ? (int)blockIdx.x : (int)blockIdx.x * COMBINE_COLS + warp;   // column of the group
+    const int gc = cu.g * NCOL + col;
+    if (gc >= p.ncols) return;   // WIDE: the whole block
+    const int n = cu.n;
     float4 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = 0.f;
-#pragma unroll 2
-    for (int j = warp; j < n; j += COMBINE_THREADS / 32) {
-        const size_t base = (size_t)slot_of(j) * NCOL + col;
-        const float mj = __ldg(p.ws_ml + base * 2), lj = __ldg(p.ws_ml + base * 2 + 1);
-        const float w = (mj == -INFINITY) ? 0.f : ptx::ex2(mj - M);
-        const float4 *o = reinterpret_cast<const float4 *>(p.ws_o + base * kLat);
-        float4 v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = __ldg(o + lane + 32 * i);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            acc[i].x += w * v[i].x;
-            acc[i].y += w * v[i].y;
-            acc[i].z += w * v[i].z;
-            acc[i].w += w * v[i].w;
+    if constexpr (!WIDE) {
+        // lane j fetches the (m, l) of partial j0 + j; the weights go round by shuffles
+        auto ml = [&](int j, float &m, float &l) {
+            m = -INFINITY;
+            l = 0.f;
+            if (j < n) {
+                const size_t base = (size_t)cu.slot_of(p, j) * NCOL + col;
+                m = __ldg(p.ws_ml + base * 2);
+                l = __ldg(p.ws_ml + base * 2 + 1);
+            }
+        };
+        float M = -INFINITY;
+        for (int j0 = 0; j0 < n; j0 += 32) {
+            float m, l;
+            ml(j0 + lane, m, l);
+            M = fmaxf(M, m);
         }
-        L += w * lj;
-    }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) red_o[warp][lane + 32 * i] = acc[i];
-    if (lane == 0) red_l[warp] = L;
-    __syncthreads();
-    if (threadIdx.x >= 128) return;
-    const int d4 = threadIdx.x;
-    float4 tot = red_o[0][d4];
-    float Lt = red_l[0];
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        for (int j0 = 0; j0 < n; j0 += 32) {
+            float mj, lj;
+            ml(j0 + lane, mj, lj);
+            const float wj = (mj == -INFINITY) ? 0.f : ptx::ex2(mj - M);
+            const int cnt = min(32, n - j0);
+#pragma unroll 4
+            for (int k = 0; k < cnt; ++k) {
+                const float w = __shfl_sync(0xffffffffu, wj, k);
+                combine_add(acc, p.ws_o + ((size_t)cu.slot_of(p, j0 + k) * NCOL + col) * kLat, lane, w);
+                L = __fmaf_rn(w, __shfl_sync(0xffffffffu, lj, k), L);
+            }
+        }
+        combine_store(p, cu, gc, lane, M, L, acc);
+    } else {
+        __shared__ float red_m[COMBINE_THREADS / 32];
+        __shared__ float red_l[COMBINE_THREADS / 32];
+        __shared__ float4 red_o[COMBINE_THREADS / 32][128];
+        float m = -INFINITY;
+        for (int j = threadIdx.x; j < n; j += COMBINE_THREADS)
+            m = fmaxf(m, __ldg(p.ws_ml + ((size_t)cu.slot_of(p, j) * NCOL + col) * 2));
 #pragma unroll
-    for (int w = 1; w < COMBINE_THREADS / 32; ++w) {
-        const float4 x = red_o[w][d4];
-        tot.x += x.x;
-        tot.y += x.y;
-        tot.z += x.z;
-        tot.w += x.w;
-        Lt += red_l[w];
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) red_m[warp] = m;
+        __syncthreads();
+        float M = red_m[0];
+#pragma unroll
+        for (int w = 1; w < COMBINE_THREADS / 32; ++w) M = fmaxf(M, red_m[w]);
+#pragma unroll 2
+        for (int j = warp; j < n; j += COMBINE_THREADS / 32) {
+            const size_t base = (size_t)cu.slot_of(p, j) * NCOL + col;
+            const float mj = __ldg(p.ws_ml + base * 2), lj = __ldg(p.ws_ml + base * 2 + 1);
+            const float w = (mj == -INFINITY) ? 0.f : ptx::ex2(mj - M);
+            combine_add(acc, p.ws_o + base * kLat, lane, w);
+            L = __fmaf_rn(w, lj, L);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) red_o[warp][lane + 32 * i] = acc[i];
+        if (lane == 0) red_l[warp] = L;
+        __syncthreads();
+        if (warp > 0) return;
+        float Lt = red_l[0];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = red_o[0][lane + 32 * i];
+#pragma unroll
+        for (int w = 1; w < COMBINE_THREADS / 32; ++w) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 x = red_o[w][lane + 32 * i];
+                acc[i].x += x.x;
+                acc[i].y += x.y;
+                acc[i].z += x.z;
+                acc[i].w += x.w;
+            }
+            Lt += red_l[w];
+        }
+        combine_store(p, cu, gc, lane, M, Lt, acc);
     }
-    const float inv = 1.f / Lt;
-    const size_t orow = (size_t)s * p.ncols + gc;
-    __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(p.out + orow * kLat) + d4 * 2;
-    o2[0] = __floats2bfloat162_rn(tot.x * inv, tot.y * inv);
-    o2[1] = __floats2bfloat162_rn(tot.z * inv, tot.w * inv);
-    if (threadIdx.x == 0 && p.lse) p.lse[orow] = (M + log2f(Lt)) * 0.69314718055994531f;
 }
 
 // ---- host-side plans ----
@@ -1484,6 +1670,31 @@ inline Plan plan_of(int S, int R, int H, const int64_t *h_len, int sms, bool inv
 }
 
 inline size_t slot_bytes() { return (size_t)NCOL * kLat * sizeof(float); }
+
+// The most partials any unit of this launch leaves (the combine's form depends on it).
+inline int max_partials(const Params &p, const Plan &pl) {
+    int most = 1;
+    if (pl.mode == MODE_SPLITS) {
+        for (int s = 0; s < p.S; ++s) most = std::max(most, (int)p.st[s].nsplit);
+    } else if (pl.mode == MODE_UNITS) {
+        // consecutive bounds inside one unit
+        int run = 0;
+        for (int i = 1; i < pl.nranges; ++i) {
+            const int64_t x = p.rb[i], xp = p.rb[i - 1];
+            const bool inside = (x & 0xffffffffll) != 0;
+            run = inside ? (((xp >> 32) == (x >> 32) && (xp & 0xffffffffll) != 0) ? run + 1 : 1) : 0;
+            most = std::max(most, run + 1);
+        }
+    } else {
+        for (int s = 0; s < p.S; ++s) {
+            const int64_t *b = p.rb, *e = p.rb + pl.nranges + 1;
+            const int c0 = (int)(std::upper_bound(b, e, p.st[s].toff) - b) - 1;
+            const int c1 = (int)(std::upper_bound(b, e, p.st[s].toff + p.st[s].nt - 1) - b) - 1;
+            most = std::max(most, c1 - c0 + 1);
+        }
+    }
+    return most;
+}
 // On a default pool the partials are at most two slots a CTA; the no-allocation entry point's
 // fixed scratch must hold that many, with the (m, l) pairs after them rounded to 256 bytes.
 static_assert(2 * (size_t)MAX_CTAS * NCOL * kLat * sizeof(float) +
@@ -1755,15 +1966,21 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
                    : pl.mode == MODE_UNITS  ? mla_attend_kernel<MODE_UNITS>
                    : pl.mode == MODE_SPARSE ? mla_attend_kernel<MODE_SPARSE>
                                             : mla_attend_kernel<MODE_SPLITS>;
-        const cudaError_t e = launch_pdl(kern, dim3(pl.nctas), dim3(f8 ? THREADS_F8 : THREADS), SMEM_TOTAL, st, p);
+        const int threads = f8 || pl.mode == MODE_SPARSE ? THREADS + 128 : THREADS;
+        const cudaError_t e = launch_pdl(kern, dim3(pl.nctas), dim3(threads), SMEM_TOTAL, st, p);
         launch_counter()++;
         if (e != cudaSuccess) return TF_E_CUDA;
     }
     if (slots) {
         ProfScope prof(pool, kProfCombine, st);
         // UNITS: only the units a range bound cuts
-        const dim3 grid = pl.mode == MODE_UNITS ? dim3(NCOL, pl.nranges - 1) : dim3(R * H, S);
-        const cudaError_t e = launch_pdl(mla_combine_kernel, grid, dim3(COMBINE_THREADS), 0, st, p);
+        // UNITS: blockIdx.y runs over the range bounds (only cut units merge)
+        const bool wide = max_partials(p, pl) > COMBINE_NARROW_MAX;
+        const int groups = (R * H + NCOL - 1) / NCOL;
+        const int gx = wide ? NCOL : NCOL / COMBINE_COLS;
+        const dim3 grid = pl.mode == MODE_UNITS ? dim3(gx, pl.nranges - 1) : dim3(gx, groups, S);
+        const cudaError_t e = launch_pdl(wide ? mla_combine_kernel<true> : mla_combine_kernel<false>, grid,
+                                         dim3(wide ? COMBINE_THREADS : COMBINE_COLS * 32), 0, st, p);
         launch_counter()++;
         if (e != cudaSuccess) return TF_E_CUDA;
     }

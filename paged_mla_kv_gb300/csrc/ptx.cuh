@@ -172,6 +172,20 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                  : "memory");
 }
 
+// 16 bytes global -> shared through L2 only (cp.async), with an L2 eviction policy; tracked by
+// the issuing thread's cp.async state.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "l"(policy)
+                 : "memory");
+}
+// The barrier gets one arrival from this thread once every cp.async it issued before has
+// completed; .noinc: the barrier's expected count already includes that arrival.
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // A contiguous shared -> global copy (16-byte aligned, a multiple of 16 bytes) in the issuing
 // thread's bulk group; bulk_s2g_wait returns once every such copy of the thread is complete
 // (its writes performed), so the kernel's successors see them.
