@@ -896,25 +896,35 @@ __global__ void __launch_bounds__(kernel_threads<MODE, FP8>(), 1) mla_attend_ker
                     stop = true;
                     break;
                 }
+                // each row's latent and rope addresses, from the lane that looked it up: shuffled
+                // once a tile, so a copy costs few instructions (this loop is issue-bound)
+                const char *lat_src = base + (size_t)ri * (kLat * 2);
+                const char *rope_src = base + kLatBlockBytes + (size_t)ri * (kRope * 2);
+                const char *lat[16];
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr)
+                    lat[rr] = reinterpret_cast<const char *>(__shfl_sync(0xffffffffu, (unsigned long long)lat_src, rr));
+                // this lane's 16-byte chunk c = lane mod 8 of box lane / 8 (+ 4 in the second half):
+                // row tr = 16 lw + rr sits at tr * 128 + 16 (c ^ (tr mod 8)), and tr mod 8 = rr mod 8
+                const int c8 = lane & 7;
                 // first half: the rope box (four rows an instruction) and latent values 0-255
                 if (!slot_free(-1) || !slot_free(0) || !slot_free(1)) {
                     stop = true;
                     break;
                 }
-#pragma unroll 4
-                for (int rr = 0; rr < 16; ++rr) {
-                    const char *b = reinterpret_cast<const char *>(__shfl_sync(0xffffffffu, (unsigned long long)base, rr));
-                    const int i = __shfl_sync(0xffffffffu, ri, rr), tr = 16 * lw + rr;
-                    ptx::cp_async16(smem + box_off(gt, lane >> 3) + tr * 128 + (((lane & 7) ^ (tr & 7)) << 4),
-                                    b + (size_t)i * (kLat * 2) + lane * 16, pol_kv);
-                }
+                {
+                    uint8_t *dst = smem + box_off(gt, lane >> 3) + 16 * lw * 128;
 #pragma unroll
-                for (int g4 = 0; g4 < 4; ++g4) {
-                    const int rr = 4 * g4 + (lane >> 3);
-                    const char *b = reinterpret_cast<const char *>(__shfl_sync(0xffffffffu, (unsigned long long)base, rr));
-                    const int i = __shfl_sync(0xffffffffu, ri, rr), tr = 16 * lw + rr;
-                    ptx::cp_async16(smem + box_off(gt, 8) + tr * 128 + (((lane & 7) ^ (tr & 7)) << 4),
-                                    b + kLatBlockBytes + (size_t)i * (kRope * 2) + (lane & 7) * 16, pol_kv);
+                    for (int rr = 0; rr < 16; ++rr)
+                        ptx::cp_async16(dst + rr * 128 + ((c8 ^ (rr & 7)) << 4), lat[rr] + lane * 16, pol_kv);
+                    uint8_t *rdst = smem + box_off(gt, 8) + 16 * lw * 128;
+#pragma unroll
+                    for (int g4 = 0; g4 < 4; ++g4) {
+                        const int rr = 4 * g4 + (lane >> 3);
+                        const char *src = reinterpret_cast<const char *>(
+                            __shfl_sync(0xffffffffu, (unsigned long long)rope_src, rr));
+                        ptx::cp_async16(rdst + rr * 128 + ((c8 ^ (rr & 7)) << 4), src + c8 * 16, pol_kv);
+                    }
                 }
                 ptx::cp_async_arrive(&c.tile_half[rs]);
                 // second half: latent values 256-511 (pairs 2-3)
@@ -922,12 +932,11 @@ __global__ void __launch_bounds__(kernel_threads<MODE, FP8>(), 1) mla_attend_ker
                     stop = true;
                     break;
                 }
-#pragma unroll 4
-                for (int rr = 0; rr < 16; ++rr) {
-                    const char *b = reinterpret_cast<const char *>(__shfl_sync(0xffffffffu, (unsigned long long)base, rr));
-                    const int i = __shfl_sync(0xffffffffu, ri, rr), tr = 16 * lw + rr;
-                    ptx::cp_async16(smem + box_off(gt, 4 + (lane >> 3)) + tr * 128 + (((lane & 7) ^ (tr & 7)) << 4),
-                                    b + (size_t)i * (kLat * 2) + 512 + lane * 16, pol_kv);
+                {
+                    uint8_t *dst = smem + box_off(gt, 4 + (lane >> 3)) + 16 * lw * 128;
+#pragma unroll
+                    for (int rr = 0; rr < 16; ++rr)
+                        ptx::cp_async16(dst + rr * 128 + ((c8 ^ (rr & 7)) << 4), lat[rr] + 512 + lane * 16, pol_kv);
                 }
                 ptx::cp_async_arrive(&c.tile_full[rs]);
             }
