@@ -12,7 +12,10 @@
 // (RANGES, UNITS, SPLITS, SPARSE) is described at the Params below.  Keys stream through
 // 64-row tiles: 9 boxes of [64 keys x 64 values] bf16 (8 latent + 1 rope), loaded by TMA with
 // 128-byte swizzle from the tile's pool page into a ring of 10 latent box-pair slots and 3 rope
-// slots (2.5 tiles in flight).  The queries' latent values 0-255 sit in TMEM as the A operand
+// slots (2.5 tiles in flight).  A tile lands in two halves (rope box and pairs 0-1; pairs 2-3),
+// and QK^T starts on the first while the second, whose slots free last, is still on its way.
+// Listed rows on BF16 pages are copied row by row with cp.async by four loader warps into the
+// same swizzled boxes.  The queries' latent values 0-255 sit in TMEM as the A operand
 // of QK^T; only their last four latent boxes and the rope box stay in shared memory, which is
 // what pays for the deeper ring.  The same shared-memory tile feeds both contractions on the
 // 5th-generation tensor cores:
@@ -28,11 +31,11 @@
 // several segments writes fp32 partials (unnormalised O, running maximum, sum) that a
 // combine kernel merges in key order.
 //
-// Warp roles (352 threads; 480 on FP8 pages): warps 0-3 rescale O^T when asked and run the
-// epilogue (one TMEM lane quadrant each); warps 4-7 softmax, and at each segment start write
-// the segment's queries into TMEM; warp 8 the TMA producer; warp 9 the TMEM allocation and the
-// QK^T issuer; warp 10 the PV issuer; on FP8 pages warps 11-14 expand each tile's codes to bf16
-// in shared memory.  The MMA issuers walk their issue loops as whole warps with one elected lane
+// Warp roles (352 threads; 480 on FP8 pages and for listed rows): warps 0-3 rescale O^T when
+// asked and run the epilogue (one TMEM lane quadrant each); warps 4-7 softmax, and at each
+// segment start write the segment's queries into TMEM; warp 8 the TMA producer; warp 9 the TMEM
+// allocation and the QK^T issuer; warp 10 the PV issuer; on FP8 pages warps 11-14 expand each
+// tile's codes to bf16 in shared memory, for listed rows on BF16 pages they copy the rows.  The MMA issuers walk their issue loops as whole warps with one elected lane
 // issuing, in rolled loops: on this GPU both kept MMA issue markedly faster than a lone lane
 // running unrolled issue code.
 #include <cuda_bf16.h>
@@ -131,9 +134,9 @@ __device__ __forceinline__ int scales_off(int gt) { return SMEM_PAIR + pair_slot
 
 struct Ctrl {
     uint64_t f8_full[NROPE];           // FP8: the tile's codes, scales and rope box landed
-    uint64_t tile_full[NROPE];         // every box of the tile landed (FP8: expanded); by rope slot
-    uint64_t tile_half[NROPE];         // prefill: the rope box and latent pairs 0-1 landed (tile_full:
-                                       // pairs 2-3)
+    uint64_t tile_half[NROPE];         // the tile's rope box and latent pairs 0-1 landed (FP8:
+                                       // expanded); by rope slot
+    uint64_t tile_full[NROPE];         // its latent pairs 2-3 landed (FP8: expanded)
     uint64_t rope_empty[NROPE];        // PV of the slot's tile is done (its rope box and P are free)
     uint64_t pair_empty[NPAIR];        // PV M-tile of the pair is done
     uint64_t p_full[NROPE];            // P of the slot's tile written and O^T rescaled for it
@@ -384,8 +387,8 @@ __global__ void __launch_bounds__(kernel_threads<MODE, FP8>(), 1) mla_attend_ker
         for (int i = 0; i < NROPE; ++i) {
             // BF16: the TMA warp's one arrival with the tile's bytes; FP8: one arrival a pair the
             // expansion warps finish
-            ptx::mbar_init(&c.tile_full[i], FP8 ? 4 : CP_ROWS ? LOAD_THREADS : 1);
-            ptx::mbar_init(&c.tile_half[i], CP_ROWS ? LOAD_THREADS : 1);
+            ptx::mbar_init(&c.tile_full[i], FP8 ? 2 : CP_ROWS ? LOAD_THREADS : 1);
+            ptx::mbar_init(&c.tile_half[i], FP8 ? 2 : CP_ROWS ? LOAD_THREADS : 1);
             ptx::mbar_init(&c.rope_empty[i], 1);
             ptx::mbar_init(&c.p_full[i], 5);       // four softmax warps and the rescale warps
             ptx::mbar_init(&c.corr_req[i], 4);
@@ -421,10 +424,9 @@ __global__ void __launch_bounds__(kernel_threads<MODE, FP8>(), 1) mla_attend_ker
     // on-chip setup done: from here on global memory (pool, tables, queries, outputs)
     ptx::griddep_wait();
 
-    // Prefill (UNITS, BF16) lands a tile in two halves: QK^T starts on the rope box and latent
-    // pairs 0-1 while pairs 2-3, whose slots the PV of the tile two back releases last, are
-    // still on their way.  Decode keeps one barrier a tile (a wait costs about four MMAs).
-    constexpr bool HALF = !FP8;
+    // A tile lands in two halves: QK^T starts on the rope box and latent pairs 0-1 while pairs
+    // 2-3, whose slots the PV of the tile two back releases last, are still on their way (FP8:
+    // still being expanded).  Two waits a tile, not one a pair: a wait costs about four MMAs.
     if (warp == 8) {
         // ================= TMA producer =================
         // Slot uses armed last (-1: never), so that no copy is left writing shared memory at exit.
@@ -432,20 +434,15 @@ __global__ void __launch_bounds__(kernel_threads<MODE, FP8>(), 1) mla_attend_ker
         for (int i = 0; i < NROPE; ++i) armed_tile[i] = armed_f8[i] = -1;
         int q_armed = -1;   // last segment whose queries were loaded
         bool stop = false;
-        // wait until the slot's previous use is released (lane 0), then arm it for `bytes`
         // wait until the tile's rope slot is released by PV of its previous tile (lane 0); BF16
-        // pages then arm the tile's landing barrier for all nine boxes
+        // pages then arm the tile's two landing barriers (rope box and pairs 0-1; pairs 2-3)
         auto take_rope = [&](int gt) -> bool {
             const int rs = rope_slot(gt);
             const uint32_t u = rope_use(gt);
             if (u > 0 && !ptx::mbar_wait(&c.rope_empty[rs], (u - 1) & 1, abort, errp, 1)) return false;
             if (!FP8) {
-                if (HALF) {
-                    ptx::mbar_arrive_expect_tx(&c.tile_half[rs], 5 * BOX_BYTES);
-                    ptx::mbar_arrive_expect_tx(&c.tile_full[rs], 4 * BOX_BYTES);
-                } else {
-                    ptx::mbar_arrive_expect_tx(&c.tile_full[rs], NBOX * BOX_BYTES);
-                }
+                ptx::mbar_arrive_expect_tx(&c.tile_half[rs], 5 * BOX_BYTES);
+                ptx::mbar_arrive_expect_tx(&c.tile_full[rs], 4 * BOX_BYTES);
                 armed_tile[rs] = (int)u;
             }
             return true;
@@ -611,7 +608,7 @@ __global__ void __launch_bounds__(kernel_threads<MODE, FP8>(), 1) mla_attend_ker
                             break;
                         }
                         if (lane < 16) {
-                            uint64_t *bar = HALF && j < 2 ? &c.tile_half[rs] : &c.tile_full[rs];
+                            uint64_t *bar = j < 2 ? &c.tile_half[rs] : &c.tile_full[rs];
                             if (j < 0) {
                                 ptx::tma_gather4(smem + box_off(gt, 8) + lane * 512, &p.tm_rope_rows, bar, 0, ro0, ro1,
                                                  ro2, ro3, pol_kv);
@@ -687,15 +684,14 @@ __global__ void __launch_bounds__(kernel_threads<MODE, FP8>(), 1) mla_attend_ker
                             stop = true;
                             break;
                         }
-                        tma_load_4d(smem + box_off(gt, 8), &p.tm_rope, HALF ? &c.tile_half[rs] : &c.tile_full[rs], 0, row,
-                                    page, cache, pol_kv);
+                        tma_load_4d(smem + box_off(gt, 8), &p.tm_rope, &c.tile_half[rs], 0, row, page, cache, pol_kv);
 #pragma unroll 1
                         for (int j = 0; j < 4; ++j) {
                             if (!free_pair(gt, j)) {
                                 stop = true;
                                 break;
                             }
-                            uint64_t *bar = HALF && j < 2 ? &c.tile_half[rs] : &c.tile_full[rs];
+                            uint64_t *bar = j < 2 ? &c.tile_half[rs] : &c.tile_full[rs];
                             for (int h = 0; h < 2; ++h)
                                 tma_load_4d(smem + box_off(gt, 2 * j + h), &p.tm_lat, bar, (2 * j + h) * 64, row, page,
                                             cache, pol_kv);
@@ -710,7 +706,7 @@ __global__ void __launch_bounds__(kernel_threads<MODE, FP8>(), 1) mla_attend_ker
             if (q_armed >= 0) ptx::mbar_wait(&c.q_full, q_armed & 1, abort, errp, 10, 1ll << 28);
             for (int i = 0; i < NROPE; ++i) {
                 if (armed_tile[i] >= 0) {
-                    if (HALF) ptx::mbar_wait(&c.tile_half[i], armed_tile[i] & 1, abort, errp, 11, 1ll << 28);
+                    ptx::mbar_wait(&c.tile_half[i], armed_tile[i] & 1, abort, errp, 11, 1ll << 28);
                     ptx::mbar_wait(&c.tile_full[i], armed_tile[i] & 1, abort, errp, 11, 1ll << 28);
                 }
                 if (armed_f8[i] >= 0) ptx::mbar_wait(&c.f8_full[i], armed_f8[i] & 1, abort, errp, 18, 1ll << 28);
@@ -765,13 +761,12 @@ __global__ void __launch_bounds__(kernel_threads<MODE, FP8>(), 1) mla_attend_ker
                     if ((b & 1) && ++ps == NPAIR) ps = 0;
                 }
             };
-            // the tile (prefill: its first half) has landed: one barrier, as a wait costs about as
-            // long as four MMAs, so the MMAs go out in long runs
-            if (!ptx::mbar_wait_warp(HALF ? &c.tile_half[rs] : &c.tile_full[rs], rope_use(tq) & 1, abort, errp, 3))
-                return false;
+            // the tile's first half has landed (a wait costs about as long as four MMAs, so the
+            // MMAs go out in runs of 20 and 16)
+            if (!ptx::mbar_wait_warp(&c.tile_half[rs], rope_use(tq) & 1, abort, errp, 3)) return false;
             // rows copied by cp.async (generic proxy) become visible to the tensor cores' reads
             if (CP_ROWS) ptx::fence_proxy_async_smem();
-            zero_tail(0, HALF ? 4 : 8, true);
+            zero_tail(0, 4, true);
             // order the MMAs after the softmax's TMEM loads of S (s_free) and the queries' TMEM
             // stores (q_tmem_full, waited before a segment's first tile); the key boxes come by
             // TMA and need no such fence
@@ -779,15 +774,12 @@ __global__ void __launch_bounds__(kernel_threads<MODE, FP8>(), 1) mla_attend_ker
             // the rope box (queries' rope box in shared memory) starts S, then the latent pairs
             ptx::mma4_bf16_ss_warp(d, q_desc0 + (uint64_t)(((Q_SMEM_BOXES - 1) * QBOX_BYTES) >> 4),
                                    kv_desc0 + (uint64_t)((SMEM_ROPE + rs * BOX_BYTES) >> 4), IDESC_QK, 1u);
-            if (HALF) {
-                latent(0, 4);
-                if (!ptx::mbar_wait_warp(&c.tile_full[rs], rope_use(tq) & 1, abort, errp, 3)) return false;
-                if (CP_ROWS) ptx::fence_proxy_async_smem();
-                zero_tail(4, 8, false);
-                latent(4, 8);
-            } else {
-                latent(0, 8);
-            }
+            latent(0, 4);
+            // the second half
+            if (!ptx::mbar_wait_warp(&c.tile_full[rs], rope_use(tq) & 1, abort, errp, 3)) return false;
+            if (CP_ROWS) ptx::fence_proxy_async_smem();
+            zero_tail(4, 8, false);
+            latent(4, 8);
             ptx::mma_commit_warp(&c.s_full[tq & 1]);
             if (tl == q.nt - 1) ptx::mma_commit_warp(&c.q_free);
             return true;
@@ -948,7 +940,8 @@ __global__ void __launch_bounds__(kernel_threads<MODE, FP8>(), 1) mla_attend_ker
         // ================= FP8 expansion (warps 11-14): half a tile row a thread =================
         // Box b's 64 codes of row r become bf16(code * scale_r), written 128B-swizzled into BF16
         // box b (16-byte chunk j of the row at j ^ (r & 7)); thread (r, hf) does codes 32hf..+31.
-        // Each finished pair is one arrival on its full barrier, after a proxy fence.
+        // Each finished pair is one arrival on the tile's half barrier (pairs 0-1) or full barrier
+        // (pairs 2-3), after a proxy fence.
         const int ft = (int)threadIdx.x - THREADS;
         const int r = ft >> 1, hf = ft & 1;
         bool ok = true;
@@ -1007,7 +1000,7 @@ __global__ void __launch_bounds__(kernel_threads<MODE, FP8>(), 1) mla_attend_ker
                     }
                     ptx::fence_proxy_async_smem();
                     ptx::named_bar(2, F8_THREADS);
-                    if (ft == 0) ptx::mbar_arrive(&c.tile_full[rs]);
+                    if (ft == 0) ptx::mbar_arrive(b0 < 4 ? &c.tile_half[rs] : &c.tile_full[rs]);
                 }
             }
         }
