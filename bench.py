@@ -594,15 +594,38 @@ def measure(name, steps, warmup, with_e2e, pg, world, peaks, peak_src):
     # end to end through the C-ABI with host buffers: queries and new rows in, outputs out
     e2e = None
     if not not with_e2e:
-        hq = [q.cpu().pin_memory() for q in qs]
-        hrows = [(a.cpu().pin_memory(), b.cpu().pin_memory()) for a, b in cur]
+        # one pinned host buffer and one device buffer a direction, so a step is one copy each way:
+        # in = every cache's queries, then its new rows' latent and rope parts; out = the outputs,
+        # then the lse (each part starts on a 256-byte boundary)
+        def layout(ts):
+            offs, n = [], 0
+            for t in ts:
+                offs.append(n)
+                n += -(-t.numel() * t.element_size() // 256) * 256
+            return offs, n
+
+        def views(buf, ts, offs):
+            return [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(ts, offs)]
+
+        ins = [t for c in range(w.num_caches) for t in (qs[c], cur[c][0], cur[c][1])]
+        in_offs, in_n = layout(ins)
+        outs = [out, lse]
+        out_offs, out_n = layout(outs)
         nb = 2   # double buffers: step i+1's inputs and step i-1's outputs move while step i runs
-        dq = [[torch.empty_like(q) for q in qs] for _ in range(nb)]
-        drows = [[(torch.empty_like(a), torch.empty_like(b)) for a, b in cur] for _ in range(nb)]
-        dout = [torch.empty_like(out) for _ in range(nb)]
-        dlse = [torch.empty_like(lse) for _ in range(nb)]
-        hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(nb)]
-        hlse = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(nb)]
+        hin = torch.empty(in_n, dtype=torch.uint8).pin_memory()
+        for t, v in zip(ins, views(hin, ins, in_offs)):
+            v.copy_(t.cpu())
+        din = [torch.empty(in_n, dtype=torch.uint8, device="cuda") for _ in range(nb)]
+        dout_b = [torch.empty(out_n, dtype=torch.uint8, device="cuda") for _ in range(nb)]
+        hout = [torch.empty(out_n, dtype=torch.uint8).pin_memory() for _ in range(nb)]
+        dq, drows, dout, dlse = [], [], [], []
+        for b_ in range(nb):
+            v = views(din[b_], ins, in_offs)
+            dq.append([v[3 * c] for c in range(w.num_caches)])
+            drows.append([(v[3 * c + 1], v[3 * c + 2]) for c in range(w.num_caches)])
+            o = views(dout_b[b_], outs, out_offs)
+            dout.append(o[0])
+            dlse.append(o[1])
         main = torch.cuda.current_stream()
         cs = torch.cuda.Stream()
         in_ready = [torch.cuda.Event() for _ in range(nb)]
@@ -614,13 +637,9 @@ def measure(name, steps, warmup, with_e2e, pg, world, peaks, peak_src):
 
         def h2d(i):
             b_ = i % nb
-            with torch.cuda.stream(cs):
-                cs.wait_event(done[b_])        # step i-2 has consumed this buffer
-                for c in range(w.num_caches):
-                    dq[b_][c].copy_(hq[c], non_blocking=True)
-                    drows[b_][c][0].copy_(hrows[c][0], non_blocking=True)
-                    drows[b_][c][1].copy_(hrows[c][1], non_blocking=True)
-                in_ready[b_].record(cs)
+            cs.wait_event(done[b_])        # step i-2 has consumed this buffer
+            din[b_].copy_(hin, non_blocking=True)
+            in_ready[b_].record(cs)
 
         def compute(i):
             b_ = i % nb
@@ -631,19 +650,19 @@ def measure(name, steps, warmup, with_e2e, pg, world, peaks, peak_src):
 
         def d2h(i):
             b_ = i % nb
-            with torch.cuda.stream(cs):
-                cs.wait_event(done[b_])
-                hout[b_].copy_(dout[b_], non_blocking=True)
-                hlse[b_].copy_(dlse[b_], non_blocking=True)
-                out_read[b_].record(cs)
+            cs.wait_event(done[b_])
+            hout[b_].copy_(dout_b[b_], non_blocking=True)
+            out_read[b_].record(cs)
 
         def run_e2e(n):
-            h2d(0)
+            with torch.cuda.stream(cs):
+                h2d(0)
             for i in range(n):
-                if i + 1 < n:
-                    h2d(i + 1)
                 compute(i)
-                d2h(i)
+                with torch.cuda.stream(cs):
+                    if i + 1 < n:
+                        h2d(i + 1)
+                    d2h(i)
             main.wait_event(out_read[(n - 1) % nb])
 
         run_e2e(max(2, warmup))
@@ -667,8 +686,7 @@ def measure(name, steps, warmup, with_e2e, pg, world, peaks, peak_src):
                 e2[i][1].record(main)
             barrier()
             e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2) / steps, pg, "cuda")
-        h2d = sum(q.numel() * 2 for q in qs) + sum(a.numel() * 2 + b.numel() * 2 for a, b in cur)
-        d2h = out.numel() * 2 + lse.numel() * 4
+        h2d, d2h = in_n, out_n   # the bytes each step's two copies move (parts padded to 256 bytes)
         ev_ = world * (units["flops"] / 1e12 if prefill else units["bytes"] / 1e9) / (e_ms / 1e3)
         e2e = {"value": ev_, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
 

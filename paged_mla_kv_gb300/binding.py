@@ -114,22 +114,39 @@ def _check(rc: int, what: str) -> None:
         raise TFError(rc, what)
 
 
+# Argument marshalling is on every call's path, so pointers travel as plain ints (ctypes turns
+# an int into a void * for a c_void_p argument) and arrays already in the right form are used
+# as they are.
+
 def _ptr(t):
     if t is None:
         return None
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
+
+
+_current_stream = None
 
 
 def _stream(stream):
+    """The raw CUDA stream: `stream` as given, else torch's current stream on the current device."""
     if stream is not None:
-        return ctypes.c_void_p(int(stream))
-    import torch
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return int(stream)
+    global _current_stream
+    if _current_stream is None:
+        import torch
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        get_dev = getattr(torch._C, "_cuda_getDevice", None)
+        if raw is not None and get_dev is not None:
+            _current_stream = lambda: raw(get_dev())
+        else:
+            _current_stream = lambda: torch.cuda.current_stream().cuda_stream
+    return _current_stream()
 
 
 def _i64(a):
-    a = np.ascontiguousarray(np.asarray(a, dtype=np.int64))
-    return a, a.ctypes.data_as(ctypes.c_void_p)
+    if not (isinstance(a, np.ndarray) and a.dtype == np.int64 and a.flags.c_contiguous):
+        a = np.ascontiguousarray(a, dtype=np.int64)
+    return a, a.ctypes.data
 
 
 def make_desc(num_caches: int, num_pages: int, poison: bool = False, seed: int = 0,
@@ -277,8 +294,9 @@ def tf_paged_mla_attend_static(pool: KVPool, cache: int, pt, max_pages: int, len
 
 
 def _i32(a):
-    a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
-    return a, a.ctypes.data_as(ctypes.c_void_p)
+    if not (isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous):
+        a = np.ascontiguousarray(a, dtype=np.int32)
+    return a, a.ctypes.data
 
 
 def tf_paged_mla_sparse_workspace_bytes(pool, S: int, H: int, nidx) -> int:
