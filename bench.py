@@ -76,18 +76,15 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> floa
 # kernel, from the ncu captures summarised in profiles/, keyed by the first 16 hex digits of
 # the SHA-256 of the kernel's source the capture was taken on: once the kernel changes, the
 # counters no longer describe it and "traffic" is reported null until it is re-captured.
-# Attention captured on source 94c4ab2dc8479ab9 (`--metrics dram__bytes_read.sum,dram__bytes_write.sum,
-# gpu__time_duration.sum`; the FP8 decode launch under `--set full`); 3212b017dcca9adb differs from
-# it in host code only (the cubins built without line info hash the same).
 NCU_TRAFFIC = {
-    # attention on source 3fb36de603d76239, decode batch: `--metrics dram__bytes_read.sum,
+    # attention on source 63bb32362694e346, one launch each: `--metrics dram__bytes_read.sum,
     # dram__bytes_write.sum,gpu__time_duration.sum --cache-control none` (L2 as the back-to-back
-    # steps leave it); profiles/mla_attend_decode_batch.md
-    "3fb36de603d76239": {"decode_batch": 360_180_736 + 1_144_320},
-    "3212b017dcca9adb": {"decode_batch": 374_700_544 + 3_504_128,
-                         "fp8_decode": 207_994_112 + 4_065_024,
-                         "prefill_100k": 1_845_974_272 + 135_486_464,
-                         "sparse_fp8_decode": 103_608_832 + 3_570_432},
+    # steps leave it) for the decode batch, the long window and listed rows; the prefill chunk from
+    # its `--section SpeedOfLight` capture (ncu's default cache flush); profiles/mla_attend_*.md
+    "63bb32362694e346": {"decode_batch": 360_656_128 + 1_842_432,
+                         "long_window": 1_210_498_304 + 643_328,
+                         "sparse_decode": 155_387_648 + 22_609_152,
+                         "prefill_100k": 20_745_148_672 + 162_108_160},
     # top-k: both launches of one call (first level 811.1 + 8.6 MB, merge 58.8 + 0.2 MB), taken
     # on source 4e5c0b41cdefdfb7; 689a485f4717fede differs from it in comments and host-side argument
     # checks only (the cubins built without line info hash the same)
