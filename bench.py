@@ -80,11 +80,13 @@ NCU_TRAFFIC = {
     # attention on source 63bb32362694e346, one launch each: `--metrics dram__bytes_read.sum,
     # dram__bytes_write.sum,gpu__time_duration.sum --cache-control none` (L2 as the back-to-back
     # steps leave it) for the decode batch, the long window and listed rows; the prefill chunk from
-    # its `--section SpeedOfLight` capture (ncu's default cache flush); profiles/mla_attend_*.md
+    # its `--section SpeedOfLight` capture (ncu's default cache flush); FP8 pages likewise with
+    # `--cache-control none`; profiles/mla_attend_*.md
     "63bb32362694e346": {"decode_batch": 360_656_128 + 1_842_432,
                          "long_window": 1_210_498_304 + 643_328,
                          "sparse_decode": 155_387_648 + 22_609_152,
-                         "prefill_100k": 20_745_148_672 + 162_108_160},
+                         "prefill_100k": 20_745_148_672 + 162_108_160,
+                         "fp8_decode": 214_276_352 + 15_531_776},
     # top-k: both launches of one call (first level 811.1 + 8.6 MB, merge 58.8 + 0.2 MB), taken
     # on source 4e5c0b41cdefdfb7; 689a485f4717fede differs from it in comments and host-side argument
     # checks only (the cubins built without line info hash the same)
