@@ -1523,7 +1523,14 @@ inline Split split_of(int64_t len, int groups) {
     return sp;
 }
 
-constexpr int64_t SEG_COST = 3;   // a segment start, in key tiles
+constexpr int64_t SEG_COST = 3;   // a prefill unit's start, in key tiles
+
+// RANGES: what a segment start (a query reload, an extra epilogue, the pipeline's refill) weighs
+// in key tiles when the ranges are cut, measured on this GPU by sweeping the weight: listed rows
+// ran best at 3 (0.476 of HBM against 0.435 at 9), one column group at 5 (decode batch 0.812
+// against 0.799 at 3 and 7), two column groups at 12 (the long window 0.560 against 0.526 at 3,
+// its last ranges holding the seven short streams).
+inline int64_t range_seg_cost(bool sparse, int groups) { return sparse ? 3 : groups == 1 ? 5 : 12; }
 
 // UNITS: cut the units' tiles (stream-major, each unit as many tiles as its last column
 // sees) into at most `sms` ranges, writing their bounds b[0..n] as unit_pos values and
@@ -1588,7 +1595,8 @@ inline int plan_unit_ranges(int S, int R, int H, int groups, const int64_t *h_le
     return n;
 }
 
-inline Plan plan_of(int S, int R, int H, const int64_t *h_len, int sms, bool invariant, int64_t *rb = nullptr) {
+inline Plan plan_of(int S, int R, int H, const int64_t *h_len, int sms, bool invariant, int64_t *rb = nullptr,
+                    bool sparse = false) {
     Plan pl;
     // R * H itself can pass INT32_MAX; callers refuse S * R * H above 2^30, so groups fits an int
     const int groups = (int)(((int64_t)R * H + NCOL - 1) / NCOL);
@@ -1626,12 +1634,13 @@ inline Plan plan_of(int S, int R, int H, const int64_t *h_len, int sms, bool inv
     if (pl.nranges < 1) pl.nranges = 1;
     pl.nctas = pl.nranges * pl.rep;
     // Range boundaries.  A range that starts a second stream pays for a query reload
-    // and an extra epilogue, about SEG_COST tiles: a stream's first tile is weighted
-    // 1 + SEG_COST and the ranges cut the weighted sequence into equal parts.  A cut
+    // and an extra epilogue, about `seg` tiles: a stream's first tile is weighted
+    // 1 + seg and the ranges cut the weighted sequence into equal parts.  A cut
     // that lands inside a stream's extra weight moves to the stream's start.
     int64_t rb_local[MAX_CTAS + 1];
     int64_t *b = rb ? rb : rb_local;
-    const int64_t U = pl.total + SEG_COST * (int64_t)(S - 1);
+    const int64_t seg = range_seg_cost(sparse, groups);
+    const int64_t U = pl.total + seg * (int64_t)(S - 1);
     b[0] = 0;
     b[pl.nranges] = pl.total;
     int s = 0;
@@ -1641,11 +1650,11 @@ inline Plan plan_of(int S, int R, int H, const int64_t *h_len, int sms, bool inv
         // advance to the last stream whose weighted start is <= tau
         while (s + 1 < S) {
             const int64_t next = toff + (h_len[s] + BK - 1) / BK;
-            if (next + SEG_COST * (int64_t)(s + 1) > tau) break;
+            if (next + seg * (int64_t)(s + 1) > tau) break;
             toff = next;
             ++s;
         }
-        const int64_t u0 = toff + SEG_COST * (int64_t)s;   // weighted start of stream s
+        const int64_t u0 = toff + seg * (int64_t)s;   // weighted start of stream s
         int64_t x = toff + (tau > u0 ? tau - u0 : 0);
         const int64_t end = toff + (h_len[s] + BK - 1) / BK;
         if (x > end) x = end;
@@ -1717,8 +1726,8 @@ static int device_sms() {
     return n < attn::MAX_CTAS ? n : attn::MAX_CTAS;
 }
 
-size_t attend_workspace_bytes(bool invariant, int S, int R, int H, const int64_t *h_len) {
-    const attn::Plan pl = attn::plan_of(S, R, H, h_len, device_sms(), invariant);
+size_t attend_workspace_bytes(bool invariant, int S, int R, int H, const int64_t *h_len, bool sparse) {
+    const attn::Plan pl = attn::plan_of(S, R, H, h_len, device_sms(), invariant, nullptr, sparse);
     if (pl.slots == 0) return 0;
     const size_t slots = pl.slots;
     const size_t o = slots * attn::slot_bytes();
@@ -1918,7 +1927,7 @@ int launch_attend(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_pages
         keys = nkeys;
     }
     const bool invariant = !sparse && (pool->desc.flags & TF_POOL_BATCH_INVARIANT) != 0;
-    Plan pl = plan_of(S, R, H, keys, device_sms(), invariant, p.rb);
+    Plan pl = plan_of(S, R, H, keys, device_sms(), invariant, p.rb, sparse);
     if (sparse) pl.mode = MODE_SPARSE;   // ranges over the lists (few column groups: R = 1, H <= 128)
     p.mode = pl.mode;
     p.total = pl.total;

@@ -286,7 +286,7 @@ extern "C" size_t tf_paged_mla_sparse_workspace_bytes(const tf_kvpool *p, int32_
     if (sparse_checks(p, S, H, h_nidx ? 1 << 30 : 1, h_nidx) != TF_OK) return 0;
     int64_t n[TF_MAX_STREAMS];
     for (int s = 0; s < S; ++s) n[s] = h_nidx[s];
-    return attend_workspace_bytes(false, S, 1, H, n);
+    return attend_workspace_bytes(false, S, 1, H, n, true);
 }
 
 extern "C" int tf_paged_mla_attend_sparse(tf_kvpool *p, int32_t cache, const int32_t *d_pt, int32_t max_pages,
@@ -307,7 +307,7 @@ extern "C" int tf_paged_mla_attend_sparse(tf_kvpool *p, int32_t cache, const int
         return TF_E_ARG;
     int64_t n[TF_MAX_STREAMS];
     for (int s = 0; s < S; ++s) n[s] = h_nidx[s];
-    const size_t need = attend_workspace_bytes(false, S, 1, H, n);
+    const size_t need = attend_workspace_bytes(false, S, 1, H, n, true);
     if (need > 0 && (!d_ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(d_ws) & 255u) != 0))
         return d_ws && ws_bytes < need ? TF_E_NOMEM : TF_E_ARG;
     return launch_attend(p, cache, d_pt, max_pages, h_len, S, 1, H, d_q, scale, d_out, d_lse, d_ws, ws_bytes,

@@ -134,7 +134,7 @@ int launch_attend_fp8(tf_kvpool *pool, int cache, const int32_t *d_pt, int max_p
                       int R, int H, const void *d_q, float scale, void *d_out, float *d_lse, void *d_ws,
                       size_t ws_bytes, size_t attend_ws, cudaStream_t st);
 int launch_diag_wait(tf_kvpool *pool, long long limit, cudaStream_t st);
-size_t attend_workspace_bytes(bool invariant, int S, int R, int H, const int64_t *h_len);
+size_t attend_workspace_bytes(bool invariant, int S, int R, int H, const int64_t *h_len, bool sparse = false);
 int attend_plan_info(int S, int R, int H, const int64_t *h_len, int sms, bool invariant, tf_attend_plan *info,
                      int64_t *range_bounds, int64_t *split_keys);
 // d_idx / max_idx / h_nidx: a sparse call (the keys are the listed rows, R = 1), or null.

@@ -360,11 +360,11 @@ def test_headers_compile_as_c_and_the_library_links_from_c(L, tmp_path):
     assert [int(x) for x in got] == want
 
 
-def _weighted_sizes(bounds, lens, seg=3):
-    """Tiles of each range plus `seg` for every stream that starts inside it (a segment start
-    costs a query reload and an extra epilogue, about three tiles)."""
+def _weighted_sizes(bounds, lens, seg):
+    """Tiles of each range plus `seg` for every stream after the first that starts inside it (a
+    segment start costs a query reload, an extra epilogue and the pipeline's refill)."""
     tiles = -(-np.asarray(lens, np.int64) // 64)
-    starts = np.concatenate([[0], np.cumsum(tiles)[:-1]])
+    starts = np.cumsum(tiles)[:-1]
     return [int(bounds[i + 1] - bounds[i]) + seg * int(np.sum((starts >= bounds[i]) & (starts < bounds[i + 1])))
             for i in range(len(bounds) - 1)]
 
@@ -380,8 +380,11 @@ def test_decode_plan_deals_every_tile_once_in_balanced_ranges(L, name):
     assert b[0] == 0 and b[-1] == tiles and np.all(np.diff(b) >= 1)     # every tile in exactly one range
     assert pl["ctas"] == pl["nranges"] * pl["groups"] <= 152
     assert pl["nranges"] == min(-(-tiles // 4), 152 // pl["groups"])     # at least 4 tiles a range
-    wsz = _weighted_sizes(b, w.lens)
-    assert max(wsz) - min(wsz) <= 8, (min(wsz), max(wsz))
+    # the weight the library gives a segment start: 5 tiles with one column group, 12 with more;
+    # a cut inside a stream's start weight moves to the stream's start, so sizes differ by up to it
+    seg = 5 if pl["groups"] == 1 else 12
+    wsz = _weighted_sizes(b, w.lens, seg)
+    assert max(wsz) - min(wsz) <= 8 + seg, (min(wsz), max(wsz))
     assert pl["slots"] in (0, 2 * pl["ctas"])                           # two partial slots a CTA
 
 
