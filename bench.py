@@ -77,16 +77,14 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> floa
 # the SHA-256 of the kernel's source the capture was taken on: once the kernel changes, the
 # counters no longer describe it and "traffic" is reported null until it is re-captured.
 NCU_TRAFFIC = {
-    # attention on source 63bb32362694e346, one launch each: `--metrics dram__bytes_read.sum,
+    # attention on source 7d9fa675422c97da, one launch each: `--metrics dram__bytes_read.sum,
     # dram__bytes_write.sum,gpu__time_duration.sum --cache-control none` (L2 as the back-to-back
-    # steps leave it) for the decode batch, the long window and listed rows; the prefill chunk from
-    # its `--section SpeedOfLight` capture (ncu's default cache flush); FP8 pages likewise with
-    # `--cache-control none`; profiles/mla_attend_*.md
-    "63bb32362694e346": {"decode_batch": 360_656_128 + 1_842_432,
-                         "long_window": 1_210_498_304 + 643_328,
-                         "sparse_decode": 155_387_648 + 22_609_152,
-                         "prefill_100k": 20_745_148_672 + 162_108_160,
-                         "fp8_decode": 214_276_352 + 15_531_776},
+    # steps leave it); the prefill chunk with ncu's default cache flush; profiles/mla_attend_*.md
+    "7d9fa675422c97da": {"decode_batch": 370_056_704 + 2_340_864,
+                         "long_window": 1_207_117_312 + 827_392,
+                         "sparse_decode": 155_352_064 + 22_679_040,
+                         "fp8_decode": 216_005_888 + 17_167_104,
+                         "prefill_100k": 20_034_719_744 + 158_304_512},
     # top-k: both launches of one call (first level 811.1 + 8.6 MB, merge 58.8 + 0.2 MB), taken
     # on source 4e5c0b41cdefdfb7; 689a485f4717fede differs from it in comments and host-side argument
     # checks only (the cubins built without line info hash the same)
