@@ -79,8 +79,10 @@ def whole_job_rate(units_per_rank: float, world: int, slowest_ms: float) -> floa
 NCU_TRAFFIC = {
     # attention on source 7d9fa675422c97da, one launch each: `--metrics dram__bytes_read.sum,
     # dram__bytes_write.sum,gpu__time_duration.sum --cache-control none` (L2 as the back-to-back
-    # steps leave it); the prefill chunk with ncu's default cache flush; profiles/mla_attend_*.md
-    "7d9fa675422c97da": {"decode_batch": 370_056_704 + 2_340_864,
+    # steps leave it); the prefill chunk with ncu's default cache flush; profiles/mla_attend_*.md.
+    # e00360dc80e0534f differs from it only in how many columns a CTA's last cut partial stages (those PV
+    # computed, in 32-column steps): all 64 for every workload below, so the same bytes move.
+    "e00360dc80e0534f": {"decode_batch": 370_056_704 + 2_340_864,
                          "long_window": 1_207_117_312 + 827_392,
                          "sparse_decode": 155_352_064 + 22_679_040,
                          "fp8_decode": 216_005_888 + 17_167_104,

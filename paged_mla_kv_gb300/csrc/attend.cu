@@ -1241,14 +1241,15 @@ __global__ void __launch_bounds__(kernel_threads<MODE, FP8>(), 1) mla_attend_ker
             ptx::tc_fence_after();
             const float *inv_l = c.row_inv_l[si & 1];
             if (q.slot >= 0 && it.last(p)) {
-                // The CTA's last segment, cut: its fp32 partial (128 KB) goes out by one bulk copy
-                // from shared memory, staged in the key ring, which no tile uses any more (the
-                // last PV is done and the TMA warp loads nothing after it).  Every CTA ends with
-                // this write at about the same time; one bulk copy a CTA moves it faster than
-                // 4,096 warp stores.
+                // The CTA's last segment, cut: its fp32 partial (up to 128 KB: the columns PV
+                // computed, in 32-column steps) goes out by one bulk copy from shared memory,
+                // staged in the key ring, which no tile uses any more (the last PV is done and the
+                // TMA warp loads nothing after it).  Every CTA ends with this write at about the
+                // same time; one bulk copy a CTA moves it faster than 4,096 warp stores.
                 float *stage = reinterpret_cast<float *>(smem + SMEM_PAIR);
+                const int nst = (npv + 31) & ~31;
                 for (int jm = 0; jm < 4; ++jm)
-                    for (int h2 = 0; h2 < NCOL; h2 += 32) {
+                    for (int h2 = 0; h2 < nst; h2 += 32) {
                         uint32_t v[32];
                         ptx::tmem_ld32(lane_base + TMEM_O + jm * 64 + h2, v);
                         ptx::tmem_ld_wait();
@@ -1259,7 +1260,7 @@ __global__ void __launch_bounds__(kernel_threads<MODE, FP8>(), 1) mla_attend_ker
                 ptx::fence_proxy_async_smem();
                 ptx::named_bar(1, 128);
                 if (threadIdx.x == 0) {
-                    ptx::bulk_s2g(ws_o + (size_t)q.slot * NCOL * kLat, stage, NCOL * kLat * sizeof(float));
+                    ptx::bulk_s2g(ws_o + (size_t)q.slot * NCOL * kLat, stage, nst * kLat * sizeof(float));
                     ptx::bulk_s2g_wait();
                 }
             } else {

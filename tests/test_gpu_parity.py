@@ -337,6 +337,39 @@ def test_repeated_calls_are_bit_identical():
     no_device_error(res.pool)
 
 
+@pytest.mark.parametrize("name", ["tiny_decode", "decode_batch"])
+def test_step_captured_in_a_cuda_graph_replays_bit_exact(name):
+    # a serving loop may capture its decode step (append, attention and combine) into a CUDA
+    # graph: every call takes its plan from host arrays and launches on the given stream only,
+    # so a replay must give the eager call's bits
+    w = Y.WORKLOADS[name]()
+    res = Resident(w)
+    q, ws, cur = res.q(), res.workspace(), res.current_rows(0)
+    out = torch.empty((w.S, w.R, w.H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.S, w.R, w.H), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+
+    def step():
+        res.append_current(0, *cur)
+        B.tf_paged_mla_attend(res.pool, 0, res.pt, res.max_pages, res.lens, q, w.scale, out, lse, ws)
+
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    compare(w, out, lse)
+    ref, ref_l = bits(out), lse.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for _ in range(3):
+        out.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(out), ref) and torch.equal(lse, ref_l)
+    no_device_error(res.pool)
+
+
 def test_bounded_wait_gives_up_and_the_context_survives():
     # a wait on a barrier that nothing completes must end, record TF_E_TIMEOUT, and leave
     # the context usable for the next call
