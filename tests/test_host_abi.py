@@ -497,3 +497,35 @@ def test_plan_info_refuses_bad_sizes(L):
     assert L.tf_paged_mla_plan_info(2, 1, 16, lp, 0, 0, None, None, None) == B.TF_E_ARG
     assert L.tf_paged_mla_plan_info(2, 101, 16, lp, 0, 0, ctypes.byref(info), None, None) == B.TF_E_RANGE
     assert L.tf_paged_mla_plan_info(2, 1, 16, lp, 0, 0, ctypes.byref(info), None, None) == B.TF_OK
+
+
+def test_plans_of_random_shapes_keep_their_invariants(L):
+    """Random batches in both range modes: the bounds cover the numbering exactly once in
+    non-empty ranges, there are at most as many ranges as SMs allow, and the plan has partial
+    slots exactly when a bound cuts a unit (host arithmetic only)."""
+    rng = np.random.default_rng(11)
+    for _ in range(300):
+        S = int(rng.integers(1, 40))
+        sms = int(rng.choice([7, 64, 148, 152, 240]))
+        if rng.random() < 0.5:
+            R, H = int(rng.integers(1, 3)), int(rng.choice([8, 16, 64, 128]))
+        else:
+            R, H = int(rng.integers(40, 400)), int(rng.choice([16, 64]))
+        lens = np.maximum(rng.integers(1, 40000, S), R).astype(np.int64)
+        pl = B.tf_paged_mla_plan_info(S, R, H, lens, sms=sms)
+        G = pl["groups"]
+        b = pl["bounds"]
+        if pl["mode"] == 0:
+            tiles = -(-lens // 64)
+            assert b[0] == 0 and b[-1] == tiles.sum() and np.all(np.diff(b) >= 1)
+            assert pl["nranges"] * G == pl["ctas"] <= sms
+            starts = np.concatenate([[0], np.cumsum(tiles)])
+            cut = any(x not in set(starts.tolist()) for x in b[1:-1])
+            assert pl["slots"] == (2 * pl["ctas"] if cut else 0)
+        else:
+            assert pl["mode"] == 1 and G * 4 > sms and pl["work"] == S * G
+            ranges, cuts, total = _unit_ranges(pl, lens, R, H)
+            assert 1 <= pl["ctas"] == pl["nranges"] <= sms
+            assert all(t > 0 for t, _ in ranges) and sum(t for t, _ in ranges) == total
+            assert b[0] == 0 and b[-1] == (S * G) << 32
+            assert pl["slots"] == (2 * pl["ctas"] if cuts else 0)
