@@ -208,10 +208,11 @@ int tf_paged_append(tf_kvpool *pool, int32_t cache, const int32_t *d_pt, int32_t
  * How the keys are shared out decides the order of the fp32 sums, never which keys
  * count; a stream's result never depends on which pool pages hold its rows.
  *  - Default: the key tiles of the batch are cut into near-equal contiguous ranges,
- *    one a CTA (decode, MTP rows), or whole (stream, head group) units go round
- *    robin over the CTAs (prefill chunks).  Every SM gets the same work whatever
- *    the mix of lengths; a stream's bits may differ (within rounding) between
- *    batches, and are identical between calls on the same batch.
+ *    one a CTA (decode, MTP rows), or the (stream, row group) units of a prefill
+ *    chunk, each read only to the last key its rows see, are numbered tile by tile
+ *    and cut the same way.  Every SM gets the same work whatever the mix of lengths;
+ *    a stream's bits may differ (within rounding) between batches, and are identical
+ *    between calls on the same batch.
  *  - Pools made with TF_POOL_BATCH_INVARIANT: each stream's keys are cut into splits
  *    whose bounds depend on that stream's length alone and merged in split order,
  *    as the pages' engine does with its fixed key chunks, so a stream attended in a
